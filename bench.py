@@ -1,0 +1,446 @@
+"""Benchmark of one MLA decode step on B300.
+
+A step is the whole hot path over one batch: append the new token's cache row
+(S1), absorb the query (S2), latent split-KV attention (S3) and the W_UV / W_O
+expansion (S4/S5), for the DeepSeek-V2-shaped layer (d=5120, n_h=128, d_h=128,
+d_c=512, d_r=64, d_cq=1536, bf16) at batch 64 with 4096 cached tokens per
+sequence. Inputs are synthetic (h ~ N(0,1), W ~ N(0, 1/fan_in), seeded) and
+resident in HBM; the cache (302 MB) and weights (298 MB) exceed the 126 MB L2,
+so no flush is needed between steps.
+
+    python bench.py [--steps K] [--warmup W] [--gpus N] [--impl ours|reference]
+
+Under torchrun each rank runs its own batch on its own GPU (weak scaling: the
+sequences of a decode batch are independent, so no collective touches the data
+path); rank 0 prints one JSON line with the max-over-ranks time.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "MLA decode tokens/s and latent-cache GB/s (fraction of roofline), 1×B300"
+NOMINAL_HBM_GBS = 8000.0
+FALLBACK_PEAKS = {"hbm_gbs": 6400.0, "bf16_tflops": 1800.0, "bf16_tflops_sustained": 1400.0}
+
+
+def load_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            d = json.load(f)
+        return d, "measured"
+    return dict(FALLBACK_PEAKS), "fallback"
+
+
+def kernel_source_hash() -> str:
+    h = hashlib.sha256()
+    csrc = os.path.join(ROOT, "head_latent_attention_24_b300", "csrc")
+    for n in sorted(os.listdir(csrc)):
+        if n.startswith("decode"):
+            with open(os.path.join(csrc, n), "rb") as f:
+                h.update(n.encode() + f.read())
+    return h.hexdigest()[:16]
+
+
+def committed_traffic(kernel_hash: str):
+    """DRAM bytes per launch of the attention kernel from the committed ncu
+    summary, if it was taken on the current kernel sources."""
+    p = os.path.join(ROOT, "profiles", "decode_attn_v2_traffic.json")
+    if not os.path.exists(p):
+        return None
+    with open(p) as f:
+        d = json.load(f)
+    if d.get("source_hash") != kernel_hash:
+        return None
+    return d.get("dram_bytes_per_launch")
+
+
+class ClockSampler:
+    """nvidia-smi samples of SM clock and throttle reasons during the timed region."""
+    Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+         "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+         "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.lines = []
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.Q}",
+                                          "--format=csv,noheader,nounits", "-lms", "100"],
+                                         stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.t = threading.Thread(target=self._read, daemon=True)
+            self.t.start()
+        except Exception:
+            self.proc = None
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        sm, smax, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.lines:
+            f = [x.strip() for x in ln.split(",")]
+            if len(f) < 9:
+                continue
+            try:
+                sm.append(float(f[1]))
+                smax.append(float(f[2]))
+            except ValueError:
+                continue
+            for n, v in zip(names, f[5:9]):
+                if v.lower() == "active":
+                    reasons.add(n)
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(smax) if smax else None,
+                "samples": len(sm), "reasons": sorted(reasons)}
+
+
+# --------------------------------------------------------------------------- workload
+def v2_shape():
+    import mla_synth as S
+    return S.workload("v2")
+
+
+def make_inputs(shp, device, seed_offset=0):
+    """Weights, context and new-token inputs on the device (seeded torch generator)."""
+    import torch
+    import mla_synth as S
+    g = torch.Generator(device=device)
+    g.manual_seed(shp.seed * 7919 + seed_offset)
+    W = {}
+    for name in S.WEIGHT_NAMES:
+        r, c = shp.weight_shape(name)
+        W[name] = (torch.randn((r, c), generator=g, device=device) * (1.0 / shp.fan_in(name)) ** 0.5).to(
+            torch.bfloat16).contiguous()
+    B, ctx = shp.batch, shp.ctx
+    h_new = torch.randn((B, shp.d), generator=g, device=device).to(torch.bfloat16).contiguous()
+    return W, h_new
+
+
+def build_cache(dec, shp, cache, device, rank=0):
+    """Append every context token (positions 0..ctx-1 of each sequence) through
+    mla_append_cache, in chunks; h of the context drawn per sequence."""
+    import torch
+    import mla_synth as S
+    B, ctx = shp.batch, shp.ctx
+    per = max(1, 32768 // ctx)
+    for b0 in range(0, B, per):
+        bs = list(range(b0, min(B, b0 + per)))
+        x = torch.cat([S.context_h_device(shp, b + 1000 * rank, ctx, device) for b in bs], 0).contiguous()
+        seq = torch.tensor(np.repeat(bs, ctx), dtype=torch.int32, device=device)
+        pos = torch.tensor(np.tile(np.arange(ctx), len(bs)), dtype=torch.int32, device=device)
+        dec.append(x, seq, pos, cache)
+    torch.cuda.synchronize()
+
+
+def oracle_sample(shp, W_dev, cache_h_fn, h_new_dev, budget_s=12.0, max_seqs=8):
+    """Time the fp64 oracle's whole step on as many sequences as fit the
+    budget (at least one). Returns (tokens/s, seconds, sequences, threads)."""
+    import torch
+    from oracle import mla as O
+    W = {k: v.double().cpu().numpy() for k, v in W_dev.items()}
+    h_new = h_new_dev.double().cpu().numpy()
+    try:
+        from threadpoolctl import threadpool_info
+        threads = max([i.get("num_threads", 1) for i in threadpool_info()] or [1])
+    except Exception:
+        threads = os.cpu_count()
+    done, spent = 0, 0.0
+    while done < max_seqs and (done == 0 or spent < budget_s):
+        b = done
+        h_ctx = cache_h_fn(b)
+        t0 = time.perf_counter()
+        O.decode_materialised([h_ctx], h_new[b:b + 1], W, shp.n_h, shp.d_h, shp.d_r, shp.rope_base)
+        spent += time.perf_counter() - t0
+        done += 1
+    return done / spent, spent, done, threads
+
+
+# --------------------------------------------------------------------------- arms
+def run_ours(args, rank, world, local_rank):
+    import torch
+    import head_latent_attention_24_b300 as M
+    import mla_synth as S
+
+    device = torch.device("cuda", local_rank)
+    torch.cuda.set_device(device)
+    shp = v2_shape()
+    B, ctx = shp.batch, shp.ctx
+    max_len = ctx + 1
+    W, h_new = make_inputs(shp, device, seed_offset=rank)
+    ls = M.LayerShape(shp.d, shp.n_h, shp.d_h, shp.d_c, shp.d_r, shp.d_cq, "bf16", shp.rope_base)
+    dec = M.MLADecoder(ls, W, B, max_len, max_pos=max_len)
+    if args.decode_path != "auto":
+        M.mla_set_decode_path(dec.handle, {"simt": M.MLA_DECODE_SIMT, "tc": M.MLA_DECODE_TCGEN05}[args.decode_path])
+    path = M.mla_get_decode_path(dec.handle)
+    cache = torch.zeros((B, max_len, shp.D), dtype=torch.bfloat16, device=device)
+    build_cache(dec, shp, cache, device, rank)
+    pos = torch.full((B,), ctx, dtype=torch.int32, device=device)
+    seqlens = pos + 1
+    stream = torch.cuda.current_stream()
+
+    def step(evs=None):
+        if evs is None:
+            return dec.step(h_new, pos, cache, seqlens)
+        evs[0].record(stream)
+        M.mla_append_cache(dec.handle, h_new, B, dec.W["W_DKV"], dec.W["W_KR"], dec.tok_seq, pos, cache, B, max_len)
+        n = M.mla_last_launch_count(dec.handle)
+        M.mla_absorb_q(dec.handle, h_new, B, dec.W["W_DQ"], dec.W["W_UQ"], dec.W["W_QR"], dec.W["W_UK"], pos,
+                       dec.q_abs, dec.ws, dec.ws.numel())
+        n += M.mla_last_launch_count(dec.handle)
+        evs[1].record(stream)
+        M.mla_decode_attn(dec.handle, dec.q_abs, cache, B, max_len, seqlens, dec.o_lat, dec.lse, dec.ws,
+                          dec.ws.numel())
+        n += M.mla_last_launch_count(dec.handle)
+        evs[2].record(stream)
+        M.mla_out_proj(dec.handle, dec.o_lat, B, dec.W["W_UV"], dec.W["W_O"], dec.u, dec.ws, dec.ws.numel())
+        n += M.mla_last_launch_count(dec.handle)
+        evs[3].record(stream)
+        return n
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize()
+    st, bits = M.mla_get_device_status(dec.handle)
+    if st != M.MLA_OK:
+        raise RuntimeError(f"device status after warm-up: {st} bits={bits}")
+
+    dist = None
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+    torch.cuda.synchronize()
+    sampler = ClockSampler(local_rank)
+    sampler.start()
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(args.steps)]
+    launches = 0
+    start = torch.cuda.Event(enable_timing=True)
+    end = torch.cuda.Event(enable_timing=True)
+    start.record(stream)
+    for k in range(args.steps):
+        launches += step(evs[k])
+    end.record(stream)
+    torch.cuda.synchronize()
+    if world > 1:
+        dist.barrier()
+    clocks = sampler.stop()
+    total_ms = start.elapsed_time(end)
+    attn_ms = [e[1].elapsed_time(e[2]) for e in evs]
+    step_ms = [e[0].elapsed_time(e[3]) for e in evs]
+    if world > 1:
+        t = torch.tensor([total_ms], device=device)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        total_ms = float(t.item())
+
+    # ---- end to end through the public API: pinned host in, host out, every step
+    h_host = torch.empty_like(h_new, device="cpu").pin_memory()
+    h_host.copy_(h_new)
+    pos_host = pos.cpu().pin_memory()
+    sl_host = seqlens.cpu().pin_memory()
+    u_host = torch.empty_like(dec.u, device="cpu").pin_memory()
+    h_dev = torch.empty_like(h_new)
+    pos_dev = torch.empty_like(pos)
+    sl_dev = torch.empty_like(seqlens)
+    if world > 1:
+        dist.barrier()
+    torch.cuda.synchronize()
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        h_dev.copy_(h_host, non_blocking=True)
+        pos_dev.copy_(pos_host, non_blocking=True)
+        sl_dev.copy_(sl_host, non_blocking=True)
+        u = dec.step(h_dev, pos_dev, cache, sl_dev)
+        u_host.copy_(u, non_blocking=True)
+        stream.synchronize()
+    e2e_s = time.perf_counter() - t0
+    if world > 1:
+        t = torch.tensor([e2e_s], device=device)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        e2e_s = float(t.item())
+
+    st, bits = M.mla_get_device_status(dec.handle)
+    if st != M.MLA_OK:
+        raise RuntimeError(f"device status after timing: {st} bits={bits}")
+
+    if rank != 0:
+        return None
+
+    peaks, peaks_src = load_peaks()
+    cache_bytes = B * max_len * shp.D * 2
+    flops = 2.0 * B * max_len * shp.n_h * (shp.D + shp.d_c)
+    attn_s = statistics.mean(attn_ms) / 1e3
+    achieved_gbs = cache_bytes / attn_s / 1e9
+    achieved_tf = flops / attn_s / 1e12
+    hbm = peaks["hbm_gbs"]
+    kh = kernel_source_hash()
+    traffic = committed_traffic(kh)
+    tokens = B * world * args.steps
+    value = tokens / (total_ms / 1e3)
+    weight_bytes = sum(v.numel() * 2 for v in W.values())
+    step_roof_s = max((cache_bytes + weight_bytes) / (hbm * 1e9),
+                      (flops + 2.0 * B * sum(v.numel() for v in W.values())) / (peaks["bf16_tflops"] * 1e12))
+    out = {
+        "metric": METRIC,
+        "value": round(value, 1),
+        "unit": "tokens/s",
+        "n_gpus": world,
+        "steps": args.steps,
+        "warmup": args.warmup,
+        "ms_per_step": round(total_ms / args.steps, 4),
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "bf16",
+        "data": "synthetic (seeded: h ~ N(0,1), W ~ N(0,1/fan_in), cache built by mla_append_cache)",
+        "config": {
+            "workload": "DeepSeek-V2-shaped MLA decode: d=5120, n_h=128, d_h=128, d_c=512, d_r=64, d_cq=1536; "
+                        "batch 64 per GPU, context 4096 (+1 new token), bf16",
+            "batch_per_gpu": B, "context": ctx, "global_batch": B * world,
+            "l2": "no flush: inputs larger than L2 (cache 302 MB + weights 298 MB > 126 MB)",
+            "decode_path": {M.MLA_DECODE_SIMT: "simt", M.MLA_DECODE_TCGEN05: "tcgen05"}[path],
+        },
+        "roofline": {
+            "kernel": "mla_decode_attn (split plan + split-KV latent attention + LSE combine)",
+            "bound": "hbm",
+            "achieved": round(achieved_gbs, 1),
+            "peak": hbm,
+            "unit": "GB/s",
+            "frac": round(achieved_gbs / hbm, 4),
+            "traffic": traffic,
+            "peak_source": f"{peaks_src} hbm_gbs",
+            "algorithmic_bytes_per_launch": cache_bytes,
+            "launch_us": round(attn_s * 1e6, 2),
+            "frac_of_nominal_8TBps": round(achieved_gbs / NOMINAL_HBM_GBS, 4),
+            "tensor_tflops": round(achieved_tf, 1),
+            "tensor_frac_of_burst": round(achieved_tf / peaks["bf16_tflops"], 4),
+        },
+        "step_roofline_frac": round(step_roof_s / (total_ms / 1e3 / args.steps), 4),
+        "e2e": {
+            "value": round(tokens / e2e_s, 1),
+            "unit": "tokens/s",
+            "h2d_bytes_per_step": h_new.numel() * 2 + pos.numel() * 4 + seqlens.numel() * 4,
+            "d2h_bytes_per_step": dec.u.numel() * 2,
+        },
+        "gpu_launches": launches,
+        "clocks": clocks,
+        "kernel_source_hash": kh,
+        "step_ms_median": round(statistics.median(step_ms), 4),
+    }
+    if world == 1 and not args.no_cpu_baseline:
+        import mla_synth as S
+
+        def ctx_h(b):
+            return S.context_h_device(shp, b, ctx, device).double().cpu().numpy()
+
+        v, spent, nseq, threads = oracle_sample(shp, W, ctx_h, h_new, budget_s=args.cpu_budget)
+        out["cpu_baseline"] = {"value": round(v, 4), "unit": "tokens/s", "cores": threads, "kind": "oracle",
+                               "host_cpus": os.cpu_count(),
+                               "sample": f"{nseq} of the {B} sequences (one decode token each, full 4097-row "
+                                         f"context, fp64 materialised K/V) in {spent:.1f} s"}
+    return out
+
+
+def run_reference(args, rank, world):
+    """The oracle as it stands, on the host cores, over a bounded sample of the
+    same workload (rank 0 only)."""
+    if rank != 0:
+        return None
+    import torch
+    from oracle import mla as O
+    import mla_synth as S
+    shp = v2_shape()
+    B, ctx = shp.batch, shp.ctx
+    rng_dev = "cuda" if torch.cuda.is_available() else "cpu"
+    W, h_new = make_inputs(shp, rng_dev)
+    Wh = {k: v.double().cpu().numpy() for k, v in W.items()}
+    hn = h_new.double().cpu().numpy()
+    try:
+        from threadpoolctl import threadpool_info
+        threads = max([i.get("num_threads", 1) for i in threadpool_info()] or [1])
+    except Exception:
+        threads = os.cpu_count()
+
+    def one(b):
+        h_ctx = S.context_h_device(shp, b, ctx, rng_dev).double().cpu().numpy()
+        t0 = time.perf_counter()
+        O.decode_materialised([h_ctx], hn[b:b + 1], Wh, shp.n_h, shp.d_h, shp.d_r, shp.rope_base)
+        return time.perf_counter() - t0
+
+    for w in range(min(args.warmup, 1)):
+        one(0)
+    times = [one(k % B) for k in range(max(1, min(args.steps, 3)))]
+    per_seq = statistics.mean(times)
+    value = 1.0 / per_seq
+    return {
+        "impl": "reference",
+        "metric": METRIC, "value": round(value, 4), "unit": "tokens/s", "n_gpus": world, "steps": len(times),
+        "warmup": args.warmup, "ms_per_step": round(per_seq * B * 1e3, 1), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": "DeepSeek-V2-shaped MLA decode: d=5120, n_h=128, d_h=128, d_c=512, d_r=64, "
+                               "d_cq=1536; batch 64, context 4096 (+1), fp64 oracle on host cores",
+                   "batch_per_gpu": B, "context": ctx},
+        "cpu_baseline": {"value": round(value, 4), "unit": "tokens/s", "cores": threads, "kind": "oracle",
+                         "sample": f"{len(times)} sequence(s) of the batch, one decode token each, full context"},
+        "e2e": {"value": round(value, 4), "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=50)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--decode-path", default="auto", choices=["auto", "simt", "tc"])
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-budget", type=float, default=12.0)
+    args = ap.parse_args()
+    if args.warmup < 3 and args.impl == "ours":
+        args.warmup = 3
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local_rank = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1 and args.impl == "ours":
+        import torch
+        import torch.distributed as dist
+        torch.cuda.set_device(local_rank)
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local_rank))
+    if args.impl == "reference":
+        out = run_reference(args, rank, world)
+    else:
+        out = run_ours(args, rank, world, local_rank)
+    if out is not None:
+        print(json.dumps(out), flush=True)
+    if world > 1 and args.impl == "ours":
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,89 @@
+// Internal declarations shared by the library's translation units.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <cuda_bf16.h>
+#include <stdint.h>
+#include <stddef.h>
+
+#include "../../include/mla.h"
+
+struct mla_handle_s {
+  mla_config_t cfg;
+  int device;
+  int num_sms;
+  float scale;             // 1/sqrt(d_h + d_r), rounded to fp32
+  float* rope_cos;         // device [max_pos, d_r/2]
+  float* rope_sin;         // device [max_pos, d_r/2]
+  int32_t* status;         // device status word
+  int32_t decode_path;     // mla_decode_path_t requested
+  int32_t last_launches;   // launches made by the last successful call
+};
+
+namespace mla {
+
+// ---------------------------------------------------------------- helpers
+__device__ __forceinline__ float to_f32(float x) { return x; }
+__device__ __forceinline__ float to_f32(__nv_bfloat16 x) { return __bfloat162float(x); }
+template <typename T> __device__ __forceinline__ T from_f32(float x);
+template <> __device__ __forceinline__ float from_f32<float>(float x) { return x; }
+template <> __device__ __forceinline__ __nv_bfloat16 from_f32<__nv_bfloat16>(float x) {
+  return __float2bfloat16_rn(x);
+}
+
+inline size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
+
+// ------------------------------------------------------------- CUDA-core GEMM
+// out[n, map(m)] = epilogue( sum_k X[n, k] * W'[m, k] ) for n < N, m < M, batch z.
+// W'[m, k] = W[m*ldw + k] (W_NORMAL) or W[k*ldw + m] (W_TRANSPOSED).
+enum WLayout { W_NORMAL = 0, W_TRANSPOSED = 1 };
+enum Epilogue {
+  EPI_STORE = 0,      // out[n*ldo + m]
+  EPI_ROPE_SEGS = 1,  // columns form segments of width d_r; RoPE at pos[n];
+                      // out[n*ldo + (m/d_r)*seg_stride + seg_off + m%d_r]
+  EPI_APPEND = 2,     // cache row (tok_seq[n], tok_pos[n]); columns >= d_c get RoPE
+};
+
+struct GemmArgs {
+  const void* X; long long ldx, bx;       // per-batch element offsets
+  const void* W; long long ldw, bw; int wlayout;
+  void* out; long long ldo, bo;
+  int N, M, K, batch;
+  int epi;
+  // RoPE
+  const float* rope_cos; const float* rope_sin; int d_r; int max_pos;
+  const int32_t* pos;          // EPI_ROPE_SEGS: position of row n
+  long long seg_stride; int seg_off;
+  // append
+  const int32_t* tok_seq; const int32_t* tok_pos; int cache_batch; int max_len; int d_c; int row_width;
+  int32_t* status;
+};
+
+cudaError_t launch_gemm_simt(const GemmArgs& a, int dtype, cudaStream_t s);
+
+// --------------------------------------------------------- decode attention
+struct DecodeArgs {
+  const void* q_abs; const void* cache; const int32_t* seqlens;
+  void* o_lat; float* lse;
+  int B, max_len, n_h, d_c, d_r;
+  float scale_log2;            // scale * log2(e)
+  // workspace carve-up
+  int32_t* plan;               // [B+1] cumulative lengths, then [chunk_len, total]
+  float* part_o;               // [slots, n_h, d_c]
+  float* part_lse;             // [slots, n_h]  (natural log)
+  int grid_chunks;             // number of token chunks (CTAs along x)
+  int32_t* status;
+};
+
+// Workspace layout for decode: plan | partial O | partial LSE.
+size_t decode_ws_bytes(int B, int n_h, int d_c, int chunks);
+void decode_ws_carve(void* ws, int B, int n_h, int d_c, int chunks,
+                     int32_t** plan, float** part_o, float** part_lse);
+int decode_simt_chunks(const mla_handle_s* h);
+
+cudaError_t launch_decode_plan(const int32_t* seqlens, int B, int max_len, int chunks, int granule,
+                               int32_t* plan, int32_t* status, cudaStream_t s);
+cudaError_t launch_decode_simt(const DecodeArgs& a, int dtype, cudaStream_t s, int* launches);
+cudaError_t launch_decode_combine(const DecodeArgs& a, int dtype, cudaStream_t s);
+
+}  // namespace mla

@@ -1,0 +1,331 @@
+// C ABI of the MLA decode library: argument checks, handle state, and the
+// launches behind each entry point. See include/mla.h for the contract.
+#include <math.h>
+#include <stdlib.h>
+#include <string.h>
+#include <vector>
+
+#include "internal.cuh"
+#include "decode_tc.cuh"
+
+using namespace mla;
+
+namespace {
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+bool on_handle_device(const mla_handle_s* h) {
+  int dev = -1;
+  if (cudaGetDevice(&dev) != cudaSuccess) return false;
+  return dev == h->device;
+}
+
+size_t esize(const mla_handle_s* h) { return h->cfg.dtype == MLA_BF16 ? 2 : 4; }
+
+int resolve_decode_path(const mla_handle_s* h) {
+  if (h->decode_path == MLA_DECODE_SIMT) return MLA_DECODE_SIMT;
+  const bool tc_ok = decode_tc_supported(h);
+  if (h->decode_path == MLA_DECODE_TCGEN05) return tc_ok ? MLA_DECODE_TCGEN05 : -1;
+  return tc_ok ? MLA_DECODE_TCGEN05 : MLA_DECODE_SIMT;
+}
+
+}  // namespace
+
+extern "C" {
+
+int32_t mla_abi_version(void) { return MLA_ABI_VERSION; }
+
+const char* mla_status_string(int32_t s) {
+  switch (s) {
+    case MLA_OK: return "MLA_OK";
+    case MLA_ERR_INVALID_ARG: return "MLA_ERR_INVALID_ARG: bad pointer, size, alignment or shape";
+    case MLA_ERR_UNSUPPORTED: return "MLA_ERR_UNSUPPORTED: no kernel for this shape";
+    case MLA_ERR_CUDA: return "MLA_ERR_CUDA: a CUDA call failed";
+    case MLA_ERR_DEVICE: return "MLA_ERR_DEVICE: a kernel met out-of-range input (see status bits)";
+    case MLA_ERR_TIMEOUT: return "MLA_ERR_TIMEOUT: a bounded wait inside a kernel expired";
+    case MLA_ERR_WORKSPACE: return "MLA_ERR_WORKSPACE: workspace missing or too small";
+    default: return "unknown mla_status_t";
+  }
+}
+
+mla_status_t mla_create(const mla_config_t* cfg, mla_handle_t* out) {
+  if (!cfg || !out) return MLA_ERR_INVALID_ARG;
+  *out = nullptr;
+  const mla_config_t c = *cfg;
+  if (c.d <= 0 || c.n_h <= 0 || c.d_h <= 0 || c.d_c <= 0 || c.d_r <= 0 || c.d_cq <= 0 || c.max_pos <= 0)
+    return MLA_ERR_INVALID_ARG;
+  if (c.dtype != MLA_BF16 && c.dtype != MLA_F32) return MLA_ERR_INVALID_ARG;
+  if ((c.d_r & 1) || (c.d_c % 8) || (c.d_r % 8) || (c.d % 8) || (c.d_cq % 8) || (c.d_h % 8))
+    return MLA_ERR_INVALID_ARG;
+  if (!(c.rope_base > 1.0) || !isfinite(c.rope_base)) return MLA_ERR_INVALID_ARG;
+  if ((long long)c.max_pos * (c.d_r / 2) > (1LL << 31)) return MLA_ERR_INVALID_ARG;
+
+  int dev = 0, sms = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return MLA_ERR_CUDA;
+  if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return MLA_ERR_CUDA;
+
+  mla_handle_s* h = static_cast<mla_handle_s*>(calloc(1, sizeof(mla_handle_s)));
+  if (!h) return MLA_ERR_CUDA;
+  h->cfg = c;
+  h->device = dev;
+  h->num_sms = sms;
+  h->scale = (float)(1.0 / sqrt((double)(c.d_h + c.d_r)));
+  h->decode_path = MLA_DECODE_AUTO;
+
+  // RoPE table: angle pos * base^(-2j/d_r) in fp64, cos/sin rounded once to fp32.
+  const int half = c.d_r / 2;
+  const size_t n = (size_t)c.max_pos * half;
+  std::vector<float> cs(n), sn(n);
+  std::vector<double> inv(half);
+  for (int j = 0; j < half; ++j) inv[j] = pow(c.rope_base, -2.0 * j / c.d_r);
+  for (int p = 0; p < c.max_pos; ++p)
+    for (int j = 0; j < half; ++j) {
+      const double ang = (double)p * inv[j];
+      cs[(size_t)p * half + j] = (float)cos(ang);
+      sn[(size_t)p * half + j] = (float)sin(ang);
+    }
+  cudaError_t e = cudaMalloc(&h->rope_cos, n * sizeof(float));
+  if (e == cudaSuccess) e = cudaMalloc(&h->rope_sin, n * sizeof(float));
+  if (e == cudaSuccess) e = cudaMalloc(&h->status, sizeof(int32_t));
+  if (e == cudaSuccess) e = cudaMemcpy(h->rope_cos, cs.data(), n * sizeof(float), cudaMemcpyHostToDevice);
+  if (e == cudaSuccess) e = cudaMemcpy(h->rope_sin, sn.data(), n * sizeof(float), cudaMemcpyHostToDevice);
+  if (e == cudaSuccess) e = cudaMemset(h->status, 0, sizeof(int32_t));
+  if (e != cudaSuccess) {
+    cudaFree(h->rope_cos);
+    cudaFree(h->rope_sin);
+    cudaFree(h->status);
+    free(h);
+    return MLA_ERR_CUDA;
+  }
+  *out = h;
+  return MLA_OK;
+}
+
+mla_status_t mla_destroy(mla_handle_t h) {
+  if (!h) return MLA_ERR_INVALID_ARG;
+  cudaDeviceSynchronize();
+  cudaFree(h->rope_cos);
+  cudaFree(h->rope_sin);
+  cudaFree(h->status);
+  free(h);
+  return MLA_OK;
+}
+
+mla_status_t mla_set_decode_path(mla_handle_t h, int32_t path) {
+  if (!h || path < MLA_DECODE_AUTO || path > MLA_DECODE_TCGEN05) return MLA_ERR_INVALID_ARG;
+  if (path == MLA_DECODE_TCGEN05 && !decode_tc_supported(h)) return MLA_ERR_UNSUPPORTED;
+  h->decode_path = path;
+  return MLA_OK;
+}
+
+mla_status_t mla_get_decode_path(mla_handle_t h, int32_t* path) {
+  if (!h || !path) return MLA_ERR_INVALID_ARG;
+  *path = resolve_decode_path(h);
+  return MLA_OK;
+}
+
+mla_status_t mla_last_launch_count(mla_handle_t h, int32_t* launches) {
+  if (!h || !launches) return MLA_ERR_INVALID_ARG;
+  *launches = h->last_launches;
+  return MLA_OK;
+}
+
+mla_status_t mla_get_device_status(mla_handle_t h, void* stream, int32_t* bits) {
+  if (!h || !bits) return MLA_ERR_INVALID_ARG;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  int32_t v = 0;
+  cudaError_t e = cudaStreamSynchronize(s);
+  if (e == cudaSuccess) e = cudaMemcpy(&v, h->status, sizeof(int32_t), cudaMemcpyDeviceToHost);
+  if (e == cudaSuccess) e = cudaMemset(h->status, 0, sizeof(int32_t));
+  if (e != cudaSuccess) return MLA_ERR_CUDA;
+  *bits = v;
+  if (v & ~MLA_DEV_TIMEOUT) return MLA_ERR_DEVICE;
+  if (v & MLA_DEV_TIMEOUT) return MLA_ERR_TIMEOUT;
+  return MLA_OK;
+}
+
+// ------------------------------------------------------------------- S1
+mla_status_t mla_append_cache(mla_handle_t h, const void* x, int32_t n_tokens, const void* W_DKV,
+                              const void* W_KR, const int32_t* tok_seq, const int32_t* tok_pos,
+                              void* cache, int32_t batch, int32_t max_len, void* stream) {
+  if (!h || n_tokens < 0 || batch <= 0 || max_len <= 0) return MLA_ERR_INVALID_ARG;
+  if (n_tokens == 0) { h->last_launches = 0; return MLA_OK; }
+  if (!x || !W_DKV || !W_KR || !tok_seq || !tok_pos || !cache) return MLA_ERR_INVALID_ARG;
+  if (!aligned16(x) || !aligned16(W_DKV) || !aligned16(W_KR) || !aligned16(tok_seq) ||
+      !aligned16(tok_pos) || !aligned16(cache))
+    return MLA_ERR_INVALID_ARG;
+  if (!on_handle_device(h)) return MLA_ERR_INVALID_ARG;
+  const mla_config_t& c = h->cfg;
+  if (c.d_r > 64) return MLA_ERR_UNSUPPORTED;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  const int D = c.d_c + c.d_r;
+  // Two weight blocks, one launch each: c_KV columns then the RoPE columns.
+  // The RoPE launch sees both halves of every rotated pair in one tile.
+  int launches = 0;
+  for (int part = 0; part < 2; ++part) {
+    GemmArgs a{};
+    a.X = x; a.ldx = c.d; a.bx = 0;
+    a.W = part == 0 ? W_DKV : W_KR; a.ldw = c.d; a.bw = 0; a.wlayout = W_NORMAL;
+    a.N = n_tokens; a.M = part == 0 ? c.d_c : c.d_r; a.K = c.d; a.batch = 1;
+    a.epi = EPI_APPEND;
+    a.rope_cos = h->rope_cos; a.rope_sin = h->rope_sin; a.d_r = c.d_r; a.max_pos = c.max_pos;
+    a.tok_seq = tok_seq; a.tok_pos = tok_pos; a.cache_batch = batch; a.max_len = max_len;
+    a.row_width = D; a.status = h->status;
+    // The RoPE block writes at column offset d_c of the row, and every one of
+    // its columns is rotated (threshold 0); its d_r <= 64 columns share one tile.
+    a.d_c = part == 0 ? c.d_c : 0;
+    a.out = part == 0 ? cache : static_cast<char*>(cache) + (size_t)c.d_c * esize(h);
+    cudaError_t e;
+    // Chunk very long token lists so the grid stays within 65535 rows of tiles.
+    const int chunk = 65535 * 64;
+    for (int t0 = 0; t0 < n_tokens; t0 += chunk) {
+      GemmArgs ac = a;
+      ac.N = n_tokens - t0 < chunk ? n_tokens - t0 : chunk;
+      ac.X = static_cast<const char*>(x) + (size_t)t0 * c.d * esize(h);
+      ac.tok_seq = tok_seq + t0;
+      ac.tok_pos = tok_pos + t0;
+      e = launch_gemm_simt(ac, c.dtype, s);
+      if (e != cudaSuccess) return MLA_ERR_CUDA;
+      ++launches;
+    }
+  }
+  h->last_launches = launches;
+  return MLA_OK;
+}
+
+// ------------------------------------------------------------------- S2
+mla_status_t mla_absorb_q_workspace_size(mla_handle_t h, int32_t batch, size_t* bytes) {
+  if (!h || !bytes || batch <= 0) return MLA_ERR_INVALID_ARG;
+  const mla_config_t& c = h->cfg;
+  *bytes = align_up((size_t)batch * c.d_cq * esize(h), 256) +
+           align_up((size_t)batch * c.n_h * c.d_h * esize(h), 256);
+  return MLA_OK;
+}
+
+mla_status_t mla_absorb_q(mla_handle_t h, const void* x, int32_t batch, const void* W_DQ, const void* W_UQ,
+                          const void* W_QR, const void* W_UK, const int32_t* pos, void* q_abs, void* ws,
+                          size_t ws_bytes, void* stream) {
+  if (!h || batch <= 0 || !x || !W_DQ || !W_UQ || !W_QR || !W_UK || !pos || !q_abs) return MLA_ERR_INVALID_ARG;
+  if (!aligned16(x) || !aligned16(W_DQ) || !aligned16(W_UQ) || !aligned16(W_QR) || !aligned16(W_UK) ||
+      !aligned16(pos) || !aligned16(q_abs) || (ws && !aligned16(ws)))
+    return MLA_ERR_INVALID_ARG;
+  size_t need = 0;
+  mla_absorb_q_workspace_size(h, batch, &need);
+  if (!ws || ws_bytes < need) return MLA_ERR_WORKSPACE;
+  if (!on_handle_device(h)) return MLA_ERR_INVALID_ARG;
+  const mla_config_t& c = h->cfg;
+  if (64 % c.d_r != 0) return MLA_ERR_UNSUPPORTED;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  const int D = c.d_c + c.d_r;
+  char* c_q = static_cast<char*>(ws);
+  char* q_c = c_q + align_up((size_t)batch * c.d_cq * esize(h), 256);
+
+  GemmArgs a{};
+  a.batch = 1; a.wlayout = W_NORMAL; a.status = h->status;
+  a.rope_cos = h->rope_cos; a.rope_sin = h->rope_sin; a.d_r = c.d_r; a.max_pos = c.max_pos;
+  // c_Q = W_DQ x
+  a.X = x; a.ldx = c.d; a.W = W_DQ; a.ldw = c.d; a.out = c_q; a.ldo = c.d_cq;
+  a.N = batch; a.M = c.d_cq; a.K = c.d; a.epi = EPI_STORE;
+  if (launch_gemm_simt(a, c.dtype, s) != cudaSuccess) return MLA_ERR_CUDA;
+  // q_C = W_UQ c_Q
+  a.X = c_q; a.ldx = c.d_cq; a.W = W_UQ; a.ldw = c.d_cq; a.out = q_c; a.ldo = (long long)c.n_h * c.d_h;
+  a.M = c.n_h * c.d_h; a.K = c.d_cq;
+  if (launch_gemm_simt(a, c.dtype, s) != cudaSuccess) return MLA_ERR_CUDA;
+  // q_R = RoPE(W_QR c_Q), written to q_abs[b, i, d_c:]
+  a.W = W_QR; a.out = q_abs; a.ldo = (long long)c.n_h * D; a.M = c.n_h * c.d_r;
+  a.epi = EPI_ROPE_SEGS; a.pos = pos; a.seg_stride = D; a.seg_off = c.d_c;
+  if (launch_gemm_simt(a, c.dtype, s) != cudaSuccess) return MLA_ERR_CUDA;
+  // q~_i = W_UK_i^T q_C_i, batched over heads, written to q_abs[b, i, :d_c]
+  GemmArgs t{};
+  t.X = q_c; t.ldx = (long long)c.n_h * c.d_h; t.bx = c.d_h;
+  t.W = W_UK; t.ldw = c.d_c; t.bw = (long long)c.d_h * c.d_c; t.wlayout = W_TRANSPOSED;
+  t.out = q_abs; t.ldo = (long long)c.n_h * D; t.bo = D;
+  t.N = batch; t.M = c.d_c; t.K = c.d_h; t.batch = c.n_h; t.epi = EPI_STORE; t.status = h->status;
+  if (launch_gemm_simt(t, c.dtype, s) != cudaSuccess) return MLA_ERR_CUDA;
+  h->last_launches = 4;
+  return MLA_OK;
+}
+
+// ------------------------------------------------------------------- S3
+mla_status_t mla_decode_workspace_size(mla_handle_t h, int32_t batch, int32_t max_len, size_t* bytes) {
+  if (!h || !bytes || batch <= 0 || max_len <= 0) return MLA_ERR_INVALID_ARG;
+  const mla_config_t& c = h->cfg;
+  size_t b = decode_ws_bytes(batch, c.n_h, c.d_c, decode_simt_chunks(h));
+  if (decode_tc_supported(h)) {
+    const size_t t = decode_ws_bytes(batch, c.n_h, c.d_c, decode_tc_chunks(h, batch));
+    if (t > b) b = t;
+  }
+  *bytes = b;
+  return MLA_OK;
+}
+
+mla_status_t mla_decode_attn(mla_handle_t h, const void* q_abs, const void* cache, int32_t batch, int32_t max_len,
+                             const int32_t* seqlens, void* o_lat, float* lse, void* ws, size_t ws_bytes,
+                             void* stream) {
+  if (!h || batch <= 0 || max_len <= 0 || !q_abs || !cache || !seqlens || !o_lat || !lse)
+    return MLA_ERR_INVALID_ARG;
+  if (!aligned16(q_abs) || !aligned16(cache) || !aligned16(seqlens) || !aligned16(o_lat) || !aligned16(lse) ||
+      (ws && !aligned16(ws)))
+    return MLA_ERR_INVALID_ARG;
+  const mla_config_t& c = h->cfg;
+  if ((long long)batch * max_len >= (1LL << 31)) return MLA_ERR_INVALID_ARG;
+  size_t need = 0;
+  mla_decode_workspace_size(h, batch, max_len, &need);
+  if (!ws || ws_bytes < need) return MLA_ERR_WORKSPACE;
+  if (!on_handle_device(h)) return MLA_ERR_INVALID_ARG;
+  const int path = resolve_decode_path(h);
+  if (path < 0) return MLA_ERR_UNSUPPORTED;
+  if (path == MLA_DECODE_SIMT && c.d_c > 512) return MLA_ERR_UNSUPPORTED;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+
+  DecodeArgs a{};
+  a.q_abs = q_abs; a.cache = cache; a.seqlens = seqlens; a.o_lat = o_lat; a.lse = lse;
+  a.B = batch; a.max_len = max_len; a.n_h = c.n_h; a.d_c = c.d_c; a.d_r = c.d_r;
+  a.scale_log2 = h->scale * 1.4426950408889634f;
+  a.status = h->status;
+  a.grid_chunks = path == MLA_DECODE_TCGEN05 ? decode_tc_chunks(h, batch) : decode_simt_chunks(h);
+  decode_ws_carve(ws, batch, c.n_h, c.d_c, a.grid_chunks, &a.plan, &a.part_o, &a.part_lse);
+  int launches = 0;
+  cudaError_t e = path == MLA_DECODE_TCGEN05 ? launch_decode_tc(h, a, s, &launches)
+                                             : launch_decode_simt(a, c.dtype, s, &launches);
+  if (e != cudaSuccess) return MLA_ERR_CUDA;
+  h->last_launches = launches;
+  return MLA_OK;
+}
+
+// ------------------------------------------------------------------- S4/S5
+mla_status_t mla_out_proj_workspace_size(mla_handle_t h, int32_t batch, size_t* bytes) {
+  if (!h || !bytes || batch <= 0) return MLA_ERR_INVALID_ARG;
+  *bytes = align_up((size_t)batch * h->cfg.n_h * h->cfg.d_h * esize(h), 256);
+  return MLA_OK;
+}
+
+mla_status_t mla_out_proj(mla_handle_t h, const void* o_lat, int32_t batch, const void* W_UV, const void* W_O,
+                          void* u, void* ws, size_t ws_bytes, void* stream) {
+  if (!h || batch <= 0 || !o_lat || !W_UV || !W_O || !u) return MLA_ERR_INVALID_ARG;
+  if (!aligned16(o_lat) || !aligned16(W_UV) || !aligned16(W_O) || !aligned16(u) || (ws && !aligned16(ws)))
+    return MLA_ERR_INVALID_ARG;
+  size_t need = 0;
+  mla_out_proj_workspace_size(h, batch, &need);
+  if (!ws || ws_bytes < need) return MLA_ERR_WORKSPACE;
+  if (!on_handle_device(h)) return MLA_ERR_INVALID_ARG;
+  const mla_config_t& c = h->cfg;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  // o_i = W_UV_i o_lat_i, batched over heads
+  GemmArgs a{};
+  a.X = o_lat; a.ldx = (long long)c.n_h * c.d_c; a.bx = c.d_c;
+  a.W = W_UV; a.ldw = c.d_c; a.bw = (long long)c.d_h * c.d_c; a.wlayout = W_NORMAL;
+  a.out = ws; a.ldo = (long long)c.n_h * c.d_h; a.bo = c.d_h;
+  a.N = batch; a.M = c.d_h; a.K = c.d_c; a.batch = c.n_h; a.epi = EPI_STORE; a.status = h->status;
+  if (launch_gemm_simt(a, c.dtype, s) != cudaSuccess) return MLA_ERR_CUDA;
+  // u = W_O o
+  GemmArgs b{};
+  b.X = ws; b.ldx = (long long)c.n_h * c.d_h; b.W = W_O; b.ldw = (long long)c.n_h * c.d_h; b.wlayout = W_NORMAL;
+  b.out = u; b.ldo = c.d; b.N = batch; b.M = c.d; b.K = c.n_h * c.d_h; b.batch = 1; b.epi = EPI_STORE;
+  b.status = h->status;
+  if (launch_gemm_simt(b, c.dtype, s) != cudaSuccess) return MLA_ERR_CUDA;
+  h->last_launches = 2;
+  return MLA_OK;
+}
+
+}  // extern "C"

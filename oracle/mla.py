@@ -209,8 +209,6 @@ def decode_materialised(h_ctx_list, h_new, W, n_h, d_h, d_r, base, pos=None, ret
     if pos is None:
         pos = np.array([len(hc) for hc in h_ctx_list])
     scale = scale_of(d_h, d_r)
-    W_UK = W["W_UK"].reshape(n_h, d_h, d_c)
-    W_UV = W["W_UV"].reshape(n_h, d_h, d_c)
     u = np.zeros((B, d))
     o_all = np.zeros((B, n_h * d_h))
     lse_all = np.zeros((B, n_h))
@@ -219,19 +217,20 @@ def decode_materialised(h_ctx_list, h_new, W, n_h, d_h, d_r, base, pos=None, ret
         toks = np.concatenate([_f64(h_ctx_list[b])[:L], h_new[b:b + 1]], axis=0)   # [L+1, d]
         c_kv = toks @ W["W_DKV"].T                                                     # [L+1, d_c]
         k_r = rope(toks @ W["W_KR"].T, np.arange(L + 1), base)                         # [L+1, d_r]
-        k_c = np.einsum("ikc,tc->itk", W_UK, c_kv)                                     # [n_h, L+1, d_h]
-        v_c = np.einsum("ikc,tc->itk", W_UV, c_kv)                                     # [n_h, L+1, d_h]
+        # k_C = W_UK c_KV and v_C = W_UV c_KV for every row, all heads stacked ([MLA] §3)
+        k_c = (c_kv @ W["W_UK"].T).reshape(L + 1, n_h, d_h).transpose(1, 0, 2)        # [n_h, L+1, d_h]
+        v_c = (c_kv @ W["W_UV"].T).reshape(L + 1, n_h, d_h).transpose(1, 0, 2)        # [n_h, L+1, d_h]
         k = np.concatenate([k_c, np.broadcast_to(k_r, (n_h,) + k_r.shape)], axis=-1)   # [n_h, L+1, d_h+d_r]
         c_q = h_new[b] @ W["W_DQ"].T
         q_c = (W["W_UQ"] @ c_q).reshape(n_h, d_h)
         q_r = rope((W["W_QR"] @ c_q).reshape(n_h, d_r), np.full(n_h, float(L)), base)
         q = np.concatenate([q_c, q_r], axis=-1)                                        # [n_h, d_h+d_r]
-        s = np.einsum("ik,itk->it", q, k) * scale
+        s = np.matmul(k, q[:, :, None])[:, :, 0] * scale                              # [n_h, L+1]
         m = s.max(axis=1, keepdims=True)
         e = np.exp(s - m)
         l = e.sum(axis=1, keepdims=True)
         a = e / l
-        o = np.einsum("it,itk->ik", a, v_c)                                            # [n_h, d_h]
+        o = np.matmul(a[:, None, :], v_c)[:, 0, :]                                     # [n_h, d_h]
         o_all[b] = o.reshape(-1)
         lse_all[b] = (m + np.log(l))[:, 0]
         u[b] = W["W_O"] @ o.reshape(-1)

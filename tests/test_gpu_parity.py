@@ -1,0 +1,306 @@
+"""Parity of every entry point of the CUDA library against the fp64 oracle,
+element by element, on seeded generator inputs (never on another stage's GPU
+output). Sizes span several tiles and ragged tails; the full-size workloads are
+checked on sampled sequences the oracle can compute."""
+import numpy as np
+import pytest
+
+import mla_synth as S
+from oracle import mla as O
+from gpu_helpers import (TOL, TOL_E2E, assert_close, dev, dev_i32, host, make_weights_dev, decoder,
+                         torch_dtype)
+
+pytestmark = pytest.mark.gpu
+
+torch = pytest.importorskip("torch")
+if not torch.cuda.is_available():
+    pytest.skip("needs a CUDA GPU", allow_module_level=True)
+import head_latent_attention_24_b300 as M  # noqa: E402
+
+SMALL = ["tiny", "minimind", "v2"]
+
+
+def small_shape(name, batch=None, ctx=None):
+    shp = S.workload(name)
+    if name == "tiny":
+        return shp
+    return shp.scaled(batch=batch or 3, ctx=ctx or 301)
+
+
+# --------------------------------------------------------------------- S1
+@pytest.mark.parametrize("name", SMALL)
+def test_append_matches_oracle_and_touches_only_its_rows(name):
+    shp = small_shape(name)
+    W = S.draw_weights(shp)
+    B, L = 3, 200
+    rng = np.random.default_rng(1)
+    n = 150
+    flat = rng.choice(B * L, size=n, replace=False)
+    seq, pos = flat // L, flat % L
+    pos[0] = L - 1
+    x = S.draw_context_h(shp, 0, n)
+    dec = decoder(shp, make_weights_dev(shp, W), B, L)
+    cache = torch.full((B, L, shp.D), float("nan"), dtype=torch_dtype(shp), device="cuda")
+    dec.append(dev(x, shp), dev_i32(seq), dev_i32(pos), cache)
+    st, bits = M.mla_get_device_status(dec.handle)
+    assert st == M.MLA_OK and bits == 0
+    got = host(cache)
+    ref = O.cache_rows(x, W["W_DKV"], W["W_KR"], pos, shp.rope_base)
+    assert_close(got[seq, pos], ref, shp.dtype, what="cache rows")
+    untouched = np.ones((B, L), bool)
+    untouched[seq, pos] = False
+    assert np.isnan(got[untouched]).all()
+
+
+@pytest.mark.parametrize("name", SMALL)
+def test_append_bit_exact_on_integer_inputs(name):
+    # Integer h and weights: every product and fp32 sum is exact, so after one
+    # rounding to the storage dtype the cache must equal the oracle bit for bit.
+    # Position 0 makes RoPE the identity; c_KV is exact at any position.
+    shp = small_shape(name)
+    rng = np.random.default_rng(2)
+    W = {k: rng.integers(-3, 4, size=shp.weight_shape(k)).astype(np.float64) for k in S.WEIGHT_NAMES}
+    n, B, L = 40, 4, 16
+    x = rng.integers(-3, 4, size=(n, shp.d)).astype(np.float64)
+    seq = np.arange(n) % B
+    pos = np.where(np.arange(n) < B, 0, 1 + np.arange(n) // B)
+    dec = decoder(shp, make_weights_dev(shp, W), B, L)
+    cache = torch.zeros((B, L, shp.D), dtype=torch_dtype(shp), device="cuda")
+    dec.append(dev(x, shp), dev_i32(seq), dev_i32(pos), cache)
+    got = host(cache)[seq, pos]
+    ref = S.to_dtype(O.cache_rows(x, W["W_DKV"], W["W_KR"], pos, shp.rope_base), shp.dtype)
+    assert np.array_equal(got[:, :shp.d_c], ref[:, :shp.d_c])
+    at0 = pos == 0
+    assert np.array_equal(got[at0], ref[at0])
+
+
+def test_append_out_of_range_rows_are_skipped_and_flagged():
+    shp = S.workload("tiny")
+    W = S.draw_weights(shp)
+    B, L = 2, 8
+    x = S.draw_context_h(shp, 0, 4)
+    dec = decoder(shp, make_weights_dev(shp, W), B, L)
+    cache = torch.zeros((B, L, shp.D), dtype=torch_dtype(shp), device="cuda")
+    dec.append(dev(x, shp), dev_i32([0, 5, 1, 0]), dev_i32([0, 1, 9, -1]), cache)
+    st, bits = M.mla_get_device_status(dec.handle)
+    assert st == M.MLA_ERR_DEVICE
+    assert bits & M.MLA_DEV_SEQ_RANGE and bits & M.MLA_DEV_POS_RANGE
+    got = host(cache)
+    ref = O.cache_rows(x[:1], W["W_DKV"], W["W_KR"], [0], shp.rope_base)
+    assert_close(got[0, 0:1], ref, shp.dtype)
+    got[0, 0] = 0
+    assert np.all(got == 0)
+    assert M.mla_get_device_status(dec.handle) == (M.MLA_OK, 0)   # cleared by the read
+
+
+# --------------------------------------------------------------------- S2
+@pytest.mark.parametrize("name", SMALL)
+def test_absorb_q_matches_oracle(name):
+    shp = small_shape(name)
+    W = S.draw_weights(shp)
+    B = 37 if name != "tiny" else 2
+    h = S.draw_new_tokens(shp, B)
+    max_pos = 5000
+    pos = np.random.default_rng(3).integers(0, max_pos, size=B)
+    pos[0], pos[-1] = 0, max_pos - 1
+    dec = decoder(shp, make_weights_dev(shp, W), B, 16, max_pos=max_pos)
+    M.mla_absorb_q(dec.handle, dev(h, shp), B, dec.W["W_DQ"], dec.W["W_UQ"], dec.W["W_QR"], dec.W["W_UK"],
+                   dev_i32(pos), dec.q_abs, dec.ws, dec.ws.numel())
+    ref = O.absorbed_query(h, W["W_DQ"], W["W_UQ"], W["W_QR"], W["W_UK"], pos, shp.n_h, shp.d_h, shp.d_r,
+                           shp.rope_base)
+    got = host(dec.q_abs)
+    assert_close(got, ref, shp.dtype, what="q_abs")
+    assert M.mla_get_device_status(dec.handle) == (M.MLA_OK, 0)
+
+
+# --------------------------------------------------------------------- S3
+def run_decode(shp, q_abs, rows_per_seq, seqlens, max_len, path=None):
+    B = len(seqlens)
+    cache = np.zeros((B, max_len, shp.D))
+    for b, r in enumerate(rows_per_seq):
+        cache[b, :len(r)] = r
+    W = {k: np.zeros(shp.weight_shape(k)) for k in S.WEIGHT_NAMES}
+    dec = decoder(shp, {k: torch.zeros(1, device="cuda") for k in W}, B, max_len)
+    if path is not None:
+        M.mla_set_decode_path(dec.handle, path)
+    M.mla_decode_attn(dec.handle, dev(q_abs, shp), dev(cache, shp), B, max_len, dev_i32(seqlens), dec.o_lat,
+                      dec.lse, dec.ws, dec.ws.numel())
+    st, bits = M.mla_get_device_status(dec.handle)
+    return host(dec.o_lat), dec.lse.cpu().numpy().astype(np.float64), st, bits, dec
+
+
+def oracle_decode(shp, q_abs, rows_per_seq, seqlens):
+    sc = O.scale_of(shp.d_h, shp.d_r)
+    outs = [O.latent_attention(q_abs[b], rows_per_seq[b][:seqlens[b]], shp.d_c, sc) for b in range(len(seqlens))]
+    return np.stack([o for o, _ in outs]), np.stack([l for _, l in outs])
+
+
+SEQLEN_PATTERNS = {
+    "uniform": lambda rng, L: np.full(5, L),
+    "ragged": lambda rng, L: np.array([1, L, 0, 33, L // 2 + 7, 64, 65, 2]),
+}
+
+
+def paths():
+    return [None, M.MLA_DECODE_SIMT]
+
+
+@pytest.mark.parametrize("name", SMALL)
+@pytest.mark.parametrize("pattern", list(SEQLEN_PATTERNS))
+def test_decode_attn_matches_oracle(name, pattern):
+    shp = S.workload(name)
+    max_len = 301 if name != "tiny" else 129
+    seqlens = SEQLEN_PATTERNS[pattern](np.random.default_rng(4), max_len)
+    B = len(seqlens)
+    q = S.draw_absorbed_queries(shp, B)
+    rows = [S.draw_latent_rows(shp, int(seqlens[b]), sub=b) for b in range(B)]
+    ref_o, ref_l = oracle_decode(shp, q, rows, seqlens)
+    got_o, got_l, st, bits, _ = run_decode(shp, q, rows, seqlens, max_len)
+    assert st == M.MLA_OK and bits == 0
+    nz = seqlens > 0
+    assert_close(got_o[nz], ref_o[nz], shp.dtype, what="o_lat")
+    assert np.all(got_o[~nz] == 0) and np.all(np.isneginf(got_l[~nz]))
+    assert np.abs(got_l[nz] - ref_l[nz]).max() <= (2e-5 if shp.dtype == "f32" else 2e-4) * max(1, np.abs(ref_l[nz]).max())
+
+
+@pytest.mark.parametrize("name", SMALL)
+def test_decode_attn_special_cases(name):
+    shp = S.workload(name)
+    max_len = 97
+    B = 3
+    q = S.draw_absorbed_queries(shp, B)
+    one = S.draw_latent_rows(shp, 1, sub=7)
+    same = np.tile(S.draw_latent_rows(shp, 1, sub=8), (max_len, 1))
+    rows = [one, same, S.draw_latent_rows(shp, max_len, sub=9)]
+    q[2] = 0.0
+    seqlens = np.array([1, max_len, max_len])
+    got_o, got_l, st, bits, _ = run_decode(shp, q, rows, seqlens, max_len)
+    sc = O.scale_of(shp.d_h, shp.d_r)
+    # seqlen 1: the only row's latent, exactly; lse = its score
+    assert np.array_equal(got_o[0], np.broadcast_to(one[0, :shp.d_c], (shp.n_h, shp.d_c)))
+    assert np.allclose(got_l[0], sc * q[0] @ one[0], rtol=1e-5, atol=1e-5)
+    # all rows equal: that row. Exact for bf16 storage (the fp32 result rounds
+    # back onto the row's bf16 values); for fp32 storage a sequence split
+    # across chunks is merged by weights that sum to one only up to fp32 rounding.
+    want = np.broadcast_to(same[0, :shp.d_c], (shp.n_h, shp.d_c))
+    if shp.dtype == "bf16":
+        assert np.array_equal(got_o[1], want)
+    else:
+        assert np.allclose(got_o[1], want, rtol=4e-7, atol=0)
+    # q = 0: the mean of the rows, lse = log(L)
+    assert_close(got_o[2], np.broadcast_to(rows[2][:, :shp.d_c].mean(0), (shp.n_h, shp.d_c)), shp.dtype)
+    assert np.allclose(got_l[2], np.log(max_len), rtol=1e-6)
+
+
+def test_decode_attn_clamps_and_flags_bad_seqlens():
+    shp = S.workload("minimind")
+    max_len = 50
+    q = S.draw_absorbed_queries(shp, 2)
+    rows = [S.draw_latent_rows(shp, max_len, sub=b) for b in range(2)]
+    got_o, got_l, st, bits, _ = run_decode(shp, q, rows, np.array([max_len + 9, -3]), max_len)
+    assert st == M.MLA_ERR_DEVICE and bits & M.MLA_DEV_SEQLEN_RANGE
+    ref_o, ref_l = oracle_decode(shp, q, rows, np.array([max_len, 0]))
+    assert_close(got_o[0], ref_o[0], shp.dtype)
+    assert np.all(got_o[1] == 0) and np.isneginf(got_l[1]).all()
+
+
+def test_decode_attn_paths_agree():
+    shp = S.workload("v2")
+    max_len = 700
+    seqlens = np.array([700, 129, 1, 640])
+    q = S.draw_absorbed_queries(shp, 4)
+    rows = [S.draw_latent_rows(shp, int(n), sub=b) for b, n in enumerate(seqlens)]
+    a = run_decode(shp, q, rows, seqlens, max_len, path=M.MLA_DECODE_SIMT)
+    b = run_decode(shp, q, rows, seqlens, max_len, path=M.MLA_DECODE_AUTO)
+    assert_close(b[0], a[0], "bf16")
+
+
+def test_workspace_and_alignment_errors():
+    shp = S.workload("tiny")
+    q = S.draw_absorbed_queries(shp, 2)
+    rows = [S.draw_latent_rows(shp, 10, sub=b) for b in range(2)]
+    _, _, _, _, dec = run_decode(shp, q, rows, np.array([10, 10]), 10)
+    qd, cd = dev(q, shp), torch.zeros((2, 10, shp.D), dtype=torch.float32, device="cuda")
+    sl = dev_i32([10, 10])
+    with pytest.raises(M.MLAError) as e:
+        M.mla_decode_attn(dec.handle, qd, cd, 2, 10, sl, dec.o_lat, dec.lse, dec.ws, 16)
+    assert e.value.status == M.MLA_ERR_WORKSPACE
+    with pytest.raises(M.MLAError) as e:
+        M.mla_decode_attn(dec.handle, qd.data_ptr() + 4, cd, 2, 10, sl, dec.o_lat, dec.lse, dec.ws, dec.ws.numel())
+    assert e.value.status == M.MLA_ERR_INVALID_ARG
+
+
+# --------------------------------------------------------------------- S4/S5
+@pytest.mark.parametrize("name", SMALL)
+def test_out_proj_matches_oracle(name):
+    shp = small_shape(name)
+    W = S.draw_weights(shp)
+    B = 19 if name != "tiny" else 2
+    o_lat = S.to_dtype(S.draw_latent_rows(shp, B * shp.n_h, sub=11)[:, :shp.d_c].reshape(B, shp.n_h, shp.d_c)
+                       / 8.0, shp.dtype)
+    dec = decoder(shp, make_weights_dev(shp, W), B, 16)
+    M.mla_out_proj(dec.handle, dev(o_lat, shp), B, dec.W["W_UV"], dec.W["W_O"], dec.u, dec.ws, dec.ws.numel())
+    ref = O.output_projection(o_lat, W["W_UV"], W["W_O"], shp.n_h, shp.d_h)
+    assert_close(host(dec.u), ref, shp.dtype, what="u")
+
+
+# --------------------------------------------------------------------- whole step
+def end_to_end(shp, ctx_lens):
+    B = len(ctx_lens)
+    W = S.draw_weights(shp)
+    h_ctx = [S.draw_context_h(shp, b, int(n)) for b, n in enumerate(ctx_lens)]
+    h_new = S.draw_new_tokens(shp, B)
+    max_len = int(max(ctx_lens)) + 1
+    dec = decoder(shp, make_weights_dev(shp, W), B, max_len)
+    cache = torch.zeros((B, max_len, shp.D), dtype=torch_dtype(shp), device="cuda")
+    seq = np.concatenate([np.full(int(n), b) for b, n in enumerate(ctx_lens)])
+    pos = np.concatenate([np.arange(int(n)) for n in ctx_lens])
+    if len(seq):
+        dec.append(dev(np.concatenate(h_ctx), shp), dev_i32(seq), dev_i32(pos), cache)
+    u = dec.step(dev(h_new, shp), dev_i32(ctx_lens), cache, dev_i32(np.asarray(ctx_lens) + 1))
+    st, bits = M.mla_get_device_status(dec.handle)
+    assert st == M.MLA_OK and bits == 0
+    ref_u = O.decode_materialised(h_ctx, h_new, W, shp.n_h, shp.d_h, shp.d_r, shp.rope_base)
+    _, ref_o, ref_l, _, _ = O.decode_absorbed(h_ctx, h_new, W, shp.n_h, shp.d_h, shp.d_r, shp.rope_base)
+    return host(u), ref_u, host(dec.o_lat), ref_o, dec.lse.cpu().numpy(), ref_l
+
+
+@pytest.mark.parametrize("name,ctx", [("tiny", [128, 128]), ("minimind", [300, 0, 45, 129]),
+                                      ("v2", [200, 1, 77])])
+def test_decode_step_end_to_end(name, ctx):
+    shp = S.workload(name)
+    u, ref_u, o, ref_o, l, ref_l = end_to_end(shp, ctx)
+    assert_close(o, ref_o, shp.dtype, tol=TOL_E2E, what="o_lat")
+    assert_close(u, ref_u, shp.dtype, tol=TOL_E2E, what="u")
+    assert np.abs(l - ref_l).max() <= 2e-2 * max(1.0, np.abs(ref_l).max())
+
+
+# --------------------------------------------------------------------- full-size workloads (sampled)
+FULL = ["minimind", "v2", "v2_ragged", "v2_long"]
+
+
+@pytest.mark.parametrize("name", FULL)
+def test_decode_attn_full_size_sampled(name):
+    """The workload's full batch and context, in the launch configuration the
+    benchmark times; the oracle checks three sampled sequences (shortest,
+    longest, one more)."""
+    shp = S.workload(name)
+    ctx = S.draw_context_lengths(shp)
+    seqlens = ctx + 1
+    B, max_len = len(seqlens), int(seqlens.max())
+    g = torch.Generator(device="cuda")
+    g.manual_seed(shp.seed)
+    cache = torch.randn((B, max_len, shp.D), generator=g, device="cuda", dtype=torch.float32).to(torch_dtype(shp))
+    q = S.draw_absorbed_queries(shp, B)
+    dec = decoder(shp, {k: torch.zeros(1, device="cuda") for k in S.WEIGHT_NAMES}, B, max_len)
+    M.mla_decode_attn(dec.handle, dev(q, shp), cache, B, max_len, dev_i32(seqlens), dec.o_lat, dec.lse, dec.ws,
+                      dec.ws.numel())
+    st, bits = M.mla_get_device_status(dec.handle)
+    assert st == M.MLA_OK and bits == 0
+    picks = sorted({int(np.argmin(seqlens)), int(np.argmax(seqlens)), B // 2})
+    sc = O.scale_of(shp.d_h, shp.d_r)
+    for b in picks:
+        rows = host(cache[b, :seqlens[b]])
+        ref_o, ref_l = O.latent_attention(q[b], rows, shp.d_c, sc)
+        assert_close(host(dec.o_lat[b]), ref_o, shp.dtype, what=f"o_lat[{b}]")
+        assert np.abs(dec.lse[b].cpu().numpy() - ref_l).max() <= 2e-4 * max(1, np.abs(ref_l).max())
