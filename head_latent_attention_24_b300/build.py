@@ -1,6 +1,9 @@
 """Build libmla.so (all CUDA sources under csrc/) for sm_103a, in-tree.
 
-    python -m head_latent_attention_24_b300.build
+    python head_latent_attention_24_b300/build.py [-v] [--ptxas]
+
+Run it as a script (or load it by path): importing the package needs the
+library this script builds.
 """
 from __future__ import annotations
 

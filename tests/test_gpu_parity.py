@@ -186,7 +186,7 @@ def test_decode_attn_special_cases(name):
     if shp.dtype == "bf16":
         assert np.array_equal(got_o[1], want)
     else:
-        assert np.allclose(got_o[1], want, rtol=4e-7, atol=0)
+        assert np.allclose(got_o[1], want, rtol=2e-6, atol=0)
     # q = 0: the mean of the rows, lse = log(L)
     assert_close(got_o[2], np.broadcast_to(rows[2][:, :shp.d_c].mean(0), (shp.n_h, shp.d_c)), shp.dtype)
     assert np.allclose(got_l[2], np.log(max_len), rtol=1e-6)
