@@ -5,7 +5,7 @@ and the current CUDA stream to the C entry point of the same name
 (include/mla.h) and raises MLAError on a non-zero status. PyTorch supplies the
 device memory and streams; all arithmetic runs in the library's kernels.
 Importing this package fails if libmla.so has not been built
-(``python -m head_latent_attention_24_b300.build``) — there is no fallback.
+(``python head_latent_attention_24_b300/build.py``) — there is no fallback.
 """
 from __future__ import annotations
 
@@ -17,7 +17,7 @@ _HERE = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(_HERE, "libmla.so")
 
 if not os.path.exists(LIB_PATH):
-    raise ImportError(f"{LIB_PATH} is missing: build it with `python -m head_latent_attention_24_b300.build`")
+    raise ImportError(f"{LIB_PATH} is missing: build it with `python head_latent_attention_24_b300/build.py`")
 
 _lib = ctypes.CDLL(LIB_PATH)
 
@@ -75,6 +75,7 @@ _c = {
     "mla_absorb_q": _sig("mla_absorb_q", [_P, _P, _I, _P, _P, _P, _P, _P, _P, _P, _S, _P]),
     "mla_decode_workspace_size": _sig("mla_decode_workspace_size", [_P, _I, _I, ctypes.POINTER(_S)]),
     "mla_decode_attn": _sig("mla_decode_attn", [_P, _P, _P, _I, _I, _P, _P, _P, _P, _S, _P]),
+    "mla_decode_attn_noalloc": _sig("mla_decode_attn_noalloc", [_I, _I, _I, _I, _I, _P, _P, _I, _I, _P, _P, _P, _P]),
     "mla_out_proj_workspace_size": _sig("mla_out_proj_workspace_size", [_P, _I, ctypes.POINTER(_S)]),
     "mla_out_proj": _sig("mla_out_proj", [_P, _P, _I, _P, _P, _P, _P, _S, _P]),
     "mla_get_device_status": _sig("mla_get_device_status", [_P, _P, ctypes.POINTER(_I)]),
@@ -155,6 +156,15 @@ def mla_decode_workspace_size(handle, batch, max_len) -> int:
 def mla_decode_attn(handle, q_abs, cache, batch, max_len, seqlens, o_lat, lse, ws, ws_bytes, stream=None):
     _check(_c["mla_decode_attn"](handle, _ptr(q_abs), _ptr(cache), batch, max_len, _ptr(seqlens), _ptr(o_lat),
                                  _ptr(lse), _ptr(ws), ws_bytes, _stream(stream)), "mla_decode_attn")
+
+
+def mla_decode_attn_noalloc(n_h, d_h, d_c, d_r, dtype, q_abs, cache, batch, max_len, seqlens, o_lat, lse,
+                            stream=None):
+    """Decode attention with no workspace argument and no allocation (scratch is
+    the library's own fixed device array; see include/mla.h)."""
+    _check(_c["mla_decode_attn_noalloc"](n_h, d_h, d_c, d_r, dtype, _ptr(q_abs), _ptr(cache), batch, max_len,
+                                         _ptr(seqlens), _ptr(o_lat), _ptr(lse), _stream(stream)),
+           "mla_decode_attn_noalloc")
 
 
 def mla_out_proj_workspace_size(handle, batch) -> int:

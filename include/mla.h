@@ -157,6 +157,30 @@ MLA_API mla_status_t mla_decode_attn(mla_handle_t handle, const void* q_abs, con
                              int32_t batch, int32_t max_len, const int32_t* seqlens,
                              void* o_lat, float* lse, void* ws, size_t ws_bytes, void* stream);
 
+/* mla_decode_attn without caller workspace and without any allocation. The
+   pages have no counterpart to this call: it exists for callers that cannot
+   call cudaMalloc — for instance an engine that hands all device memory to its
+   own pool at start-up and forbids allocations outside it, or a latency-bound
+   loop that cannot afford cudaMalloc's implicit device synchronisation — and
+   so cannot create a handle or a workspace.
+   Same computation, layouts and results (within rounding) as mla_decode_attn
+   on the CUDA-core kernel family; the shape comes as arguments (n_h, d_h, d_c,
+   d_r, dtype = mla_dtype_t) instead of a handle.
+   Scratch: the split plan and split-KV partials live in one 8 MiB array in
+   device global memory, defined in the library; every GPU that loads the
+   library holds it until the process exits. Requests whose plan and partials
+   do not fit (roughly 4 * n_h * (d_c + 1) * (batch + 1) bytes at the fewest
+   splits) return MLA_ERR_WORKSPACE; d_c above 512 returns MLA_ERR_UNSUPPORTED.
+   The first call on each device looks up the array's device address (with
+   that device current); make that first call before any stream capture.
+   Every call shares the one array, so calls that overlap on the GPU (other
+   streams, other host threads on the same device) race and corrupt each
+   other's results; serialise them. Out-of-range seqlens are clamped to
+   [0, max_len] (their flag is not reported). Asynchronous on `stream`. */
+MLA_API mla_status_t mla_decode_attn_noalloc(int32_t n_h, int32_t d_h, int32_t d_c, int32_t d_r, int32_t dtype,
+                                     const void* q_abs, const void* cache, int32_t batch, int32_t max_len,
+                                     const int32_t* seqlens, void* o_lat, float* lse, void* stream);
+
 /* Workspace bytes mla_out_proj needs (the expanded per-head outputs o). */
 MLA_API mla_status_t mla_out_proj_workspace_size(mla_handle_t handle, int32_t batch, size_t* bytes);
 
