@@ -192,6 +192,32 @@ def test_decode_attn_special_cases(name):
     assert np.allclose(got_l[2], np.log(max_len), rtol=1e-6)
 
 
+@pytest.mark.parametrize("name", SMALL)
+@pytest.mark.parametrize("direction", ["rising", "falling"])
+def test_decode_attn_monotone_scores(name, direction):
+    # Scores that climb by ~12 (base 2) per 64 rows move the running maximum on
+    # every tile, so the online softmax must rescale its accumulator each time;
+    # falling scores keep the first tile's maximum throughout.
+    shp = S.workload(name)
+    max_len = 700
+    seqlens = np.array([700, 333, 64, 65])
+    B = len(seqlens)
+    sc = O.scale_of(shp.d_h, shp.d_r)
+    q = np.zeros((B, shp.n_h, shp.D))
+    q[:, :, 0] = S.to_dtype(np.linspace(0.5, 1.0, shp.n_h), shp.dtype)
+    rows = []
+    for b, n in enumerate(seqlens):
+        r = S.draw_latent_rows(shp, int(n), sub=40 + b) * 0.25
+        t = np.arange(n) if direction == "rising" else (n - 1 - np.arange(n))
+        r[:, 0] = S.to_dtype(t * (12.0 / 64.0) / np.log2(np.e) / sc, shp.dtype)
+        rows.append(S.to_dtype(r, shp.dtype))
+    ref_o, ref_l = oracle_decode(shp, q, rows, seqlens)
+    got_o, got_l, st, bits, _ = run_decode(shp, q, rows, seqlens, max_len)
+    assert st == M.MLA_OK and bits == 0
+    assert_close(got_o, ref_o, shp.dtype, what="o_lat")
+    assert np.abs(got_l - ref_l).max() <= (2e-5 if shp.dtype == "f32" else 2e-4) * max(1, np.abs(ref_l).max())
+
+
 def test_decode_attn_clamps_and_flags_bad_seqlens():
     shp = S.workload("minimind")
     max_len = 50
