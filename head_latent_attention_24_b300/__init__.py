@@ -39,6 +39,9 @@ MLA_DEV_TIMEOUT = 0x10
 MLA_DECODE_AUTO = 0
 MLA_DECODE_SIMT = 1
 MLA_DECODE_TCGEN05 = 2
+MLA_PROJ_AUTO = 0
+MLA_PROJ_SIMT = 1
+MLA_PROJ_TCGEN05 = 2
 
 
 class mla_config_t(ctypes.Structure):
@@ -81,6 +84,7 @@ _c = {
     "mla_get_device_status": _sig("mla_get_device_status", [_P, _P, ctypes.POINTER(_I)]),
     "mla_set_decode_path": _sig("mla_set_decode_path", [_P, _I]),
     "mla_get_decode_path": _sig("mla_get_decode_path", [_P, ctypes.POINTER(_I)]),
+    "mla_set_proj_path": _sig("mla_set_proj_path", [_P, _I]),
     "mla_last_launch_count": _sig("mla_last_launch_count", [_P, ctypes.POINTER(_I)]),
 }
 
@@ -195,6 +199,10 @@ def mla_get_decode_path(handle) -> int:
     p = _I()
     _check(_c["mla_get_decode_path"](handle, ctypes.byref(p)), "mla_get_decode_path")
     return p.value
+
+
+def mla_set_proj_path(handle, path):
+    _check(_c["mla_set_proj_path"](handle, path), "mla_set_proj_path")
 
 
 def mla_last_launch_count(handle) -> int:

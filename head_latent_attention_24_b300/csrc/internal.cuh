@@ -17,6 +17,7 @@ struct mla_handle_s {
   float* rope_sin;         // device [max_pos, d_r/2]
   int32_t* status;         // device status word
   int32_t decode_path;     // mla_decode_path_t requested
+  int32_t proj_path;       // mla_proj_path_t requested
   int32_t last_launches;   // launches made by the last successful call
 };
 
@@ -60,6 +61,32 @@ struct GemmArgs {
 };
 
 cudaError_t launch_gemm_simt(const GemmArgs& a, int dtype, cudaStream_t s);
+
+// ----------------------------------------------------- tensor-core GEMM (bf16)
+// Same product and epilogues as GemmArgs, for bf16 storage, on tcgen05:
+// out[n, col(m)] = epilogue( sum_k X[n, k] * W'[m, k] ) with the weights as the
+// 128-row MMA operand and the (few) activation rows as N. Up to two weight
+// segments are stacked along m (S1: W_DKV rows, then W_KR rows); segment s
+// fills output columns [col0[s], col0[s] + rows[s]).
+struct TcGemm {
+  int nseg;
+  const void* w[2];            // segment base (batch 0)
+  int rows[2];                 // m extent of each segment
+  int col0[2];                 // first output column of each segment
+  long long ldw, bw;           // element stride between W rows; between batches
+  int w_transposed;            // W'[m, k] = W[k*ldw + m] (stored [K rows][M cols])
+  const void* x; long long ldx, bx;
+  int N, K, Z;                 // rows of X, reduction length, batch count
+  int epi; void* out; long long ldo, bo;
+  const float* rope_cos; const float* rope_sin; int d_r; int max_pos;
+  const int32_t* pos; long long seg_stride; int seg_off;
+  const int32_t* tok_seq; const int32_t* tok_pos; int cache_batch; int max_len; int d_c; int row_width;
+  int32_t* status;
+};
+// Returns cudaErrorInvalidValue for shapes the kernel does not take (see the
+// checks in gemm_tc.cu); the caller then uses launch_gemm_simt.
+cudaError_t launch_gemm_tc(const TcGemm& g, int num_sms, cudaStream_t s);
+bool gemm_tc_shape_ok(const TcGemm& g);
 
 // --------------------------------------------------------- decode attention
 struct DecodeArgs {

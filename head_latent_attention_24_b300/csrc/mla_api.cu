@@ -22,6 +22,19 @@ bool on_handle_device(const mla_handle_s* h) {
 
 size_t esize(const mla_handle_s* h) { return h->cfg.dtype == MLA_BF16 ? 2 : 4; }
 
+bool use_tc_proj(const mla_handle_s* h, const TcGemm& g) {
+  if (h->cfg.dtype != MLA_BF16 || h->proj_path == MLA_PROJ_SIMT) return false;
+  return gemm_tc_shape_ok(g);
+}
+
+TcGemm tc_base(const mla_handle_s* h) {
+  TcGemm g{};
+  g.nseg = 1; g.Z = 1;
+  g.rope_cos = h->rope_cos; g.rope_sin = h->rope_sin; g.d_r = h->cfg.d_r; g.max_pos = h->cfg.max_pos;
+  g.status = h->status;
+  return g;
+}
+
 int resolve_decode_path(const mla_handle_s* h) {
   if (h->decode_path == MLA_DECODE_SIMT) return MLA_DECODE_SIMT;
   const bool tc_ok = decode_tc_supported(h);
@@ -124,6 +137,13 @@ mla_status_t mla_get_decode_path(mla_handle_t h, int32_t* path) {
   return MLA_OK;
 }
 
+mla_status_t mla_set_proj_path(mla_handle_t h, int32_t path) {
+  if (!h || path < MLA_PROJ_AUTO || path > MLA_PROJ_TCGEN05) return MLA_ERR_INVALID_ARG;
+  if (path == MLA_PROJ_TCGEN05 && h->cfg.dtype != MLA_BF16) return MLA_ERR_UNSUPPORTED;
+  h->proj_path = path;
+  return MLA_OK;
+}
+
 mla_status_t mla_last_launch_count(mla_handle_t h, int32_t* launches) {
   if (!h || !launches) return MLA_ERR_INVALID_ARG;
   *launches = h->last_launches;
@@ -159,9 +179,34 @@ mla_status_t mla_append_cache(mla_handle_t h, const void* x, int32_t n_tokens, c
   if (c.d_r > 64) return MLA_ERR_UNSUPPORTED;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   const int D = c.d_c + c.d_r;
-  // Two weight blocks, one launch each: c_KV columns then the RoPE columns.
-  // The RoPE launch sees both halves of every rotated pair in one tile.
   int launches = 0;
+  {
+    // One launch: the W_DKV rows then the W_KR rows, scattered to the cache rows.
+    TcGemm g = tc_base(h);
+    g.nseg = 2; g.w[0] = W_DKV; g.w[1] = W_KR; g.rows[0] = c.d_c; g.rows[1] = c.d_r;
+    g.col0[0] = 0; g.col0[1] = c.d_c; g.ldw = c.d; g.bw = 0;
+    g.x = x; g.ldx = c.d; g.bx = 0; g.K = c.d;
+    g.epi = EPI_APPEND; g.out = cache; g.tok_seq = tok_seq; g.tok_pos = tok_pos; g.cache_batch = batch;
+    g.max_len = max_len; g.d_c = c.d_c; g.row_width = D;
+    g.N = n_tokens;
+    if (h->proj_path == MLA_PROJ_TCGEN05 && !use_tc_proj(h, g)) return MLA_ERR_UNSUPPORTED;
+    if (use_tc_proj(h, g)) {
+      const int chunk = 65535 * 256;
+      for (int t0 = 0; t0 < n_tokens; t0 += chunk) {
+        TcGemm gc = g;
+        gc.N = n_tokens - t0 < chunk ? n_tokens - t0 : chunk;
+        gc.x = static_cast<const char*>(x) + (size_t)t0 * c.d * esize(h);
+        gc.tok_seq = tok_seq + t0;
+        gc.tok_pos = tok_pos + t0;
+        if (launch_gemm_tc(gc, h->num_sms, s) != cudaSuccess) return MLA_ERR_CUDA;
+        ++launches;
+      }
+      h->last_launches = launches;
+      return MLA_OK;
+    }
+  }
+  // CUDA-core kernel: two weight blocks, one launch each: c_KV columns then the RoPE columns.
+  // The RoPE launch sees both halves of every rotated pair in one tile.
   for (int part = 0; part < 2; ++part) {
     GemmArgs a{};
     a.X = x; a.ldx = c.d; a.bx = 0;
@@ -220,6 +265,32 @@ mla_status_t mla_absorb_q(mla_handle_t h, const void* x, int32_t batch, const vo
   char* c_q = static_cast<char*>(ws);
   char* q_c = c_q + align_up((size_t)batch * c.d_cq * esize(h), 256);
 
+  {
+    TcGemm g1 = tc_base(h);  // c_Q = W_DQ x
+    g1.w[0] = W_DQ; g1.rows[0] = c.d_cq; g1.ldw = c.d; g1.x = x; g1.ldx = c.d; g1.N = batch; g1.K = c.d;
+    g1.epi = EPI_STORE; g1.out = c_q; g1.ldo = c.d_cq;
+    TcGemm g2 = tc_base(h);  // q_C = W_UQ c_Q
+    g2.w[0] = W_UQ; g2.rows[0] = c.n_h * c.d_h; g2.ldw = c.d_cq; g2.x = c_q; g2.ldx = c.d_cq; g2.N = batch;
+    g2.K = c.d_cq; g2.epi = EPI_STORE; g2.out = q_c; g2.ldo = (long long)c.n_h * c.d_h;
+    TcGemm g3 = tc_base(h);  // q_R = RoPE(W_QR c_Q) -> q_abs[b, i, d_c:]
+    g3.w[0] = W_QR; g3.rows[0] = c.n_h * c.d_r; g3.ldw = c.d_cq; g3.x = c_q; g3.ldx = c.d_cq; g3.N = batch;
+    g3.K = c.d_cq; g3.epi = EPI_ROPE_SEGS; g3.out = q_abs; g3.ldo = (long long)c.n_h * D; g3.pos = pos;
+    g3.seg_stride = D; g3.seg_off = c.d_c;
+    TcGemm g4 = tc_base(h);  // q~_i = W_UK_i^T q_C_i -> q_abs[b, i, :d_c]
+    g4.w[0] = W_UK; g4.rows[0] = c.d_c; g4.w_transposed = 1; g4.ldw = c.d_c; g4.bw = (long long)c.d_h * c.d_c;
+    g4.x = q_c; g4.ldx = (long long)c.n_h * c.d_h; g4.bx = c.d_h; g4.N = batch; g4.K = c.d_h; g4.Z = c.n_h;
+    g4.epi = EPI_STORE; g4.out = q_abs; g4.ldo = (long long)c.n_h * D; g4.bo = D;
+    const bool tc = use_tc_proj(h, g1) && use_tc_proj(h, g2) && use_tc_proj(h, g3) && use_tc_proj(h, g4);
+    if (h->proj_path == MLA_PROJ_TCGEN05 && !tc) return MLA_ERR_UNSUPPORTED;
+    if (tc) {
+      if (launch_gemm_tc(g1, h->num_sms, s) != cudaSuccess) return MLA_ERR_CUDA;
+      if (launch_gemm_tc(g2, h->num_sms, s) != cudaSuccess) return MLA_ERR_CUDA;
+      if (launch_gemm_tc(g3, h->num_sms, s) != cudaSuccess) return MLA_ERR_CUDA;
+      if (launch_gemm_tc(g4, h->num_sms, s) != cudaSuccess) return MLA_ERR_CUDA;
+      h->last_launches = 4;
+      return MLA_OK;
+    }
+  }
   GemmArgs a{};
   a.batch = 1; a.wlayout = W_NORMAL; a.status = h->status;
   a.rope_cos = h->rope_cos; a.rope_sin = h->rope_sin; a.d_r = c.d_r; a.max_pos = c.max_pos;
@@ -311,6 +382,24 @@ mla_status_t mla_out_proj(mla_handle_t h, const void* o_lat, int32_t batch, cons
   if (!on_handle_device(h)) return MLA_ERR_INVALID_ARG;
   const mla_config_t& c = h->cfg;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
+  {
+    TcGemm g1 = tc_base(h);  // o_i = W_UV_i o_lat_i
+    g1.w[0] = W_UV; g1.rows[0] = c.d_h; g1.ldw = c.d_c; g1.bw = (long long)c.d_h * c.d_c;
+    g1.x = o_lat; g1.ldx = (long long)c.n_h * c.d_c; g1.bx = c.d_c; g1.N = batch; g1.K = c.d_c; g1.Z = c.n_h;
+    g1.epi = EPI_STORE; g1.out = ws; g1.ldo = (long long)c.n_h * c.d_h; g1.bo = c.d_h;
+    TcGemm g2 = tc_base(h);  // u = W_O o
+    g2.w[0] = W_O; g2.rows[0] = c.d; g2.ldw = (long long)c.n_h * c.d_h; g2.x = ws;
+    g2.ldx = (long long)c.n_h * c.d_h; g2.N = batch; g2.K = c.n_h * c.d_h; g2.epi = EPI_STORE; g2.out = u;
+    g2.ldo = c.d;
+    const bool tc = use_tc_proj(h, g1) && use_tc_proj(h, g2);
+    if (h->proj_path == MLA_PROJ_TCGEN05 && !tc) return MLA_ERR_UNSUPPORTED;
+    if (tc) {
+      if (launch_gemm_tc(g1, h->num_sms, s) != cudaSuccess) return MLA_ERR_CUDA;
+      if (launch_gemm_tc(g2, h->num_sms, s) != cudaSuccess) return MLA_ERR_CUDA;
+      h->last_launches = 2;
+      return MLA_OK;
+    }
+  }
   // o_i = W_UV_i o_lat_i, batched over heads
   GemmArgs a{};
   a.X = o_lat; a.ldx = (long long)c.n_h * c.d_c; a.bx = c.d_c;

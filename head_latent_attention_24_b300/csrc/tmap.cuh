@@ -10,4 +10,11 @@ namespace mla {
 // Returns false if the driver rejects the map.
 bool make_tmap_2d_bf16_sw128(CUtensorMap* map, const void* base, uint64_t inner, uint64_t outer,
                              uint64_t row_bytes, uint32_t box_inner, uint32_t box_outer);
+// 3-D bf16 tensor with extents dims[0] (contiguous), dims[1], dims[2] and byte
+// strides strides[0] (between dim-1 steps) and strides[1] (between dim-2
+// steps); box box[0] x box[1] x box[2], 128-byte swizzle (box[0] * 2 <= 128).
+// Elements outside the extents read as zero. Returns false if the driver
+// rejects the map.
+bool make_tmap_3d_bf16_sw128(CUtensorMap* map, const void* base, const uint64_t dims[3],
+                             const uint64_t strides[2], const uint32_t box[3]);
 }  // namespace mla

@@ -202,6 +202,13 @@ MLA_API mla_status_t mla_set_decode_path(mla_handle_t handle, int32_t path);
 /* The path AUTO resolves to for this handle (MLA_DECODE_SIMT or MLA_DECODE_TCGEN05). */
 MLA_API mla_status_t mla_get_decode_path(mla_handle_t handle, int32_t* path);
 
+/* Kernel family of the projections (mla_append_cache, mla_absorb_q,
+   mla_out_proj). AUTO picks the tensor-core (tcgen05) kernel for bf16 layers
+   whose strides it takes (every width a multiple of 8, d_r dividing 128), else
+   the CUDA-core one; fp32 layers always use the CUDA-core kernel. */
+typedef enum { MLA_PROJ_AUTO = 0, MLA_PROJ_SIMT = 1, MLA_PROJ_TCGEN05 = 2 } mla_proj_path_t;
+MLA_API mla_status_t mla_set_proj_path(mla_handle_t handle, int32_t path);
+
 /* Number of kernel launches the last successful call of each entry point made
    (for launch accounting in benchmarks). */
 MLA_API mla_status_t mla_last_launch_count(mla_handle_t handle, int32_t* launches);

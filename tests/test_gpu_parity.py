@@ -18,6 +18,13 @@ if not torch.cuda.is_available():
 import head_latent_attention_24_b300 as M  # noqa: E402
 
 SMALL = ["tiny", "minimind", "v2"]
+# Projection kernel families: the tensor-core kernel (AUTO for bf16) and the
+# CUDA-core kernel (forced). fp32 layers always take the CUDA-core kernel.
+PROJ = ["auto", "simt"]
+
+
+def set_proj(dec, proj):
+    M.mla_set_proj_path(dec.handle, M.MLA_PROJ_SIMT if proj == "simt" else M.MLA_PROJ_AUTO)
 
 
 def small_shape(name, batch=None, ctx=None):
@@ -29,17 +36,20 @@ def small_shape(name, batch=None, ctx=None):
 
 # --------------------------------------------------------------------- S1
 @pytest.mark.parametrize("name", SMALL)
-def test_append_matches_oracle_and_touches_only_its_rows(name):
+@pytest.mark.parametrize("proj", PROJ)
+@pytest.mark.parametrize("n", [150, 600])
+def test_append_matches_oracle_and_touches_only_its_rows(name, proj, n):
+    # n = 600 spans three 256-row tiles of the tensor-core kernel with a ragged tail
     shp = small_shape(name)
     W = S.draw_weights(shp)
-    B, L = 3, 200
+    B, L = 3, 250
     rng = np.random.default_rng(1)
-    n = 150
-    flat = rng.choice(B * L, size=n, replace=False)
+    # distinct rows, the first one at the last position of the last sequence
+    flat = np.concatenate([[B * L - 1], rng.choice(B * L - 1, size=n - 1, replace=False)])
     seq, pos = flat // L, flat % L
-    pos[0] = L - 1
     x = S.draw_context_h(shp, 0, n)
     dec = decoder(shp, make_weights_dev(shp, W), B, L)
+    set_proj(dec, proj)
     cache = torch.full((B, L, shp.D), float("nan"), dtype=torch_dtype(shp), device="cuda")
     dec.append(dev(x, shp), dev_i32(seq), dev_i32(pos), cache)
     st, bits = M.mla_get_device_status(dec.handle)
@@ -53,7 +63,8 @@ def test_append_matches_oracle_and_touches_only_its_rows(name):
 
 
 @pytest.mark.parametrize("name", SMALL)
-def test_append_bit_exact_on_integer_inputs(name):
+@pytest.mark.parametrize("proj", PROJ)
+def test_append_bit_exact_on_integer_inputs(name, proj):
     # Integer h and weights: every product and fp32 sum is exact, so after one
     # rounding to the storage dtype the cache must equal the oracle bit for bit.
     # Position 0 makes RoPE the identity; c_KV is exact at any position.
@@ -65,6 +76,7 @@ def test_append_bit_exact_on_integer_inputs(name):
     seq = np.arange(n) % B
     pos = np.where(np.arange(n) < B, 0, 1 + np.arange(n) // B)
     dec = decoder(shp, make_weights_dev(shp, W), B, L)
+    set_proj(dec, proj)
     cache = torch.zeros((B, L, shp.D), dtype=torch_dtype(shp), device="cuda")
     dec.append(dev(x, shp), dev_i32(seq), dev_i32(pos), cache)
     got = host(cache)[seq, pos]
@@ -95,7 +107,8 @@ def test_append_out_of_range_rows_are_skipped_and_flagged():
 
 # --------------------------------------------------------------------- S2
 @pytest.mark.parametrize("name", SMALL)
-def test_absorb_q_matches_oracle(name):
+@pytest.mark.parametrize("proj", PROJ)
+def test_absorb_q_matches_oracle(name, proj):
     shp = small_shape(name)
     W = S.draw_weights(shp)
     B = 37 if name != "tiny" else 2
@@ -104,6 +117,7 @@ def test_absorb_q_matches_oracle(name):
     pos = np.random.default_rng(3).integers(0, max_pos, size=B)
     pos[0], pos[-1] = 0, max_pos - 1
     dec = decoder(shp, make_weights_dev(shp, W), B, 16, max_pos=max_pos)
+    set_proj(dec, proj)
     M.mla_absorb_q(dec.handle, dev(h, shp), B, dec.W["W_DQ"], dec.W["W_UQ"], dec.W["W_QR"], dec.W["W_UK"],
                    dev_i32(pos), dec.q_abs, dec.ws, dec.ws.numel())
     ref = O.absorbed_query(h, W["W_DQ"], W["W_UQ"], W["W_QR"], W["W_UK"], pos, shp.n_h, shp.d_h, shp.d_r,
@@ -258,16 +272,47 @@ def test_workspace_and_alignment_errors():
 
 # --------------------------------------------------------------------- S4/S5
 @pytest.mark.parametrize("name", SMALL)
-def test_out_proj_matches_oracle(name):
+@pytest.mark.parametrize("proj", PROJ)
+def test_out_proj_matches_oracle(name, proj):
     shp = small_shape(name)
     W = S.draw_weights(shp)
     B = 19 if name != "tiny" else 2
     o_lat = S.to_dtype(S.draw_latent_rows(shp, B * shp.n_h, sub=11)[:, :shp.d_c].reshape(B, shp.n_h, shp.d_c)
                        / 8.0, shp.dtype)
     dec = decoder(shp, make_weights_dev(shp, W), B, 16)
+    set_proj(dec, proj)
     M.mla_out_proj(dec.handle, dev(o_lat, shp), B, dec.W["W_UV"], dec.W["W_O"], dec.u, dec.ws, dec.ws.numel())
     ref = O.output_projection(o_lat, W["W_UV"], W["W_O"], shp.n_h, shp.d_h)
     assert_close(host(dec.u), ref, shp.dtype, what="u")
+
+
+@pytest.mark.parametrize("name", ["minimind", "v2"])
+def test_projections_full_size(name):
+    """The benchmark's projection shapes (batch 256 for MiniMind, 64 for V2, the
+    full layer widths), in the launch configuration the benchmark uses: new-token
+    cache rows, the absorbed query and the output projection against the oracle."""
+    shp = S.workload(name)
+    W = S.draw_weights(shp)
+    B = shp.batch
+    h = S.draw_new_tokens(shp, B)
+    pos = np.random.default_rng(5).integers(0, 4097, size=B)
+    dec = decoder(shp, make_weights_dev(shp, W), B, 4097, max_pos=4097)
+    cache = torch.full((B, 4097, shp.D), float("nan"), dtype=torch_dtype(shp), device="cuda")
+    M.mla_append_cache(dec.handle, dev(h, shp), B, dec.W["W_DKV"], dec.W["W_KR"], dec.tok_seq, dev_i32(pos), cache,
+                       B, 4097)
+    M.mla_absorb_q(dec.handle, dev(h, shp), B, dec.W["W_DQ"], dec.W["W_UQ"], dec.W["W_QR"], dec.W["W_UK"],
+                   dev_i32(pos), dec.q_abs, dec.ws, dec.ws.numel())
+    o_lat = S.to_dtype(S.draw_latent_rows(shp, B * shp.n_h, sub=12)[:, :shp.d_c].reshape(B, shp.n_h, shp.d_c)
+                       / 8.0, shp.dtype)
+    M.mla_out_proj(dec.handle, dev(o_lat, shp), B, dec.W["W_UV"], dec.W["W_O"], dec.u, dec.ws, dec.ws.numel())
+    assert M.mla_get_device_status(dec.handle) == (M.MLA_OK, 0)
+    got_rows = host(cache)[np.arange(B), pos]
+    assert_close(got_rows, O.cache_rows(h, W["W_DKV"], W["W_KR"], pos, shp.rope_base), shp.dtype, what="cache rows")
+    ref_q = O.absorbed_query(h, W["W_DQ"], W["W_UQ"], W["W_QR"], W["W_UK"], pos, shp.n_h, shp.d_h, shp.d_r,
+                             shp.rope_base)
+    assert_close(host(dec.q_abs), ref_q, shp.dtype, what="q_abs")
+    ref_u = O.output_projection(o_lat, W["W_UV"], W["W_O"], shp.n_h, shp.d_h)
+    assert_close(host(dec.u), ref_u, shp.dtype, what="u")
 
 
 # --------------------------------------------------------------------- whole step
