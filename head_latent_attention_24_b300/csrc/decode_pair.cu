@@ -1,0 +1,724 @@
+// Tensor-core split-KV latent attention for the many-head latent shape
+// (n_h = 128, d_c = 512, d_r = 64, bf16): tcgen05.mma with TMEM accumulators,
+// TMA-fed shared-memory rings, a CTA pair that splits the work by stage.
+//
+// What is computed (page "MLA：潜在表示压缩与解耦 RoPE", §6 two-part score and
+// §7 softmax with scale 1/sqrt(d_h + d_r); page "Latent 压缩", value deferral):
+// for every head i of every sequence
+//   s_{i,t} = q_abs_i . row_t * scale,  o_lat_i = sum_t softmax_t(s_{i,t}) c_KV_t,  and the LSE.
+//
+// Why a pair split by stage. With 128 heads the latent accumulator O
+// (128 heads x 512 fp32) fills all 512 TMEM columns of an SM, and the scores
+// need columns of their own; the absorbed queries (128 x 576 bf16, 144 KB) do
+// not fit next to a pipelined cache tile in shared memory either. So the two
+// CTAs of a cluster divide the work:
+//   * CTA 0 ("score") holds q~ (the 512 latent columns of q_abs) in TMEM as
+//     the A operand and q_R in shared memory, streams full cache tiles
+//     (128 rows x 576) through a ring, and computes S = Q . C^T (M = 128
+//     heads, N = 128 rows, K = 576) into a double-buffered TMEM score block.
+//     Eight softmax warps (two per TMEM lane quarter, 64 rows each) turn each
+//     score tile into bf16 probabilities P and write them, 64 rows at a time,
+//     straight into CTA 1's shared memory.
+//   * CTA 1 ("value") keeps O = sum_t P_t c_KV_t in all of its TMEM and
+//     streams only the latent part of the same rows (mostly from L2, where
+//     CTA 0's loads left them): O += P . C (M = 128 heads, N = 128 latent
+//     columns x 4, K = 64 rows per unit). Its four correction warps apply the
+//     rare softmax rescale to O, zero cache rows past a sequence end (P is 0
+//     there, but the rows may hold NaN), and write o_lat / partials at the end
+//     of each piece.
+// Every MMA has M = 128 and N = 128, the shapes that run at the full tensor
+// rate; only P (2 bytes per head and row) crosses between the SMs.
+//
+// Softmax: online, in base 2, with a lazy reference maximum per head: the
+// reference moves (and O is rescaled) only when a tile's maximum rises more
+// than 8 above it, so P <= 256 and rescales are rare after the first tile.
+//
+// Work split: the plan of the CUDA-core kernel (all sequences' rows end to
+// end, cut into equal chunks, one per pair); a piece covering a whole
+// sequence writes o_lat/lse directly, any other piece a partial slot that
+// the LSE combine kernel merges.
+//
+// Every mbarrier wait is bounded; on expiry a CTA records MLA_DEV_TIMEOUT,
+// stops issuing work, waits (bounded) for its own copies in flight, joins the
+// final cluster barrier and frees its TMEM.
+#include "decode_tc.cuh"
+#include "tc_ptx.cuh"
+#include "tmap.cuh"
+
+namespace mla {
+
+namespace {
+
+using namespace tc;
+
+constexpr int NH = 128, DC = 512, DR = 64, DD = DC + DR;  // the shape this kernel serves
+constexpr int TR = 128;                 // cache rows per score tile (MMA N of QK)
+constexpr int UR = 64;                  // cache rows per value unit (K of one PV round)
+constexpr int NCH = DD / 64;            // 9 column chunks of 64 per row (128 B each)
+constexpr int NTHREADS = 320;           // 10 warps
+constexpr long long WAIT_CYCLES = 4000000000LL;  // ~2 s
+constexpr float kLn2 = 0.693147180559945309f;
+constexpr float RESCALE_THRESHOLD = 8.0f;
+
+// Cache tiles are fetched through a 3-D view of the cache, {64 columns, rows,
+// 9 column chunks} with the chunk as the outermost dimension, so one TMA box
+// brings several 128-byte column chunks of many rows and lands them chunk-major
+// ([chunk][row][128 B], 128-byte swizzle): the K-major layout tcgen05 reads.
+// TMA throughput per SM is set by the number of boxes, so boxes are large.
+// CTA 0 shared-memory layout (bytes from the 1024-aligned base)
+constexpr int QR_BYTES = NH * 64 * 2;             // 16 KB: q_R of 128 heads
+constexpr int S0_CPB = 3;                         // column chunks per score box
+constexpr int S0_RING = 3;                        // score ring slots (one box each)
+constexpr int S0_CHUNK = TR * 128;                // 16 KB: 128 rows x 64 columns
+constexpr int S0_SLOT = S0_CPB * S0_CHUNK;        // 48 KB
+// A P unit travels as one bulk copy: P (128 heads x 64 rows bf16, K-major,
+// 128-byte swizzle) followed by its Info block.
+constexpr int NPB = 3;                            // P buffers (one per value unit) on each side
+constexpr int P_BYTES = NH * UR * 2;              // 16 KB
+constexpr int P_STRIDE = 18 * 1024;               // P + Info, 1024-aligned buffers
+constexpr int S0_QR_OFF = 0;
+constexpr int S0_RING_OFF = QR_BYTES;
+constexpr int S0_STG_OFF = S0_RING_OFF + S0_RING * S0_SLOT;   // P staging buffers
+constexpr int S0_END = S0_STG_OFF + NPB * P_STRIDE;
+// CTA 1 shared-memory layout
+constexpr int S1_CPB = 4;                         // latent chunks per value box
+constexpr int S1_RING = 5;
+constexpr int S1_CHUNK = UR * 128;                // 8 KB: 64 rows x 64 latent columns
+constexpr int S1_SLOT = S1_CPB * S1_CHUNK;        // 32 KB: 64 rows x 256 latent columns
+constexpr int S1_P_OFF = 0;
+constexpr int S1_RING_OFF = NPB * P_STRIDE;
+constexpr int S1_END = S1_RING_OFF + S1_RING * S1_SLOT;
+constexpr int SMEM_DYN = (S0_END > S1_END ? S0_END : S1_END) + 1024;
+
+// TMEM columns
+constexpr uint32_t TMEM_COLS = 512;
+constexpr uint32_t QL_COL = 0;          // CTA 0: q~ as the A operand, 256 columns
+constexpr uint32_t S_COL = 256;         // CTA 0: two score blocks of 128 columns
+// CTA 1: O at columns [0, 512), latent column block nb at nb * 128
+
+constexpr uint32_t FLAG_RESCALE = 1u, FLAG_LAST = 2u;
+
+struct Info {                 // follows P in each buffer
+  float alpha[NH];            // rescale factor of O before this unit (if FLAG_RESCALE)
+  float l[NH];                // softmax denominator of the piece (if FLAG_LAST)
+  uint32_t flags;
+  uint32_t pad[3];
+};
+constexpr int P_COPY_BYTES = P_BYTES + (int)sizeof(Info);
+static_assert(P_COPY_BYTES % 16 == 0 && P_COPY_BYTES <= P_STRIDE, "P unit layout");
+
+struct Ctl {
+  // CTA 0
+  uint64_t r0_full[S0_RING], r0_empty[S0_RING];
+  uint64_t q_free, q_ready, s_full[2], s_free[2];
+  uint64_t p_free[NPB];       // arrivals: CTA 1's MMA commit + CTA 1's info read
+  // CTA 1
+  uint64_t r1_full[S1_RING], r1_empty[S1_RING];
+  uint64_t p_full[NPB];       // CTA 1's own arming arrival + the bulk copy's bytes
+  uint64_t unit_ready[NPB];   // CTA 1 correction warps -> MMA
+  // PV of the unit in P buffer b complete. One barrier per buffer: a waiter
+  // at unit u has seen p_full(u), which implies PV(u - NPB) completed, and
+  // PV(u + NPB) needs its unit_ready, so each barrier is within one phase of
+  // what its waiter expects (a single barrier could run two phases behind).
+  uint64_t pv_done[NPB];
+  uint64_t o_free;
+  uint32_t tmem_base;
+  int abort;
+  float mx[2][2][NH];         // CTA 0: per-half tile maxima, double-buffered by tile
+  float lsum[2][NH];          // CTA 0: per-half softmax sums at a piece end
+};
+
+__device__ __forceinline__ void sm_sync() { asm volatile("bar.sync 1, 256;" ::: "memory"); }
+__device__ __forceinline__ bool sm_any(bool v) {
+  uint32_t out;
+  asm volatile(
+      "{\n .reg .pred pi, po;\n setp.ne.u32 pi, %1, 0;\n barrier.cta.red.or.pred po, 1, 256, pi;\n"
+      " selp.u32 %0, 1, 0, po;\n}\n"
+      : "=r"(out)
+      : "r"((uint32_t)v)
+      : "memory");
+  return out != 0;
+}
+// The 128 softmax threads of one half (named barriers 3 and 4).
+__device__ __forceinline__ void half_sync(int hf) {
+  asm volatile("bar.sync %0, 128;" ::"r"(3 + hf) : "memory");
+}
+__device__ __forceinline__ bool half_any(int hf, bool v) {
+  uint32_t out;
+  asm volatile(
+      "{\n .reg .pred pi, po;\n setp.ne.u32 pi, %1, 0;\n barrier.cta.red.or.pred po, %2, 128, pi;\n"
+      " selp.u32 %0, 1, 0, po;\n}\n"
+      : "=r"(out)
+      : "r"((uint32_t)v), "r"(3 + hf)
+      : "memory");
+  return out != 0;
+}
+__device__ __forceinline__ void cw_sync() { asm volatile("bar.sync 2, 128;" ::: "memory"); }
+__device__ __forceinline__ bool cw_any(bool v) {
+  uint32_t out;
+  asm volatile(
+      "{\n .reg .pred pi, po;\n setp.ne.u32 pi, %1, 0;\n barrier.cta.red.or.pred po, 2, 128, pi;\n"
+      " selp.u32 %0, 1, 0, po;\n}\n"
+      : "=r"(out)
+      : "r"((uint32_t)v)
+      : "memory");
+  return out != 0;
+}
+
+__device__ __forceinline__ int find_seq_p(const int32_t* __restrict__ cum, int B, int r) {
+  int lo = 0, hi = B;
+  while (hi - lo > 1) {
+    const int mid = (lo + hi) >> 1;
+    if (cum[mid] <= r) lo = mid; else hi = mid;
+  }
+  while (lo < B - 1 && cum[lo + 1] <= r) ++lo;
+  return lo;
+}
+
+// The pieces (sequence, row range) of one chunk of the plan.
+struct Pieces {
+  const int32_t* cum; int B, start, end, b;
+  __device__ void init(const int32_t* c, int B_, int chunk) {
+    cum = c; B = B_;
+    const int cl = cum[B + 1], total = cum[B + 2];
+    start = chunk * cl;
+    end = min(start + cl, total);
+    b = start < end ? find_seq_p(cum, B, start) : B;
+  }
+  __device__ bool next(int& seq, int& t0, int& t1, bool& whole) {
+    while (b < B && cum[b] < end) {
+      const int s0 = cum[b], s1 = cum[b + 1];
+      const int cur = b++;
+      if (s1 == s0) continue;
+      const int p0 = max(s0, start), p1 = min(s1, end);
+      seq = cur; t0 = p0 - s0; t1 = p1 - s0; whole = (p0 == s0 && p1 == s1);
+      return true;
+    }
+    return false;
+  }
+};
+
+__device__ __forceinline__ bool wait_or_abort(uint64_t* bar, uint32_t parity, Ctl& ctl, int32_t* status) {
+  if (*reinterpret_cast<volatile int*>(&ctl.abort)) return false;
+  if (mbar_wait(bar, parity, WAIT_CYCLES)) return true;
+  atomicOr(status, MLA_DEV_TIMEOUT);
+  ctl.abort = 1;
+  return false;
+}
+
+__device__ __forceinline__ bool wait_cluster_or_abort(uint64_t* bar, uint32_t parity, Ctl& ctl, int32_t* status) {
+  if (*reinterpret_cast<volatile int*>(&ctl.abort)) return false;
+  if (mbar_wait_cluster(bar, parity, WAIT_CYCLES)) return true;
+  atomicOr(status, MLA_DEV_TIMEOUT);
+  ctl.abort = 1;
+  return false;
+}
+
+__global__ void __launch_bounds__(NTHREADS, 1)
+    decode_pair_kernel(const __grid_constant__ CUtensorMap map_kv0, const __grid_constant__ CUtensorMap map_kv1,
+                       const DecodeArgs a) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  __shared__ Ctl ctl;
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const uint32_t rank = cluster_rank();
+  const int chunk = blockIdx.x >> 1;
+  const int B = a.B;
+
+  if (threadIdx.x == 0) {
+    for (int i = 0; i < S0_RING; ++i) { mbar_init(&ctl.r0_full[i], 1); mbar_init(&ctl.r0_empty[i], 1); }
+    for (int i = 0; i < 2; ++i) { mbar_init(&ctl.s_full[i], 1); mbar_init(&ctl.s_free[i], 8); }
+    mbar_init(&ctl.q_free, 1);
+    mbar_init(&ctl.q_ready, 8);
+    for (int i = 0; i < NPB; ++i) {
+      mbar_init(&ctl.p_free[i], 2);
+      mbar_init(&ctl.p_full[i], 1);
+      mbar_init(&ctl.unit_ready[i], 4);
+    }
+    for (int i = 0; i < S1_RING; ++i) { mbar_init(&ctl.r1_full[i], 1); mbar_init(&ctl.r1_empty[i], 1); }
+    for (int i = 0; i < NPB; ++i) mbar_init(&ctl.pv_done[i], 1);
+    mbar_init(&ctl.o_free, 4);
+    ctl.abort = 0;
+    if (cluster_rank() == 1)  // arm the first use of every P buffer
+      for (int i = 0; i < NPB; ++i) mbar_arrive_expect_tx(&ctl.p_full[i], P_COPY_BYTES);
+    fence_mbar_init();
+  }
+  if (warp == 1) {
+    tmem_alloc(&ctl.tmem_base, TMEM_COLS);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  cluster_sync();  // both CTAs' barriers are initialised before any remote arrive
+  tc_fence_after();
+  const uint32_t tbase = ctl.tmem_base;
+  const uint32_t sbase = smem_u32(smem);
+  const float sl2 = a.scale_log2;
+
+  if (rank == 0) {
+    // ================================================================ CTA 0: scores and softmax
+    if (warp == 0) {
+      // ---------------------------------------------------------- TMA producer
+      if (lane == 0) {
+        prefetch_tensormap(&map_kv0);
+        Pieces it;
+        it.init(a.plan, B, chunk);
+        int seq, t0, t1;
+        bool whole;
+        int i = 0;
+        bool ok = true;
+        while (ok && it.next(seq, t0, t1, whole)) {
+          for (int r = t0; r < t1 && ok; r += TR) {
+            const int row = seq * a.max_len + r;
+            for (int c = 0; c < NCH; c += S0_CPB, ++i) {
+              const int sl = i % S0_RING;
+              if (i >= S0_RING) ok = wait_or_abort(&ctl.r0_empty[sl], ((i / S0_RING) - 1) & 1, ctl, a.status);
+              if (!ok) break;
+              mbar_arrive_expect_tx(&ctl.r0_full[sl], S0_SLOT);
+              tma_load_3d(smem + S0_RING_OFF + sl * S0_SLOT, &map_kv0, &ctl.r0_full[sl], 0, row, c);
+            }
+          }
+        }
+        if (!ok) {  // let copies in flight land before the CTA can exit
+          for (int s = 0; s < S0_RING; ++s) mbar_wait(&ctl.r0_full[s], 0, WAIT_CYCLES / 8);
+        }
+      }
+    } else if (warp == 1) {
+      // ---------------------------------------------------------- MMA issuer (QK)
+      if (lane == 0) {
+        constexpr uint32_t IDESC = idesc_bf16(128, TR, false, false);
+        Pieces it;
+        it.init(a.plan, B, chunk);
+        int seq, t0, t1;
+        bool whole;
+        int piece = 0, g = 0, i = 0;
+        bool ok = true;
+        const uint32_t qr = sbase + S0_QR_OFF;
+        while (ok && it.next(seq, t0, t1, whole)) {
+          ok = wait_or_abort(&ctl.q_ready, piece & 1, ctl, a.status);
+          if (!ok) break;
+          tc_fence_after();
+          for (int r = t0; r < t1 && ok; r += TR, ++g) {
+            const int sb = g & 1;
+            if (g >= 2) ok = wait_or_abort(&ctl.s_free[sb], ((g >> 1) - 1) & 1, ctl, a.status);
+            if (!ok) break;
+            tc_fence_after();
+            const uint32_t d = tbase + S_COL + sb * TR;
+            for (int c0 = 0; c0 < NCH; c0 += S0_CPB, ++i) {
+              const int sl = i % S0_RING;
+              ok = wait_or_abort(&ctl.r0_full[sl], (i / S0_RING) & 1, ctl, a.status);
+              if (!ok) break;
+              tc_fence_after();
+#pragma unroll
+              for (int cc = 0; cc < S0_CPB; ++cc) {
+                const int c = c0 + cc;
+                const uint32_t kb = sbase + S0_RING_OFF + sl * S0_SLOT + cc * S0_CHUNK;
+#pragma unroll
+                for (int k = 0; k < 4; ++k) {
+                  const uint64_t bd = sdesc_sw128(kb + k * 32, 16, 1024);
+                  if (c < NCH - 1)
+                    mma_bf16_ta(d, tbase + QL_COL + c * 32 + k * 8, bd, IDESC, (c > 0 || k > 0) ? 1u : 0u);
+                  else
+                    mma_bf16(d, sdesc_sw128(qr + k * 32, 16, 1024), bd, IDESC, 1u);
+                }
+              }
+              mma_commit(&ctl.r0_empty[sl]);
+            }
+            if (ok) mma_commit(&ctl.s_full[sb]);
+          }
+          if (ok) mma_commit(&ctl.q_free);
+          ++piece;
+        }
+      }
+    } else {
+      // ---------------------------------------------------------- softmax warps 2..9
+      const int quarter = warp & 3;
+      const int hf = (warp - 2) >> 2;                 // which 64 rows of a tile
+      const int h = quarter * 32 + lane;              // head = TMEM lane
+      const uint32_t lane_base = static_cast<uint32_t>(quarter * 32) << 16;
+      const uint32_t peer_p = mapa_shared(sbase + S1_P_OFF, 1);
+      const uint32_t peer_pfull = mapa_shared(smem_u32(&ctl.p_full[0]), 1);
+      Pieces it;
+      it.init(a.plan, B, chunk);
+      int seq, t0, t1;
+      bool whole;
+      int piece = 0, g = 0, u = 0;
+      bool ok = true;
+      while (ok && it.next(seq, t0, t1, whole)) {
+        // q~ of this piece's sequence into TMEM (this warp's lanes, its 128 of 256 columns)
+        if (piece >= 1) {
+          ok = wait_or_abort(&ctl.q_free, (piece - 1) & 1, ctl, a.status);
+          ok = !sm_any(!ok);
+          if (!ok) break;
+          tc_fence_after();
+        }
+        {
+          const uint4* qrow = reinterpret_cast<const uint4*>(static_cast<const __nv_bfloat16*>(a.q_abs) +
+                                                             ((size_t)seq * NH + h) * DD);
+          // q_R row h into shared memory (K-major, 128-byte swizzle): this half
+          // writes 16-byte units 4*hf .. 4*hf+3 of the row's 8
+          uint8_t* qr_row = smem + S0_QR_OFF + (h >> 3) * 1024 + (h & 7) * 128;
+#pragma unroll
+          for (int v = 4 * hf; v < 4 * hf + 4; ++v)
+            *reinterpret_cast<uint4*>(qr_row + ((v ^ (h & 7)) << 4)) = __ldg(qrow + DC / 8 + v);
+          fence_proxy_async_smem();
+          const uint4* src = qrow + hf * 32;
+#pragma unroll 1
+          for (int j = 0; j < 4; ++j) {
+            uint32_t r[32];
+#pragma unroll
+            for (int v = 0; v < 8; ++v) {
+              const uint4 x = __ldg(src + j * 8 + v);
+              r[4 * v] = x.x; r[4 * v + 1] = x.y; r[4 * v + 2] = x.z; r[4 * v + 3] = x.w;
+            }
+            tmem_st32(tbase + lane_base + QL_COL + hf * 128 + j * 32, r);
+          }
+          tmem_st_wait();
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&ctl.q_ready);
+        }
+        float m_ref = -INFINITY, l_part = 0.f;
+        const int len = t1 - t0;
+        const int ntiles = (len + TR - 1) / TR;
+        for (int k = 0; k < ntiles; ++k, ++g) {
+          const int nvalid = min(TR, len - k * TR);
+          const bool has_unit = hf == 0 || nvalid > UR;
+          const int my_u = u + hf;                     // this half's unit index
+          const bool last_tile = k == ntiles - 1;
+          const int sb = g & 1;
+          ok = wait_or_abort(&ctl.s_full[sb], (g >> 1) & 1, ctl, a.status);
+          ok = !sm_any(!ok);
+          if (!ok) break;
+          tc_fence_after();
+          float s[64];
+#pragma unroll
+          for (int c = 0; c < 64; c += 16) {
+            float v[16];
+            tmem_ld16(tbase + lane_base + S_COL + sb * TR + hf * 64 + c, v);
+#pragma unroll
+            for (int i2 = 0; i2 < 16; ++i2) s[c + i2] = v[i2];
+          }
+          tmem_ld_wait();
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&ctl.s_free[sb]);
+          float mt = -INFINITY;
+          const int nv_half = nvalid - hf * 64;
+#pragma unroll
+          for (int i2 = 0; i2 < 64; ++i2) {
+            s[i2] = (i2 < nv_half) ? s[i2] * sl2 : -INFINITY;
+            mt = fmaxf(mt, s[i2]);
+          }
+          ctl.mx[sb][hf][h] = mt;
+          sm_sync();
+          mt = fmaxf(ctl.mx[sb][0][h], ctl.mx[sb][1][h]);
+          bool need = false;
+          float alpha = 1.f;
+          if (m_ref == -INFINITY || mt > m_ref + RESCALE_THRESHOLD) {
+            need = true;
+            alpha = (m_ref == -INFINITY) ? 0.f : exp2f(m_ref - mt);
+            m_ref = mt;
+          }
+          const bool any_rescale = sm_any(need && k > 0);
+          float psum = 0.f;
+          uint32_t packed[32];
+#pragma unroll
+          for (int i2 = 0; i2 < 64; i2 += 2) {
+            const float p0 = exp2f(s[i2] - m_ref), p1 = exp2f(s[i2 + 1] - m_ref);
+            psum += p0 + p1;
+            __nv_bfloat162 pr = __floats2bfloat162_rn(p0, p1);
+            packed[i2 / 2] = *reinterpret_cast<uint32_t*>(&pr);
+          }
+          l_part = l_part * alpha + psum;
+          if (last_tile) {
+            ctl.lsum[hf][h] = l_part;
+            sm_sync();
+          }
+          if (has_unit) {
+            const int pb = my_u % NPB;
+            bool w = true;
+            if (my_u >= NPB) w = wait_cluster_or_abort(&ctl.p_free[pb], ((my_u / NPB) - 1) & 1, ctl, a.status);
+            w = !half_any(hf, !w);  // the half takes one branch: it meets at a barrier below
+            ok = ok && w;
+            if (w) {
+              // P row h of this unit (64 bf16 = 8 units of 16 B, 128-byte swizzle)
+              // and its Info into the local staging buffer, then one bulk copy
+              uint8_t* stg = smem + S0_STG_OFF + pb * P_STRIDE;
+              uint8_t* row = stg + (h >> 3) * 1024 + (h & 7) * 128;
+#pragma unroll
+              for (int v = 0; v < 8; ++v)
+                *reinterpret_cast<uint4*>(row + ((v ^ (h & 7)) << 4)) =
+                    make_uint4(packed[4 * v], packed[4 * v + 1], packed[4 * v + 2], packed[4 * v + 3]);
+              Info* inf = reinterpret_cast<Info*>(stg + P_BYTES);
+              const bool last_unit = last_tile && (hf == 1 || nvalid <= UR);
+              inf->alpha[h] = alpha;
+              if (last_unit) {
+                const float l = ctl.lsum[0][h] + ctl.lsum[1][h];
+                inf->l[h] = l;
+                const float lse = l > 0.f ? (m_ref + log2f(l)) * kLn2 : -INFINITY;
+                if (whole) a.lse[(size_t)seq * NH + h] = lse;
+                else a.part_lse[(size_t)(seq + chunk) * NH + h] = lse;
+              }
+              if (h == 0) inf->flags = ((hf == 0 && any_rescale) ? FLAG_RESCALE : 0u) | (last_unit ? FLAG_LAST : 0u);
+              fence_proxy_async_smem();
+              half_sync(hf);
+              if (h == 0)
+                bulk_copy_to_cluster(peer_p + pb * P_STRIDE, stg, P_COPY_BYTES, peer_pfull + pb * 8);
+            }
+          }
+          ok = !sm_any(!ok);
+          if (!ok) break;
+          u += (nvalid > UR) ? 2 : 1;
+        }
+        ++piece;
+      }
+    }
+  } else {
+    // ================================================================ CTA 1: values
+    if (warp == 0) {
+      // ---------------------------------------------------------- TMA producer (latent part)
+      if (lane == 0) {
+        prefetch_tensormap(&map_kv1);
+        Pieces it;
+        it.init(a.plan, B, chunk);
+        int seq, t0, t1;
+        bool whole;
+        int i = 0;
+        bool ok = true;
+        while (ok && it.next(seq, t0, t1, whole)) {
+          for (int r = t0; r < t1 && ok; r += UR) {
+            const int row = seq * a.max_len + r;
+            for (int j = 0; j < 2; ++j, ++i) {
+              const int sl = i % S1_RING;
+              if (i >= S1_RING) ok = wait_or_abort(&ctl.r1_empty[sl], ((i / S1_RING) - 1) & 1, ctl, a.status);
+              if (!ok) break;
+              mbar_arrive_expect_tx(&ctl.r1_full[sl], S1_SLOT);
+              tma_load_3d(smem + S1_RING_OFF + sl * S1_SLOT, &map_kv1, &ctl.r1_full[sl], 0, row, j * S1_CPB);
+            }
+          }
+        }
+        if (!ok) {
+          for (int s = 0; s < S1_RING; ++s) mbar_wait(&ctl.r1_full[s], 0, WAIT_CYCLES / 8);
+        }
+      }
+    } else if (warp == 1) {
+      // ---------------------------------------------------------- MMA issuer (PV)
+      if (lane == 0) {
+        constexpr uint32_t IDESC = idesc_bf16(128, 128, false, true);
+        Pieces it;
+        it.init(a.plan, B, chunk);
+        int seq, t0, t1;
+        bool whole;
+        int piece = 0, u = 0, i = 0;
+        bool ok = true;
+        while (ok && it.next(seq, t0, t1, whole)) {
+          if (piece > 0) ok = wait_or_abort(&ctl.o_free, (piece - 1) & 1, ctl, a.status);
+          bool first = true;
+          for (int r = t0; r < t1 && ok; r += UR, ++u) {
+            const int pb = u % NPB;
+            ok = wait_cluster_or_abort(&ctl.p_full[pb], (u / NPB) & 1, ctl, a.status) &&
+                 wait_or_abort(&ctl.unit_ready[pb], (u / NPB) & 1, ctl, a.status);
+            if (!ok) break;
+            tc_fence_after();
+            const uint32_t pa = sbase + S1_P_OFF + pb * P_STRIDE;
+            for (int j = 0; j < 2; ++j, ++i) {
+              const int sl = i % S1_RING;
+              ok = wait_or_abort(&ctl.r1_full[sl], (i / S1_RING) & 1, ctl, a.status);
+              if (!ok) break;
+              tc_fence_after();
+#pragma unroll
+              for (int nb2 = 0; nb2 < 2; ++nb2) {
+                // latent columns [256 j + 128 nb2, +128): two 8 KB chunks, 8 KB apart
+                const uint32_t vb = sbase + S1_RING_OFF + sl * S1_SLOT + nb2 * 2 * S1_CHUNK;
+#pragma unroll
+                for (int k = 0; k < 4; ++k) {
+                  mma_bf16(tbase + (2 * j + nb2) * 128, sdesc_sw128(pa + k * 32, 16, 1024),
+                           sdesc_sw128(vb + k * 2048, S1_CHUNK, 1024), IDESC, (first && k == 0) ? 0u : 1u);
+                }
+              }
+              mma_commit(&ctl.r1_empty[sl]);
+            }
+            if (!ok) break;
+            first = false;
+            mma_commit_multicast(&ctl.p_free[pb], 0x1);
+            mma_commit(&ctl.pv_done[pb]);
+          }
+          ++piece;
+        }
+      }
+    } else if (warp < 6) {
+      // ---------------------------------------------------------- correction / epilogue warps 2..5
+      const int quarter = warp & 3;
+      const int h = quarter * 32 + lane;
+      const int ct = threadIdx.x - 64;   // 0..127
+      const uint32_t lane_base = static_cast<uint32_t>(quarter * 32) << 16;
+      const uint32_t peer_pfree = mapa_shared(smem_u32(&ctl.p_free[0]), 0);
+      Pieces it;
+      it.init(a.plan, B, chunk);
+      int seq, t0, t1;
+      bool whole;
+      int piece = 0, u = 0, i = 0;
+      bool ok = true;
+      while (ok && it.next(seq, t0, t1, whole)) {
+        float inv_l = 0.f;
+        bool first = true;
+        for (int r = t0; r < t1 && ok; r += UR, ++u, i += 2) {
+          const int nrows = min(UR, t1 - r);
+          const int pb = u % NPB;
+          ok = wait_cluster_or_abort(&ctl.p_full[pb], (u / NPB) & 1, ctl, a.status);
+          ok = !cw_any(!ok);
+          if (!ok) break;
+          const Info* inf = reinterpret_cast<const Info*>(smem + S1_P_OFF + pb * P_STRIDE + P_BYTES);
+          const uint32_t flags = *reinterpret_cast<const volatile uint32_t*>(&inf->flags);
+          const float alpha = inf->alpha[h];
+          if (flags & FLAG_LAST) {
+            const float l = inf->l[h];
+            inv_l = l > 0.f ? 1.f / l : 0.f;
+          }
+          if ((flags & FLAG_RESCALE) && !first) {
+            // O must hold every earlier unit before it is rescaled
+            ok = wait_or_abort(&ctl.pv_done[(u - 1) % NPB], ((u - 1) / NPB) & 1, ctl, a.status);
+            ok = !cw_any(!ok);
+            if (!ok) break;
+            tc_fence_after();
+#pragma unroll 1
+            for (int c = 0; c < DC; c += 16) {
+              float v[16];
+              tmem_ld16(tbase + lane_base + c, v);
+              tmem_ld_wait();
+#pragma unroll
+              for (int i2 = 0; i2 < 16; ++i2) v[i2] *= alpha;
+              tmem_st16(tbase + lane_base + c, v);
+            }
+            tmem_st_wait();
+          }
+          if (nrows < UR) {
+            // zero the unit's rows past the piece end in its 2 slots (8 latent chunks)
+            for (int j = 0; j < 2; ++j) {
+              const int sl = (i + j) % S1_RING;
+              ok = wait_or_abort(&ctl.r1_full[sl], ((i + j) / S1_RING) & 1, ctl, a.status);
+              if (!ok) break;
+            }
+            ok = !cw_any(!ok);
+            if (!ok) break;
+            const int per_chunk = (UR - nrows) * 8;    // 16-byte words of one chunk's dead rows
+            for (int w = ct; w < per_chunk * 8; w += 128) {
+              const int ch = w / per_chunk, rem = w % per_chunk;
+              const int row = nrows + rem / 8, part = rem % 8;
+              uint8_t* base = smem + S1_RING_OFF + ((i + ch / S1_CPB) % S1_RING) * S1_SLOT + (ch % S1_CPB) * S1_CHUNK;
+              *reinterpret_cast<uint4*>(base + row * 128 + part * 16) = make_uint4(0, 0, 0, 0);
+            }
+            fence_proxy_async_smem();
+          }
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&ctl.unit_ready[pb]);
+          cw_sync();  // every correction thread has read this buffer's Info
+          if (ct == 0) {
+            mbar_arrive_expect_tx(&ctl.p_full[pb], P_COPY_BYTES);  // arm the buffer's next use
+            mbar_arrive_remote(peer_pfree + pb * 8);
+          }
+          first = false;
+          if (flags & FLAG_LAST) {
+            // ------------------------------------------------ epilogue of the piece
+            ok = wait_or_abort(&ctl.pv_done[pb], (u / NPB) & 1, ctl, a.status);
+            ok = !cw_any(!ok);
+            if (!ok) break;
+            tc_fence_after();
+#pragma unroll 1
+            for (int c = 0; c < DC; c += 16) {
+              float v[16];
+              tmem_ld16(tbase + lane_base + c, v);
+              tmem_ld_wait();
+              if (whole) {
+                uint32_t pk[8];
+#pragma unroll
+                for (int i2 = 0; i2 < 8; ++i2) {
+                  __nv_bfloat162 pr = __floats2bfloat162_rn(v[2 * i2] * inv_l, v[2 * i2 + 1] * inv_l);
+                  pk[i2] = *reinterpret_cast<uint32_t*>(&pr);
+                }
+                uint4* dst = reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(a.o_lat) +
+                                                      ((size_t)seq * NH + h) * DC + c);
+                dst[0] = make_uint4(pk[0], pk[1], pk[2], pk[3]);
+                dst[1] = make_uint4(pk[4], pk[5], pk[6], pk[7]);
+              } else {
+                float4* dst = reinterpret_cast<float4*>(a.part_o + ((size_t)(seq + chunk) * NH + h) * DC + c);
+#pragma unroll
+                for (int i2 = 0; i2 < 4; ++i2)
+                  dst[i2] = make_float4(v[4 * i2] * inv_l, v[4 * i2 + 1] * inv_l, v[4 * i2 + 2] * inv_l,
+                                        v[4 * i2 + 3] * inv_l);
+              }
+            }
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&ctl.o_free);
+          }
+        }
+        ++piece;
+      }
+    }
+  }
+
+  // ------------------------------------------------------------------ teardown
+  __syncwarp();
+  tc_fence_before();
+  __syncthreads();
+  cluster_sync();  // no CTA leaves while its peer may still write into it
+  tc_fence_after();
+  if (warp == 1) tmem_dealloc(tbase, TMEM_COLS);
+}
+
+}  // namespace
+
+bool decode_tc_supported(const mla_handle_s* h) {
+  const mla_config_t& c = h->cfg;
+  return c.dtype == MLA_BF16 && c.n_h == NH && c.d_c == DC && c.d_r == DR;
+}
+
+int decode_tc_chunks(const mla_handle_s* h, int) {
+  const int pairs = h->num_sms / 2;
+  return pairs < 1 ? 1 : pairs;
+}
+
+cudaError_t launch_decode_tc(const mla_handle_s* h, const DecodeArgs& a, cudaStream_t s, int* launches) {
+  // Cache viewed as {64 columns, rows, 9 column chunks}: row stride 1152 B,
+  // chunk stride 128 B (the chunk is the outer box dimension).
+  CUtensorMap map_kv0, map_kv1;
+  const uint64_t dims[3] = {64, (uint64_t)a.B * a.max_len, NCH};
+  const uint64_t strides[2] = {DD * 2, 128};
+  const uint32_t box0[3] = {64, TR, S0_CPB}, box1[3] = {64, UR, S1_CPB};
+  if (!make_tmap_3d_bf16_sw128(&map_kv0, a.cache, dims, strides, box0)) return cudaErrorInvalidValue;
+  if (!make_tmap_3d_bf16_sw128(&map_kv1, a.cache, dims, strides, box1)) return cudaErrorInvalidValue;
+  cudaError_t e = launch_decode_plan(a.seqlens, a.B, a.max_len, a.grid_chunks, UR, a.plan, a.status, s);
+  if (e != cudaSuccess) return e;
+  static bool attr_set = false;
+  if (!attr_set) {
+    e = cudaFuncSetAttribute(decode_pair_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_DYN);
+    if (e != cudaSuccess) return e;
+    attr_set = true;
+  }
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)(2 * a.grid_chunks));
+  cfg.blockDim = dim3(NTHREADS);
+  cfg.dynamicSmemBytes = SMEM_DYN;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = 2;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  e = cudaLaunchKernelEx(&cfg, decode_pair_kernel, map_kv0, map_kv1, a);
+  if (e != cudaSuccess) return e;
+  e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+  e = launch_decode_combine(a, MLA_BF16, s);
+  if (launches) *launches = 3;
+  (void)h;
+  return e;
+}
+
+}  // namespace mla

@@ -232,6 +232,47 @@ def test_decode_attn_monotone_scores(name, direction):
     assert np.abs(got_l - ref_l).max() <= (2e-5 if shp.dtype == "f32" else 2e-4) * max(1, np.abs(ref_l).max())
 
 
+# Sequence layouts that give every chunk of the split-KV plan several
+# 128-row tiles (the other cases mostly give one tile per chunk): whole
+# sequences of 3 tiles per chunk, one long sequence split over every chunk,
+# and lengths that end mid-tile.
+LONG_LAYOUTS = {
+    "3_tiles_whole": lambda: np.full(74, 384),
+    "1_seq_split": lambda: np.array([74 * 384]),
+    "ragged_tails": lambda: np.array([5000, 4097, 333, 64 * 75 + 1]),
+}
+
+
+@pytest.mark.parametrize("layout", list(LONG_LAYOUTS))
+def test_decode_attn_multi_tile_chunks(layout):
+    shp = S.workload("v2")
+    seqlens = LONG_LAYOUTS[layout]()
+    B, max_len = len(seqlens), int(seqlens.max())
+    q = S.draw_absorbed_queries(shp, B)
+    rows = [S.draw_latent_rows(shp, int(n), sub=60 + b) for b, n in enumerate(seqlens)]
+    ref_o, ref_l = oracle_decode(shp, q, rows, seqlens)
+    got_o, got_l, st, bits, _ = run_decode(shp, q, rows, seqlens, max_len)
+    assert st == M.MLA_OK and bits == 0
+    assert np.abs(got_l - ref_l).max() <= 2e-4 * max(1, np.abs(ref_l).max())
+    assert_close(got_o, ref_o, shp.dtype, what="o_lat")
+
+
+def test_decode_attn_equal_rows_long():
+    # Every row of a sequence equal: o_lat is that row whatever the weights,
+    # as long as the weights applied to the rows are the ones summed into the
+    # softmax denominator. Several tiles per chunk.
+    shp = S.workload("v2")
+    seqlens = np.array([9000, 7000])
+    B, max_len = 2, 9000
+    q = S.draw_absorbed_queries(shp, B)
+    rows = [np.tile(S.draw_latent_rows(shp, 1, sub=70 + b), (int(n), 1)) for b, n in enumerate(seqlens)]
+    got_o, got_l, st, bits, _ = run_decode(shp, q, rows, seqlens, max_len)
+    assert st == M.MLA_OK and bits == 0
+    for b in range(B):
+        want = np.broadcast_to(rows[b][0, :shp.d_c], (shp.n_h, shp.d_c))
+        assert_close(got_o[b], want, shp.dtype, what=f"o_lat[{b}]")
+
+
 def test_decode_attn_clamps_and_flags_bad_seqlens():
     shp = S.workload("minimind")
     max_len = 50
