@@ -57,7 +57,7 @@ def build(verbose: bool = False, ptxas_info: bool = False) -> str:
     if os.path.exists(LIB) and os.path.getmtime(LIB) >= max(os.path.getmtime(o) for o in objs):
         return LIB
     tmp = LIB + ".tmp"
-    cmd = [nvcc()] + ARCH + ["-shared", "-Xcompiler", "-fPIC", "-o", tmp] + objs
+    cmd = [nvcc()] + ARCH + ["-shared", "-Xcompiler", "-fPIC", "-Xlinker", "--no-undefined", "-o", tmp] + objs
     if verbose:
         print(" ".join(cmd), flush=True)
     r = subprocess.run(cmd, capture_output=True, text=True)

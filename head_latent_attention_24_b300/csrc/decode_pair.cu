@@ -96,10 +96,10 @@ constexpr uint32_t QL_COL = 0;          // CTA 0: q~ as the A operand, 256 colum
 constexpr uint32_t S_COL = 256;         // CTA 0: two score blocks of 128 columns
 // CTA 1: O at columns [0, 512), latent column block nb at nb * 128
 
-constexpr uint32_t FLAG_RESCALE = 1u, FLAG_LAST = 2u;
+constexpr uint32_t FLAG_LAST = 1u;
 
 struct Info {                 // follows P in each buffer
-  float alpha[NH];            // rescale factor of O before this unit (if FLAG_RESCALE)
+  float alpha[NH];            // factor O is rescaled by before this unit (1 = none)
   float l[NH];                // softmax denominator of the piece (if FLAG_LAST)
   uint32_t flags;
   uint32_t pad[3];
@@ -139,14 +139,11 @@ __device__ __forceinline__ bool sm_any(bool v) {
       : "memory");
   return out != 0;
 }
-// The 128 softmax threads of one half (named barriers 3 and 4).
-__device__ __forceinline__ void half_sync(int hf) {
-  asm volatile("bar.sync %0, 128;" ::"r"(3 + hf) : "memory");
-}
-__device__ __forceinline__ bool half_any(int hf, bool v) {
+// The 128 softmax threads of one half (named barriers 3 and 4): all true?
+__device__ __forceinline__ bool half_all(int hf, bool v) {
   uint32_t out;
   asm volatile(
-      "{\n .reg .pred pi, po;\n setp.ne.u32 pi, %1, 0;\n barrier.cta.red.or.pred po, %2, 128, pi;\n"
+      "{\n .reg .pred pi, po;\n setp.ne.u32 pi, %1, 0;\n barrier.cta.red.and.pred po, %2, 128, pi;\n"
       " selp.u32 %0, 1, 0, po;\n}\n"
       : "=r"(out)
       : "r"((uint32_t)v), "r"(3 + hf)
@@ -388,9 +385,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
           const int my_u = u + hf;                     // this half's unit index
           const bool last_tile = k == ntiles - 1;
           const int sb = g & 1;
-          ok = wait_or_abort(&ctl.s_full[sb], (g >> 1) & 1, ctl, a.status);
-          ok = !sm_any(!ok);
-          if (!ok) break;
+          const bool w = wait_or_abort(&ctl.s_full[sb], (g >> 1) & 1, ctl, a.status);
           tc_fence_after();
           float s[64];
 #pragma unroll
@@ -404,48 +399,53 @@ __global__ void __launch_bounds__(NTHREADS, 1)
           tc_fence_before();
           __syncwarp();
           if (lane == 0) mbar_arrive(&ctl.s_free[sb]);
-          float mt = -INFINITY;
-          const int nv_half = nvalid - hf * 64;
+          // scores in base 2, rows past the piece end at -inf; tile maximum
+          float m4[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
+          if (nvalid == TR) {
 #pragma unroll
-          for (int i2 = 0; i2 < 64; ++i2) {
-            s[i2] = (i2 < nv_half) ? s[i2] * sl2 : -INFINITY;
-            mt = fmaxf(mt, s[i2]);
+            for (int i2 = 0; i2 < 64; ++i2) {
+              s[i2] *= sl2;
+              m4[i2 & 3] = fmaxf(m4[i2 & 3], s[i2]);
+            }
+          } else {
+            const int nv_half = nvalid - hf * 64;
+#pragma unroll
+            for (int i2 = 0; i2 < 64; ++i2) {
+              s[i2] = (i2 < nv_half) ? s[i2] * sl2 : -INFINITY;
+              m4[i2 & 3] = fmaxf(m4[i2 & 3], s[i2]);
+            }
           }
-          ctl.mx[sb][hf][h] = mt;
-          sm_sync();
-          mt = fmaxf(ctl.mx[sb][0][h], ctl.mx[sb][1][h]);
-          bool need = false;
+          ctl.mx[sb][hf][h] = fmaxf(fmaxf(m4[0], m4[1]), fmaxf(m4[2], m4[3]));
+          // one barrier per tile: exchange the halves' maxima and vote on aborting
+          if (sm_any(!w || !ok)) { ok = false; break; }
+          const float mt = fmaxf(ctl.mx[sb][0][h], ctl.mx[sb][1][h]);
           float alpha = 1.f;
           if (m_ref == -INFINITY || mt > m_ref + RESCALE_THRESHOLD) {
-            need = true;
-            alpha = (m_ref == -INFINITY) ? 0.f : exp2f(m_ref - mt);
+            alpha = (m_ref == -INFINITY) ? 0.f : ex2_approx(m_ref - mt);
             m_ref = mt;
           }
-          const bool any_rescale = sm_any(need && k > 0);
-          float psum = 0.f;
+          float p4[4] = {0.f, 0.f, 0.f, 0.f};
           uint32_t packed[32];
 #pragma unroll
           for (int i2 = 0; i2 < 64; i2 += 2) {
-            const float p0 = exp2f(s[i2] - m_ref), p1 = exp2f(s[i2 + 1] - m_ref);
-            psum += p0 + p1;
+            const float p0 = ex2_approx(s[i2] - m_ref), p1 = ex2_approx(s[i2 + 1] - m_ref);
+            p4[(i2 >> 1) & 3] += p0 + p1;
             __nv_bfloat162 pr = __floats2bfloat162_rn(p0, p1);
             packed[i2 / 2] = *reinterpret_cast<uint32_t*>(&pr);
           }
-          l_part = l_part * alpha + psum;
+          l_part = l_part * alpha + ((p4[0] + p4[1]) + (p4[2] + p4[3]));
           if (last_tile) {
             ctl.lsum[hf][h] = l_part;
             sm_sync();
           }
           if (has_unit) {
             const int pb = my_u % NPB;
-            bool w = true;
-            if (my_u >= NPB) w = wait_cluster_or_abort(&ctl.p_free[pb], ((my_u / NPB) - 1) & 1, ctl, a.status);
-            w = !half_any(hf, !w);  // the half takes one branch: it meets at a barrier below
-            ok = ok && w;
-            if (w) {
-              // P row h of this unit (64 bf16 = 8 units of 16 B, 128-byte swizzle)
-              // and its Info into the local staging buffer, then one bulk copy
-              uint8_t* stg = smem + S0_STG_OFF + pb * P_STRIDE;
+            bool wf = true;
+            if (my_u >= NPB) wf = wait_cluster_or_abort(&ctl.p_free[pb], ((my_u / NPB) - 1) & 1, ctl, a.status);
+            // P row h of this unit (64 bf16 = 8 units of 16 B, 128-byte swizzle)
+            // and its Info into the local staging buffer, then one bulk copy
+            uint8_t* stg = smem + S0_STG_OFF + pb * P_STRIDE;
+            if (wf) {
               uint8_t* row = stg + (h >> 3) * 1024 + (h & 7) * 128;
 #pragma unroll
               for (int v = 0; v < 8; ++v)
@@ -453,7 +453,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
                     make_uint4(packed[4 * v], packed[4 * v + 1], packed[4 * v + 2], packed[4 * v + 3]);
               Info* inf = reinterpret_cast<Info*>(stg + P_BYTES);
               const bool last_unit = last_tile && (hf == 1 || nvalid <= UR);
-              inf->alpha[h] = alpha;
+              inf->alpha[h] = hf == 0 ? alpha : 1.f;  // the rescale applies before the tile's first unit
               if (last_unit) {
                 const float l = ctl.lsum[0][h] + ctl.lsum[1][h];
                 inf->l[h] = l;
@@ -461,17 +461,17 @@ __global__ void __launch_bounds__(NTHREADS, 1)
                 if (whole) a.lse[(size_t)seq * NH + h] = lse;
                 else a.part_lse[(size_t)(seq + chunk) * NH + h] = lse;
               }
-              if (h == 0) inf->flags = ((hf == 0 && any_rescale) ? FLAG_RESCALE : 0u) | (last_unit ? FLAG_LAST : 0u);
+              if (h == 0) inf->flags = last_unit ? FLAG_LAST : 0u;
               fence_proxy_async_smem();
-              half_sync(hf);
-              if (h == 0)
-                bulk_copy_to_cluster(peer_p + pb * P_STRIDE, stg, P_COPY_BYTES, peer_pfull + pb * 8);
             }
+            // the half meets here: the copy is issued only if every thread wrote its row
+            const bool all = half_all(hf, wf);
+            if (!all) ok = false;
+            if (all && h == 0) bulk_copy_to_cluster(peer_p + pb * P_STRIDE, stg, P_COPY_BYTES, peer_pfull + pb * 8);
           }
-          ok = !sm_any(!ok);
-          if (!ok) break;
           u += (nvalid > UR) ? 2 : 1;
         }
+        if (sm_any(!ok)) break;
         ++piece;
       }
     }
@@ -577,11 +577,11 @@ __global__ void __launch_bounds__(NTHREADS, 1)
             const float l = inf->l[h];
             inv_l = l > 0.f ? 1.f / l : 0.f;
           }
-          if ((flags & FLAG_RESCALE) && !first) {
+          // Rescale this warp's 32 rows of O when any of them has alpha != 1
+          // (never before a piece's first unit: its PV overwrites O).
+          if (!first && __any_sync(0xffffffffu, alpha != 1.f)) {
             // O must hold every earlier unit before it is rescaled
-            ok = wait_or_abort(&ctl.pv_done[(u - 1) % NPB], ((u - 1) / NPB) & 1, ctl, a.status);
-            ok = !cw_any(!ok);
-            if (!ok) break;
+            if (!wait_or_abort(&ctl.pv_done[(u - 1) % NPB], ((u - 1) / NPB) & 1, ctl, a.status)) ok = false;
             tc_fence_after();
 #pragma unroll 1
             for (int c = 0; c < DC; c += 16) {
@@ -615,7 +615,8 @@ __global__ void __launch_bounds__(NTHREADS, 1)
           tc_fence_before();
           __syncwarp();
           if (lane == 0) mbar_arrive(&ctl.unit_ready[pb]);
-          cw_sync();  // every correction thread has read this buffer's Info
+          ok = !cw_any(!ok);  // also: every correction thread has read this buffer's Info
+          if (!ok) break;
           if (ct == 0) {
             mbar_arrive_expect_tx(&ctl.p_full[pb], P_COPY_BYTES);  // arm the buffer's next use
             mbar_arrive_remote(peer_pfree + pb * 8);
