@@ -69,8 +69,8 @@ def committed_traffic(kernel_hash: str):
 
 class ClockSampler:
     """SM clock and clock-event (throttle) reasons sampled during the timed
-    region: NVML polled every ~1 ms from a thread (the region lasts tens of
-    milliseconds), with nvidia-smi as the fallback when NVML is missing."""
+    region: the driver's NVML library polled every ~1 ms from a thread (the
+    region lasts tens of milliseconds)."""
     REASONS = {0x8: "hw_slowdown", 0x40: "hw_thermal_slowdown", 0x20: "sw_thermal_slowdown", 0x4: "sw_power_cap"}
 
     def __init__(self, gpu_index: int):
@@ -82,16 +82,25 @@ class ClockSampler:
 
     def _poll(self):
         try:
-            import pynvml
-            pynvml.nvmlInit()
-            h = pynvml.nvmlDeviceGetHandleByIndex(self.gpu)
-            self.max_mhz = pynvml.nvmlDeviceGetMaxClockInfo(h, pynvml.NVML_CLOCK_SM)
-            get_reasons = getattr(pynvml, "nvmlDeviceGetCurrentClocksEventReasons", None) or \
-                pynvml.nvmlDeviceGetCurrentClocksThrottleReasons
+            import ctypes
+            nv = ctypes.CDLL("libnvidia-ml.so.1")
+            if nv.nvmlInit_v2() != 0:
+                raise RuntimeError("nvmlInit failed")
+            h = ctypes.c_void_p()
+            if nv.nvmlDeviceGetHandleByIndex_v2(ctypes.c_uint(self.gpu), ctypes.byref(h)) != 0:
+                raise RuntimeError("nvmlDeviceGetHandleByIndex failed")
+            clk, mx, reasons = ctypes.c_uint(), ctypes.c_uint(), ctypes.c_ulonglong()
+            NVML_CLOCK_SM = 1
+            if nv.nvmlDeviceGetMaxClockInfo(h, NVML_CLOCK_SM, ctypes.byref(mx)) == 0:
+                self.max_mhz = mx.value
+            get_reasons = getattr(nv, "nvmlDeviceGetCurrentClocksEventReasons", None) or \
+                nv.nvmlDeviceGetCurrentClocksThrottleReasons
             while not self.stop_flag.is_set():
-                self.samples.append((pynvml.nvmlDeviceGetClockInfo(h, pynvml.NVML_CLOCK_SM), int(get_reasons(h))))
+                if nv.nvmlDeviceGetClockInfo(h, NVML_CLOCK_SM, ctypes.byref(clk)) == 0 and \
+                        get_reasons(h, ctypes.byref(reasons)) == 0:
+                    self.samples.append((clk.value, int(reasons.value)))
                 time.sleep(0.001)
-            pynvml.nvmlShutdown()
+            nv.nvmlShutdown()
         except Exception as e:  # noqa: BLE001
             self.err = f"{type(e).__name__}: {e}"
 

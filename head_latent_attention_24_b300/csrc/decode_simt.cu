@@ -266,44 +266,51 @@ __global__ void __launch_bounds__(NT) decode_simt_kernel(const DecodeArgs a) {
 
 // One CTA per (sequence, head): merges the partial results of a split sequence
 // and writes o_lat = 0, lse = -inf for an empty one.
+// One warp per (sequence, head): the lanes reduce the pieces' LSEs with
+// shuffles and stream the fp32 partials with 16-byte loads (a warp reads 512
+// contiguous bytes per load), writing o_lat = sum_j e^{lse_j - lse} o_j.
 template <typename T>
-__global__ void __launch_bounds__(128) decode_combine_kernel(const DecodeArgs a) {
-  extern __shared__ float wts[];  // [max parts]
-  __shared__ float red[2];
-  const int b = blockIdx.x, h = blockIdx.y, tid = threadIdx.x;
+__global__ void __launch_bounds__(256) decode_combine_kernel(const DecodeArgs a) {
+  const int b = blockIdx.x, warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int h = blockIdx.y * 8 + warp;
   const int B = a.B, d_c = a.d_c;
+  if (h >= a.n_h) return;
   const int32_t* cum = a.plan;
   const int chunk_len = cum[B + 1];
   const int s0 = cum[b], s1 = cum[b + 1];
   T* o_out = static_cast<T*>(a.o_lat) + ((long long)b * a.n_h + h) * d_c;
   if (s1 == s0) {
-    for (int cc = tid; cc < d_c; cc += blockDim.x) o_out[cc] = from_f32<T>(0.f);
-    if (tid == 0) a.lse[(long long)b * a.n_h + h] = -INFINITY;
+    for (int cc = lane; cc < d_c; cc += 32) o_out[cc] = from_f32<T>(0.f);
+    if (lane == 0) a.lse[(long long)b * a.n_h + h] = -INFINITY;
     return;
   }
   const int c0 = s0 / chunk_len, c1 = (s1 - 1) / chunk_len;
   if (c0 == c1) return;  // written whole by the attention kernel
   const int np = c1 - c0 + 1;
-  if (tid == 0) {
-    float mx = -INFINITY;
-    for (int j = 0; j < np; ++j) mx = fmaxf(mx, a.part_lse[(long long)(b + c0 + j) * a.n_h + h]);
-    float sum = 0.f;
+  const float* plse = a.part_lse + (long long)(b + c0) * a.n_h + h;
+  float mx = -INFINITY;
+  for (int j = lane; j < np; j += 32) mx = fmaxf(mx, plse[(long long)j * a.n_h]);
+  mx = warp_max(mx);
+  float sum = 0.f;
+  for (int j = lane; j < np; j += 32) sum += expf(plse[(long long)j * a.n_h] - mx);
+  sum = warp_sum(sum);
+  const float inv = 1.f / sum;
+  const float* po = a.part_o + ((long long)(b + c0) * a.n_h + h) * d_c;
+  const long long pstride = (long long)a.n_h * d_c;
+  for (int e0 = lane * 4; e0 < d_c; e0 += 128) {
+    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
     for (int j = 0; j < np; ++j) {
-      const float w = expf(a.part_lse[(long long)(b + c0 + j) * a.n_h + h] - mx);
-      wts[j] = w;
-      sum += w;
+      const float w = expf(plse[(long long)j * a.n_h] - mx) * inv;
+      const float4 v = *reinterpret_cast<const float4*>(po + j * pstride + e0);
+      acc.x = fmaf(w, v.x, acc.x); acc.y = fmaf(w, v.y, acc.y);
+      acc.z = fmaf(w, v.z, acc.z); acc.w = fmaf(w, v.w, acc.w);
     }
-    red[0] = sum;
-    red[1] = mx;
+    o_out[e0] = from_f32<T>(acc.x);
+    o_out[e0 + 1] = from_f32<T>(acc.y);
+    o_out[e0 + 2] = from_f32<T>(acc.z);
+    o_out[e0 + 3] = from_f32<T>(acc.w);
   }
-  __syncthreads();
-  const float inv = 1.f / red[0];
-  for (int cc = tid; cc < d_c; cc += blockDim.x) {
-    float o = 0.f;
-    for (int j = 0; j < np; ++j) o = fmaf(wts[j], a.part_o[((long long)(b + c0 + j) * a.n_h + h) * d_c + cc], o);
-    o_out[cc] = from_f32<T>(o * inv);
-  }
-  if (tid == 0) a.lse[(long long)b * a.n_h + h] = red[1] + logf(red[0]);
+  if (lane == 0) a.lse[(long long)b * a.n_h + h] = mx + logf(sum);
 }
 
 }  // namespace
@@ -342,12 +349,11 @@ cudaError_t launch_decode_simt(const DecodeArgs& a, int dtype, cudaStream_t s, i
 }
 
 cudaError_t launch_decode_combine(const DecodeArgs& a, int dtype, cudaStream_t s) {
-  dim3 grid(a.B, a.n_h);
-  const size_t smem = sizeof(float) * ((size_t)a.grid_chunks + 1);
+  dim3 grid(a.B, (a.n_h + 7) / 8);
   if (dtype == MLA_BF16)
-    decode_combine_kernel<__nv_bfloat16><<<grid, 128, smem, s>>>(a);
+    decode_combine_kernel<__nv_bfloat16><<<grid, 256, 0, s>>>(a);
   else
-    decode_combine_kernel<float><<<grid, 128, smem, s>>>(a);
+    decode_combine_kernel<float><<<grid, 256, 0, s>>>(a);
   return cudaGetLastError();
 }
 
