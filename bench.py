@@ -132,20 +132,43 @@ def v2_shape():
     return S.workload("v2")
 
 
-def make_inputs(shp, device, seed_offset=0):
-    """Weights, context and new-token inputs on the device (seeded torch generator)."""
+def make_inputs(shp, device, rank=0):
+    """Weights (the same layer on every rank) and this rank's new-token inputs,
+    on the device, from seeded torch generators."""
     import torch
     import mla_synth as S
     g = torch.Generator(device=device)
-    g.manual_seed(shp.seed * 7919 + seed_offset)
+    g.manual_seed(shp.seed * 7919)
     W = {}
     for name in S.WEIGHT_NAMES:
         r, c = shp.weight_shape(name)
         W[name] = (torch.randn((r, c), generator=g, device=device) * (1.0 / shp.fan_in(name)) ** 0.5).to(
             torch.bfloat16).contiguous()
-    B, ctx = shp.batch, shp.ctx
-    h_new = torch.randn((B, shp.d), generator=g, device=device).to(torch.bfloat16).contiguous()
+    g.manual_seed(shp.seed * 7919 + 1 + rank)
+    h_new = torch.randn((shp.batch, shp.d), generator=g, device=device).to(torch.bfloat16).contiguous()
     return W, h_new
+
+
+def context_seq_id(b: int, rank: int) -> int:
+    """Generator id of sequence b of a rank's batch: distinct over ranks, so
+    each rank serves its own sequences (data parallel over the batch)."""
+    return b + 1000 * rank
+
+
+def max_over_ranks(x: float, device) -> float:
+    """The slowest rank's value of a per-rank time (the job ends with it)."""
+    import torch
+    import torch.distributed as dist
+    if not (dist.is_available() and dist.is_initialized()) or dist.get_world_size() == 1:
+        return x
+    t = torch.tensor([x], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_tokens_per_s(batch_per_rank: int, world: int, steps: int, max_ms: float) -> float:
+    """Whole-job throughput: every rank's tokens over the slowest rank's time."""
+    return batch_per_rank * world * steps / (max_ms * 1e-3)
 
 
 def build_cache(dec, shp, cache, device, rank=0):
@@ -157,7 +180,7 @@ def build_cache(dec, shp, cache, device, rank=0):
     per = max(1, 32768 // ctx)
     for b0 in range(0, B, per):
         bs = list(range(b0, min(B, b0 + per)))
-        x = torch.cat([S.context_h_device(shp, b + 1000 * rank, ctx, device) for b in bs], 0).contiguous()
+        x = torch.cat([S.context_h_device(shp, context_seq_id(b, rank), ctx, device) for b in bs], 0).contiguous()
         seq = torch.tensor(np.repeat(bs, ctx), dtype=torch.int32, device=device)
         pos = torch.tensor(np.tile(np.arange(ctx), len(bs)), dtype=torch.int32, device=device)
         dec.append(x, seq, pos, cache)
@@ -198,7 +221,7 @@ def run_ours(args, rank, world, local_rank):
     shp = v2_shape()
     B, ctx = shp.batch, shp.ctx
     max_len = ctx + 1
-    W, h_new = make_inputs(shp, device, seed_offset=rank)
+    W, h_new = make_inputs(shp, device, rank)
     ls = M.LayerShape(shp.d, shp.n_h, shp.d_h, shp.d_c, shp.d_r, shp.d_cq, "bf16", shp.rope_base)
     dec = M.MLADecoder(ls, W, B, max_len, max_pos=max_len)
     if args.decode_path != "auto":
@@ -258,10 +281,7 @@ def run_ours(args, rank, world, local_rank):
     total_ms = start.elapsed_time(end)
     attn_ms = [e[1].elapsed_time(e[2]) for e in evs]
     step_ms = [e[0].elapsed_time(e[3]) for e in evs]
-    if world > 1:
-        t = torch.tensor([total_ms], device=device)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        total_ms = float(t.item())
+    total_ms = max_over_ranks(total_ms, device)
 
     # ---- end to end through the public API: pinned host in, host out, every step
     h_host = torch.empty_like(h_new, device="cpu").pin_memory()
@@ -284,10 +304,7 @@ def run_ours(args, rank, world, local_rank):
         u_host.copy_(u, non_blocking=True)
         stream.synchronize()
     e2e_s = time.perf_counter() - t0
-    if world > 1:
-        t = torch.tensor([e2e_s], device=device)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        e2e_s = float(t.item())
+    e2e_s = max_over_ranks(e2e_s, device)
 
     st, bits = M.mla_get_device_status(dec.handle)
     if st != M.MLA_OK:
@@ -306,7 +323,7 @@ def run_ours(args, rank, world, local_rank):
     kh = kernel_source_hash()
     traffic = committed_traffic(kh)
     tokens = B * world * args.steps
-    value = tokens / (total_ms / 1e3)
+    value = job_tokens_per_s(B, world, args.steps, total_ms)
     weight_bytes = sum(v.numel() * 2 for v in W.values())
     step_roof_s = max((cache_bytes + weight_bytes) / (hbm * 1e9),
                       (flops + 2.0 * B * sum(v.numel() for v in W.values())) / (peaks["bf16_tflops"] * 1e12))
@@ -347,7 +364,7 @@ def run_ours(args, rank, world, local_rank):
         },
         "step_roofline_frac": round(step_roof_s / (total_ms / 1e3 / args.steps), 4),
         "e2e": {
-            "value": round(tokens / e2e_s, 1),
+            "value": round(job_tokens_per_s(B, world, args.steps, e2e_s * 1e3), 1),
             "unit": "tokens/s",
             "h2d_bytes_per_step": h_new.numel() * 2 + pos.numel() * 4 + seqlens.numel() * 4,
             "d2h_bytes_per_step": dec.u.numel() * 2,
