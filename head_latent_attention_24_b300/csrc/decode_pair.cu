@@ -21,13 +21,16 @@
 //     straight into CTA 1's shared memory.
 //   * CTA 1 ("value") keeps O = sum_t P_t c_KV_t in all of its TMEM and
 //     streams only the latent part of the same rows (mostly from L2, where
-//     CTA 0's loads left them): O += P . C (M = 128 heads, N = 128 latent
-//     columns x 4, K = 64 rows per unit). Its four correction warps apply the
+//     CTA 0's loads left them): O += P . C (M = 128 heads, N = 256 latent
+//     columns x 2, K = 64 rows per unit). Its four correction warps apply the
 //     rare softmax rescale to O, zero cache rows past a sequence end (P is 0
 //     there, but the rows may hold NaN), and write o_lat / partials at the end
 //     of each piece.
-// Every MMA has M = 128 and N = 128, the shapes that run at the full tensor
-// rate; only P (2 bytes per head and row) crosses between the SMs.
+// Every MMA has M = 128 and N >= 128, the shapes that run at the full tensor
+// rate; only P (2 bytes per head and row) crosses between the SMs. One thread
+// issues each CTA's MMAs, and at this rate its instruction count matters: the
+// issue loops are unrolled over a tile's boxes and add compile-time offsets to
+// shared-memory descriptors built once per kernel.
 //
 // Softmax: online, in base 2, with a lazy reference maximum per head: the
 // reference moves (and O is rescaled) only when a tile's maximum rises more
@@ -292,6 +295,8 @@ __global__ void __launch_bounds__(NTHREADS, 1)
         int piece = 0, g = 0, i = 0;
         bool ok = true;
         const uint32_t qr = sbase + S0_QR_OFF;
+        const uint64_t ring_desc = sdesc_sw128(sbase + S0_RING_OFF, 16, 1024);
+        const uint64_t qr_desc = sdesc_sw128(qr, 16, 1024);
         while (ok && it.next(seq, t0, t1, whole)) {
           ok = wait_or_abort(&ctl.q_ready, piece & 1, ctl, a.status);
           if (!ok) break;
@@ -302,22 +307,23 @@ __global__ void __launch_bounds__(NTHREADS, 1)
             if (!ok) break;
             tc_fence_after();
             const uint32_t d = tbase + S_COL + sb * TR;
-            for (int c0 = 0; c0 < NCH; c0 += S0_CPB, ++i) {
+#pragma unroll
+            for (int bx = 0; bx < NCH / S0_CPB; ++bx, ++i) {
               const int sl = i % S0_RING;
               ok = wait_or_abort(&ctl.r0_full[sl], (i / S0_RING) & 1, ctl, a.status);
               if (!ok) break;
               tc_fence_after();
+              const uint64_t bslot = ring_desc + (uint64_t)((sl * S0_SLOT) >> 4);
 #pragma unroll
               for (int cc = 0; cc < S0_CPB; ++cc) {
-                const int c = c0 + cc;
-                const uint32_t kb = sbase + S0_RING_OFF + sl * S0_SLOT + cc * S0_CHUNK;
+                const int c = bx * S0_CPB + cc;
 #pragma unroll
                 for (int k = 0; k < 4; ++k) {
-                  const uint64_t bd = sdesc_sw128(kb + k * 32, 16, 1024);
+                  const uint64_t bd = bslot + (uint64_t)((cc * S0_CHUNK + k * 32) >> 4);
                   if (c < NCH - 1)
                     mma_bf16_ta(d, tbase + QL_COL + c * 32 + k * 8, bd, IDESC, (c > 0 || k > 0) ? 1u : 0u);
                   else
-                    mma_bf16(d, sdesc_sw128(qr + k * 32, 16, 1024), bd, IDESC, 1u);
+                    mma_bf16(d, qr_desc + (uint64_t)((k * 32) >> 4), bd, IDESC, 1u);
                 }
               }
               mma_commit(&ctl.r0_empty[sl]);
@@ -506,7 +512,9 @@ __global__ void __launch_bounds__(NTHREADS, 1)
     } else if (warp == 1) {
       // ---------------------------------------------------------- MMA issuer (PV)
       if (lane == 0) {
-        constexpr uint32_t IDESC = idesc_bf16(128, 128, false, true);
+        constexpr uint32_t IDESC = idesc_bf16(128, 256, false, true);
+        const uint64_t p_desc = sdesc_sw128(sbase + S1_P_OFF, 16, 1024);
+        const uint64_t v_desc = sdesc_sw128(sbase + S1_RING_OFF, S1_CHUNK, 1024);
         Pieces it;
         it.init(a.plan, B, chunk);
         int seq, t0, t1;
@@ -522,22 +530,19 @@ __global__ void __launch_bounds__(NTHREADS, 1)
                  wait_or_abort(&ctl.unit_ready[pb], (u / NPB) & 1, ctl, a.status);
             if (!ok) break;
             tc_fence_after();
-            const uint32_t pa = sbase + S1_P_OFF + pb * P_STRIDE;
+            const uint64_t pd = p_desc + (uint64_t)((pb * P_STRIDE) >> 4);
+#pragma unroll
             for (int j = 0; j < 2; ++j, ++i) {
               const int sl = i % S1_RING;
               ok = wait_or_abort(&ctl.r1_full[sl], (i / S1_RING) & 1, ctl, a.status);
               if (!ok) break;
               tc_fence_after();
+              // latent columns [256 j, 256 j + 256): four 8 KB chunks, 8 KB apart
+              const uint64_t vd = v_desc + (uint64_t)((sl * S1_SLOT) >> 4);
 #pragma unroll
-              for (int nb2 = 0; nb2 < 2; ++nb2) {
-                // latent columns [256 j + 128 nb2, +128): two 8 KB chunks, 8 KB apart
-                const uint32_t vb = sbase + S1_RING_OFF + sl * S1_SLOT + nb2 * 2 * S1_CHUNK;
-#pragma unroll
-                for (int k = 0; k < 4; ++k) {
-                  mma_bf16(tbase + (2 * j + nb2) * 128, sdesc_sw128(pa + k * 32, 16, 1024),
-                           sdesc_sw128(vb + k * 2048, S1_CHUNK, 1024), IDESC, (first && k == 0) ? 0u : 1u);
-                }
-              }
+              for (int k = 0; k < 4; ++k)
+                mma_bf16(tbase + j * 256, pd + (uint64_t)((k * 32) >> 4), vd + (uint64_t)((k * 2048) >> 4), IDESC,
+                       (first && k == 0) ? 0u : 1u);
               mma_commit(&ctl.r1_empty[sl]);
             }
             if (!ok) break;

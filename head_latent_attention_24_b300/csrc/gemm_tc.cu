@@ -10,12 +10,21 @@
 // weight byte is read once, so the step is bound by weight bandwidth. The
 // weights are therefore the 128-row MMA operand A (TMA-streamed, K-major or,
 // for W_UK^T, MN-major) and the activation rows are the N dimension; the fp32
-// accumulator D[m][n] lives in TMEM. To spread a weight matrix over all SMs
-// the reduction is split along K across the CTAs of a thread-block cluster
-// (up to 8); each CTA writes its partial tile to its own shared memory and
-// the cluster sums the partials in a fixed order through distributed shared
-// memory, so results do not depend on timing. The same kernel, unsplit and
-// with N tiles of 256 rows, builds a whole context's cache rows.
+// accumulator D[m][n] lives in TMEM.
+//
+// A stage holds CPB (1, 2 or 4) column chunks of 64: the weight tile arrives
+// as one TMA box through a 4-D view {64 columns, rows, column chunks, batch}
+// with the chunk outside the row, which lands chunk-major in the 128-byte
+// swizzled K-major layout tcgen05 reads, and the activation chunks as a second
+// box. An SM completes only about two million TMA copies per second whatever
+// their size, so large boxes are what lets the weights stream at HBM speed.
+//
+// To spread a weight matrix over the SMs the reduction is split along K
+// across the CTAs of a thread-block cluster (up to 8); each CTA writes its
+// partial tile to its own shared memory and the cluster sums the partials in
+// a fixed order through distributed shared memory, so results do not depend
+// on timing. When there are more 128-row tiles than SMs (W_UK^T, batched over
+// heads), one CTA instead computes MT tiles that share their activations.
 //
 // Warp roles: warp 0 issues TMA, warp 1 owns TMEM and issues tcgen05.mma from
 // one thread, warps 2-5 drain TMEM, reduce and run the epilogue. Every
@@ -32,20 +41,21 @@ namespace {
 using namespace tc;
 
 constexpr int BM = 128;            // weight rows per tile (MMA M)
-constexpr int BK = 64;             // reduction columns per stage (128 B of bf16)
-constexpr int A_BYTES = BM * BK * 2;
+constexpr int BK = 64;             // reduction columns per chunk (128 B of bf16)
+constexpr int CHUNK_A = BM * BK * 2;   // 16 KB: one chunk of a weight tile
 constexpr int NTHREADS = 192;
 constexpr int MAX_SPLITS = 8;
+constexpr int MAX_MT = 4;
+constexpr int SMEM_BUDGET = 200 * 1024;
 constexpr long long WAIT_CYCLES = 4000000000LL;  // ~2 s
 
 struct Params {
   int mtiles0, mtiles_total;   // tiles of segment 0; of both segments
+  int mt;                      // 128-row tiles per CTA (> 1 only without split-K)
   int rows[2], col0[2];
   int N, K, Z;
-  int n_tile, nstage, stage_bytes, splits, kchunks;
+  int n_tile, nstage, stage_bytes, splits, kstages;
   uint32_t tmem_cols, idesc;
-  int w_transposed;
-  int x_swapped;               // X map dims are {K, Z, N} instead of {K, N, Z}
   int epi; void* out; long long ldo, bo;
   const float* rope_cos; const float* rope_sin; int d_r; int max_pos;
   const int32_t* pos; long long seg_stride; int seg_off;
@@ -71,26 +81,32 @@ __device__ __forceinline__ float rope_apply(float v, float partner, bool first_h
   return first_half ? (v * c - partner * s) : (v * c + partner * s);
 }
 
-__global__ void __launch_bounds__(NTHREADS, 2)
+// CPB: column chunks per stage. TRANS: the weights are stored [K rows][M
+// columns] and read MN-major (A'[m, k] = W[k, m]).
+template <int CPB, bool TRANS>
+__global__ void __launch_bounds__(NTHREADS, 1)
     gemm_tc_kernel(const __grid_constant__ CUtensorMap map_w0, const __grid_constant__ CUtensorMap map_w1,
                    const __grid_constant__ CUtensorMap map_x, const Params p) {
+  constexpr int A_TILE = CPB * CHUNK_A;   // one weight tile of one stage
+  constexpr int KSTEPS = CPB * (BK / 16);
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   __shared__ Ctl ctl;
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int S = p.splits;
-  const int tile = blockIdx.x / S, split = blockIdx.x % S;
-  const int seg = tile < p.mtiles0 ? 0 : 1;
-  const int m0 = (seg == 0 ? tile : tile - p.mtiles0) * BM;
+  const int S = p.splits, MT = p.mt;
+  const int group = blockIdx.x / S, split = blockIdx.x % S;
+  const int tile0 = group * MT;
+  const int seg = tile0 < p.mtiles0 ? 0 : 1;
+  const int m0 = (seg == 0 ? tile0 : tile0 - p.mtiles0) * BM;
   const int n0 = blockIdx.y * p.n_tile;
   const int z = blockIdx.z;
-  const int kc0 = (int)((long long)split * p.kchunks / S), kc1 = (int)((long long)(split + 1) * p.kchunks / S);
-  const int nk = kc1 - kc0;
+  const int ks0 = (int)((long long)split * p.kstages / S), ks1 = (int)((long long)(split + 1) * p.kstages / S);
+  const int nk = ks1 - ks0;
   const CUtensorMap* map_w = seg == 0 ? &map_w0 : &map_w1;
 
   if (threadIdx.x == 0) {
-    for (int s = 0; s < p.nstage; ++s) { mbar_init(&ctl.full[s], 1); mbar_init(&ctl.empty[s], 1); }
+    for (int i = 0; i < p.nstage; ++i) { mbar_init(&ctl.full[i], 1); mbar_init(&ctl.empty[i], 1); }
     mbar_init(&ctl.acc_full, 1);
     ctl.abort = 0;
     fence_mbar_init();
@@ -113,38 +129,44 @@ __global__ void __launch_bounds__(NTHREADS, 2)
       prefetch_tensormap(&map_x);
       const uint32_t bytes = (uint32_t)p.stage_bytes;
       for (int i = 0; i < nk; ++i) {
-        const int s = i % p.nstage;
-        if (i >= p.nstage && !wait_bar(&ctl.empty[s], ((i / p.nstage) - 1) & 1, ctl, p.status)) break;
-        uint8_t* sa = smem + s * p.stage_bytes;
-        uint8_t* sx = sa + A_BYTES;
-        const int k0 = (kc0 + i) * BK;
-        mbar_arrive_expect_tx(&ctl.full[s], bytes);
-        if (p.w_transposed) {
-          tma_load_3d(sa, map_w, &ctl.full[s], m0, k0, z);
-          tma_load_3d(sa + A_BYTES / 2, map_w, &ctl.full[s], m0 + 64, k0, z);
-        } else {
-          tma_load_3d(sa, map_w, &ctl.full[s], k0, m0, z);
+        const int st = i % p.nstage;
+        if (i >= p.nstage && !wait_bar(&ctl.empty[st], ((i / p.nstage) - 1) & 1, ctl, p.status)) break;
+        uint8_t* sa = smem + st * p.stage_bytes;
+        const int kc = (ks0 + i) * CPB;   // first column chunk of the stage
+        mbar_arrive_expect_tx(&ctl.full[st], bytes);
+        for (int t = 0; t < MT; ++t) {
+          if (TRANS) tma_load_4d(sa + t * A_TILE, map_w, &ctl.full[st], 0, kc * BK, (m0 + t * BM) / 64, z);
+          else tma_load_4d(sa + t * A_TILE, map_w, &ctl.full[st], 0, m0 + t * BM, kc, z);
         }
-        if (p.x_swapped) tma_load_3d(sx, &map_x, &ctl.full[s], k0, z, n0);
-        else tma_load_3d(sx, &map_x, &ctl.full[s], k0, n0, z);
+        tma_load_4d(sa + MT * A_TILE, &map_x, &ctl.full[st], 0, n0, kc, z);
       }
     }
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer
     if (lane == 0) {
+      // Descriptors are built once; each MMA adds a byte offset / 16 to the
+      // start-address field (shared addresses stay below 256 KB).
+      const uint32_t sbase = smem_u32(smem);
+      const uint64_t a_desc0 = TRANS ? sdesc_sw128(sbase, CPB * BK * 128, 1024) : sdesc_sw128(sbase, 16, 1024);
+      const uint64_t x_desc0 = sdesc_sw128(sbase, 16, 1024);
+      const uint32_t x_chunk = (uint32_t)p.n_tile * 128;
       for (int i = 0; i < nk; ++i) {
-        const int s = i % p.nstage;
-        if (!wait_bar(&ctl.full[s], (i / p.nstage) & 1, ctl, p.status)) break;
+        const int st = i % p.nstage;
+        if (!wait_bar(&ctl.full[st], (i / p.nstage) & 1, ctl, p.status)) break;
         tc_fence_after();
-        const uint32_t sa = smem_u32(smem + s * p.stage_bytes), sx = sa + A_BYTES;
+        const uint32_t soff = (uint32_t)(st * p.stage_bytes);
+        const uint64_t xd = x_desc0 + ((soff + (uint32_t)MT * A_TILE) >> 4);
+        for (int t = 0; t < MT; ++t) {
+          const uint64_t ad = a_desc0 + ((soff + (uint32_t)t * A_TILE) >> 4);
+          const uint32_t d = tbase + (uint32_t)(t * p.n_tile);
 #pragma unroll
-        for (int k = 0; k < BK / 16; ++k) {
-          const uint64_t ad = p.w_transposed ? sdesc_sw128(sa + k * 2048, A_BYTES / 2, 1024)
-                                             : sdesc_sw128(sa + k * 32, 16, 1024);
-          const uint64_t bd = sdesc_sw128(sx + k * 32, 16, 1024);
-          mma_bf16(tbase, ad, bd, p.idesc, (i > 0 || k > 0) ? 1u : 0u);
+          for (int kk = 0; kk < KSTEPS; ++kk) {
+            const uint32_t a_off = TRANS ? (uint32_t)(kk * 2048) : (uint32_t)((kk >> 2) * CHUNK_A + (kk & 3) * 32);
+            const uint64_t xk = xd + (((uint32_t)(kk >> 2) * x_chunk + (uint32_t)(kk & 3) * 32) >> 4);
+            mma_bf16(d, ad + (a_off >> 4), xk, p.idesc, (i > 0 || kk > 0) ? 1u : 0u);
+          }
         }
-        mma_commit(&ctl.empty[s]);
+        mma_commit(&ctl.empty[st]);
       }
       mma_commit(&ctl.acc_full);
     }
@@ -152,20 +174,22 @@ __global__ void __launch_bounds__(NTHREADS, 2)
     // ------------------------------------------------------------ epilogue warps 2..5
     const int quarter = warp & 3;
     const int m = quarter * 32 + lane;           // this thread's TMEM lane = tile row
-    float* cs = reinterpret_cast<float*>(smem);  // [n_tile][BM] partial, reuses the stages
+    float* cs = reinterpret_cast<float*>(smem);  // [MT][n_tile][BM] partials, reuses the stages
     const bool ok = nk > 0 && wait_bar(&ctl.acc_full, 0, ctl, p.status);
     if (ok) tc_fence_after();
-    for (int c = 0; c < p.n_tile; c += 16) {
-      float v[16];
-      if (ok) {
-        tmem_ld16(tbase + (static_cast<uint32_t>(quarter * 32) << 16) + c, v);
-        tmem_ld_wait();
-      } else {
+    for (int t = 0; t < MT; ++t) {
+      for (int c = 0; c < p.n_tile; c += 16) {
+        float v[16];
+        if (ok) {
+          tmem_ld16(tbase + (static_cast<uint32_t>(quarter * 32) << 16) + (uint32_t)(t * p.n_tile + c), v);
+          tmem_ld_wait();
+        } else {
 #pragma unroll
-        for (int i = 0; i < 16; ++i) v[i] = 0.f;
+          for (int i = 0; i < 16; ++i) v[i] = 0.f;
+        }
+#pragma unroll
+        for (int i = 0; i < 16; ++i) cs[(t * p.n_tile + c + i) * BM + m] = v[i];
       }
-#pragma unroll
-      for (int i = 0; i < 16; ++i) cs[(c + i) * BM + m] = v[i];
     }
   }
 
@@ -174,80 +198,79 @@ __global__ void __launch_bounds__(NTHREADS, 2)
   tc_fence_before();
   cluster_sync();  // every partial tile of the cluster is in shared memory
   const int n_valid = min(p.n_tile, p.N - n0);
-  if (warp >= 2) {
+  if (warp >= 2 && S > 1) {
+    // MT == 1 whenever S > 1
     const int et = threadIdx.x - 64;
     float* cs = reinterpret_cast<float*>(smem);
-    if (S > 1) {
-      const uint32_t cs_addr = smem_u32(cs);
-      const int rgrp = et >> 5, m4 = (et & 31) * 4;
-      for (int n = split + S * rgrp; n < n_valid; n += 4 * S) {
-        float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-        const uint32_t off = (uint32_t)((n * BM + m4) * 4);
-        for (int r = 0; r < S; ++r) {
-          const uint32_t a = mapa_shared(cs_addr + off, (uint32_t)r);
-          float4 v;
-          asm volatile("ld.shared::cluster.v4.f32 {%0,%1,%2,%3}, [%4];"
-                       : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w)
-                       : "r"(a)
-                       : "memory");
-          acc.x += v.x; acc.y += v.y; acc.z += v.z; acc.w += v.w;
-        }
-        // Peers may still be reading this CTA's partials: the sum goes to a
-        // separate region holding this CTA's own rows.
-        *reinterpret_cast<float4*>(cs + p.n_tile * BM + (n / S) * BM + m4) = acc;
+    const uint32_t cs_addr = smem_u32(cs);
+    const int rgrp = et >> 5, m4 = (et & 31) * 4;
+    for (int n = split + S * rgrp; n < n_valid; n += 4 * S) {
+      float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+      const uint32_t off = (uint32_t)((n * BM + m4) * 4);
+      for (int r = 0; r < S; ++r) {
+        const uint32_t a = mapa_shared(cs_addr + off, (uint32_t)r);
+        float4 v;
+        asm volatile("ld.shared::cluster.v4.f32 {%0,%1,%2,%3}, [%4];"
+                     : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w)
+                     : "r"(a)
+                     : "memory");
+        acc.x += v.x; acc.y += v.y; acc.z += v.z; acc.w += v.w;
       }
+      // Peers may still be reading this CTA's partials: the sum goes to a
+      // separate region holding this CTA's own rows.
+      *reinterpret_cast<float4*>(cs + p.n_tile * BM + (n / S) * BM + m4) = acc;
     }
   }
   cluster_sync();  // all remote reads done: no CTA's shared memory is needed by a peer any more
   if (warp >= 2) {
     const int et = threadIdx.x - 64;
     const float* cs = reinterpret_cast<const float*>(smem);
-    // reduced rows: own rows n = split + S*j sit at (n_tile + j) rows when S > 1
     __nv_bfloat16* out = static_cast<__nv_bfloat16*>(p.out);
-    const int mm = m0 + et;  // row within the segment
-    const bool m_ok = mm < p.rows[seg];
-    for (int n = split; n < n_valid; n += S) {
-      const float* row = S > 1 ? cs + (p.n_tile + n / S) * BM : cs + n * BM;
-      const long long gn = (long long)n0 + n;
-      if (!m_ok) continue;
-      const float v = row[et];
-      if (p.epi == EPI_STORE) {
-        out[z * p.bo + gn * p.ldo + p.col0[seg] + mm] = __float2bfloat16_rn(v);
-      } else if (p.epi == EPI_ROPE_SEGS) {
-        const int half = p.d_r / 2;
-        const int sg = mm / p.d_r, j = mm % p.d_r;
-        int ps = p.pos[gn];
-        if (ps < 0 || ps >= p.max_pos) {
-          if (j == 0 && sg == 0) atomicOr(p.status, MLA_DEV_QPOS_RANGE);
-          ps = ps < 0 ? 0 : p.max_pos - 1;
-        }
-        const int jj = j < half ? j : j - half;
-        const float c = p.rope_cos[(long long)ps * half + jj], s = p.rope_sin[(long long)ps * half + jj];
-        const float partner = j < half ? row[et + half] : row[et - half];
-        out[gn * p.ldo + sg * p.seg_stride + p.seg_off + j] = __float2bfloat16_rn(rope_apply(v, partner, j < half, c, s));
-      } else {  // EPI_APPEND
-        const int sq = p.tok_seq[gn], ps = p.tok_pos[gn];
-        const bool seq_ok = sq >= 0 && sq < p.cache_batch;
-        const bool pos_ok = ps >= 0 && ps < p.max_len && ps < p.max_pos;
-        const int gm = p.col0[seg] + mm;
-        if (!seq_ok || !pos_ok) {
-          if (gm == 0) atomicOr(p.status, (seq_ok ? 0 : MLA_DEV_SEQ_RANGE) | (pos_ok ? 0 : MLA_DEV_POS_RANGE));
-          continue;
-        }
-        float r = v;
-        if (gm >= p.d_c) {
+    for (int t = 0; t < MT; ++t) {
+      // reduced rows: own rows n = split + S*j sit at (n_tile + j) rows when S > 1
+      const int mm = m0 + t * BM + et;  // row within the segment
+      if (mm >= p.rows[seg]) continue;
+      for (int n = split; n < n_valid; n += S) {
+        const float* row = S > 1 ? cs + (p.n_tile + n / S) * BM : cs + (t * p.n_tile + n) * BM;
+        const long long gn = (long long)n0 + n;
+        const float v = row[et];
+        if (p.epi == EPI_STORE) {
+          out[z * p.bo + gn * p.ldo + p.col0[seg] + mm] = __float2bfloat16_rn(v);
+        } else if (p.epi == EPI_ROPE_SEGS) {
           const int half = p.d_r / 2;
-          const int j = gm - p.d_c;
+          const int sg = mm / p.d_r, j = mm % p.d_r;
+          int ps = p.pos[gn];
+          if (ps < 0 || ps >= p.max_pos) {
+            if (j == 0 && sg == 0) atomicOr(p.status, MLA_DEV_QPOS_RANGE);
+            ps = ps < 0 ? 0 : p.max_pos - 1;
+          }
           const int jj = j < half ? j : j - half;
-          const float c = p.rope_cos[(long long)ps * half + jj], s = p.rope_sin[(long long)ps * half + jj];
+          const float c = p.rope_cos[(long long)ps * half + jj], sn = p.rope_sin[(long long)ps * half + jj];
           const float partner = j < half ? row[et + half] : row[et - half];
-          r = rope_apply(v, partner, j < half, c, s);
+          out[gn * p.ldo + sg * p.seg_stride + p.seg_off + j] = __float2bfloat16_rn(rope_apply(v, partner, j < half, c, sn));
+        } else {  // EPI_APPEND
+          const int sq = p.tok_seq[gn], ps = p.tok_pos[gn];
+          const bool seq_ok = sq >= 0 && sq < p.cache_batch;
+          const bool pos_ok = ps >= 0 && ps < p.max_len && ps < p.max_pos;
+          const int gm = p.col0[seg] + mm;
+          if (!seq_ok || !pos_ok) {
+            if (gm == 0) atomicOr(p.status, (seq_ok ? 0 : MLA_DEV_SEQ_RANGE) | (pos_ok ? 0 : MLA_DEV_POS_RANGE));
+            continue;
+          }
+          float r = v;
+          if (gm >= p.d_c) {
+            const int half = p.d_r / 2;
+            const int j = gm - p.d_c;
+            const int jj = j < half ? j : j - half;
+            const float c = p.rope_cos[(long long)ps * half + jj], sn = p.rope_sin[(long long)ps * half + jj];
+            const float partner = j < half ? row[et + half] : row[et - half];
+            r = rope_apply(v, partner, j < half, c, sn);
+          }
+          out[((long long)sq * p.max_len + ps) * p.row_width + gm] = __float2bfloat16_rn(r);
         }
-        out[((long long)sq * p.max_len + ps) * p.row_width + gm] = __float2bfloat16_rn(r);
       }
     }
   }
-
   __syncwarp();
   tc_fence_before();
   __syncthreads();
@@ -261,14 +284,43 @@ uint32_t pow2_at_least(uint32_t x) {
   return r;
 }
 
+template <int CPB, bool TRANS>
+cudaError_t launch_typed(const CUtensorMap* mw, const CUtensorMap& mx, const Params& p, dim3 grid, size_t smem_dyn,
+                         cudaStream_t s) {
+  static size_t smem_set = 0;  // per instantiation: the largest size requested so far
+  if (smem_dyn > smem_set) {
+    cudaError_t e = cudaFuncSetAttribute(gemm_tc_kernel<CPB, TRANS>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         (int)smem_dyn);
+    if (e != cudaSuccess) return e;
+    smem_set = smem_dyn;
+  }
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = dim3(NTHREADS);
+  cfg.dynamicSmemBytes = smem_dyn;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = (unsigned)p.splits;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  cudaError_t e = cudaLaunchKernelEx(&cfg, gemm_tc_kernel<CPB, TRANS>, mw[0], mw[1], mx, p);
+  if (e != cudaSuccess) return e;
+  return cudaGetLastError();
+}
+
 }  // namespace
 
 bool gemm_tc_shape_ok(const TcGemm& g) {
   if (g.N <= 0 || g.K <= 0 || g.Z <= 0 || g.nseg < 1 || g.nseg > 2) return false;
-  if ((g.K % 8) || (g.ldx % 8) || (g.bx % 8) || (g.ldw % 8) || (g.bw % 8)) return false;
+  // Column chunks of 64 must not run past a row: the chunked views have no
+  // per-row bound inside a chunk.
+  if ((g.K % BK) || (g.ldx % 8) || (g.bx % 8) || (g.ldw % 8) || (g.bw % 8)) return false;
   for (int s = 0; s < g.nseg; ++s) {
     if (g.rows[s] <= 0 || !g.w[s] || (reinterpret_cast<uintptr_t>(g.w[s]) & 15)) return false;
-    if (g.w_transposed && (g.rows[s] % 8)) return false;
+    if (g.w_transposed && (g.rows[s] % 64)) return false;
   }
   if (reinterpret_cast<uintptr_t>(g.x) & 15) return false;
   if (g.nseg == 2 && g.w_transposed) return false;
@@ -287,92 +339,93 @@ cudaError_t launch_gemm_tc(const TcGemm& g, int num_sms, cudaStream_t s) {
   p.mtiles_total = p.mtiles0 + (g.nseg == 2 ? (g.rows[1] + BM - 1) / BM : 0);
   p.N = g.N; p.K = g.K; p.Z = g.Z;
   p.n_tile = g.N >= 256 ? 256 : ((g.N + 15) / 16) * 16;
-  p.stage_bytes = A_BYTES + p.n_tile * 128;
-  const int ctas_per_sm = p.n_tile <= 64 ? 2 : 1;
-  const int smem_budget = ctas_per_sm == 2 ? 100 * 1024 : 200 * 1024;
-  p.nstage = smem_budget / p.stage_bytes;
-  if (p.nstage > 8) p.nstage = 8;
-  if (p.nstage < 2) return cudaErrorInvalidValue;
-  p.kchunks = (g.K + BK - 1) / BK;
+  const int kchunks = g.K / BK;
   const long long n_tiles = (g.N + p.n_tile - 1) / p.n_tile;
   if (n_tiles > 65535 || g.Z > 65535) return cudaErrorInvalidValue;
-  const long long tiles = (long long)p.mtiles_total * n_tiles * g.Z;
-  long long S = tiles >= (long long)num_sms * ctas_per_sm ? 1 : ((long long)num_sms * ctas_per_sm) / tiles;
+  if (num_sms < 1) num_sms = 1;
+
+  // Tiles per CTA: more than one only when the tiles outnumber the SMs and
+  // split-K is therefore off (one segment; the tiles' accumulators fit TMEM).
+  int mt = 1;
+  const long long tiles1 = (long long)p.mtiles_total * n_tiles * g.Z;
+  if (tiles1 > num_sms && g.nseg == 1 && g.epi == EPI_STORE) {
+    for (int c = 2; c <= MAX_MT; c *= 2)
+      if (p.mtiles_total % c == 0 && c * p.n_tile <= 512) {
+        mt = c;
+        if (tiles1 / c <= num_sms) break;
+      }
+  }
+  p.mt = mt;
+  // Chunks per stage: as many as keep two stages within the budget (one
+  // stage if it is the only one), at most what the reduction has.
+  auto stage_of = [&](int cpb) { return mt * cpb * CHUNK_A + cpb * p.n_tile * 128; };
+  int cpb = 4;
+  while (cpb > 1 && (cpb > kchunks || 2 * stage_of(cpb) > SMEM_BUDGET) &&
+         !(cpb <= kchunks && (kchunks + cpb - 1) / cpb == 1 && stage_of(cpb) <= SMEM_BUDGET))
+    cpb >>= 1;
+  p.stage_bytes = stage_of(cpb);
+  if (p.stage_bytes > SMEM_BUDGET) return cudaErrorInvalidValue;
+  p.kstages = (kchunks + cpb - 1) / cpb;
+  p.nstage = SMEM_BUDGET / p.stage_bytes;
+  if (p.nstage > 8) p.nstage = 8;
+  if (p.nstage > p.kstages) p.nstage = p.kstages;
+  const long long tiles = tiles1 / mt;
+  long long S = tiles >= num_sms ? 1 : num_sms / tiles;
   if (S > MAX_SPLITS) S = MAX_SPLITS;
-  if (S > p.kchunks) S = p.kchunks;
-  if (S < 1) S = 1;
+  if (S > p.kstages) S = p.kstages;
+  if (mt > 1 || S < 1) S = 1;
   p.splits = (int)S;
-  // Partial tile [n_tile][128] fp32, plus the reduced own rows when split.
-  const size_t cs_bytes = (size_t)p.n_tile * BM * 4 + (S > 1 ? (size_t)((p.n_tile + S - 1) / S) * BM * 4 : 0);
-  const size_t smem = (size_t)p.nstage * p.stage_bytes;
-  const size_t smem_dyn = (cs_bytes > smem ? cs_bytes : smem) + 1024;
-  p.tmem_cols = pow2_at_least((uint32_t)p.n_tile);
+  // Partial tiles [MT][n_tile][128] fp32, plus the reduced own rows when split.
+  const size_t cs_bytes = (size_t)mt * p.n_tile * BM * 4 + (S > 1 ? (size_t)((p.n_tile + S - 1) / S) * BM * 4 : 0);
+  const size_t stages = (size_t)p.nstage * p.stage_bytes;
+  const size_t smem_dyn = (cs_bytes > stages ? cs_bytes : stages) + 1024;
+  p.tmem_cols = pow2_at_least((uint32_t)(mt * p.n_tile));
   p.idesc = idesc_bf16(BM, p.n_tile, g.w_transposed != 0, false);
-  p.w_transposed = g.w_transposed;
   p.epi = g.epi; p.out = g.out; p.ldo = g.ldo; p.bo = g.bo;
   p.rope_cos = g.rope_cos; p.rope_sin = g.rope_sin; p.d_r = g.d_r; p.max_pos = g.max_pos;
   p.pos = g.pos; p.seg_stride = g.seg_stride; p.seg_off = g.seg_off;
   p.tok_seq = g.tok_seq; p.tok_pos = g.tok_pos; p.cache_batch = g.cache_batch; p.max_len = g.max_len;
   p.d_c = g.d_c; p.row_width = g.row_width; p.status = g.status;
 
-  // Tensor maps. Weights: {K, rows, Z} K-major, or {rows, K, Z} when stored
-  // transposed. Activations: {K, N, Z}, or {K, Z, N} when the batch stride is
-  // the smaller one (per-head slices of one row), so strides grow outward.
+  // Tensor maps, all 4-D with the column chunk outside the row:
+  //   weights    {64, rows, K/64, Z}   box {64, 128, CPB, 1}
+  //   transposed {64, K, rows/64, Z}   box {64, 64 CPB, 2, 1}   (stored [K][rows])
+  //   activation {64, N, K/64, Z}      box {64, n_tile, CPB, 1}
   CUtensorMap mw[2], mx;
   for (int sg = 0; sg < 2; ++sg) {
     const int src = sg < g.nseg ? sg : 0;
-    uint64_t dims[3], strides[2];
-    uint32_t box[3];
+    uint64_t dims[4], strides[3];
+    uint32_t box[4];
+    // with one batch the outer stride is never stepped; give it the tensor's size
+    const uint64_t zstride = g.Z > 1 ? (uint64_t)g.bw * 2
+                                     : (uint64_t)(g.w_transposed ? g.K : g.rows[src]) * (uint64_t)g.ldw * 2;
     if (g.w_transposed) {
-      dims[0] = (uint64_t)g.rows[src]; dims[1] = (uint64_t)g.K; dims[2] = (uint64_t)g.Z;
-      box[0] = 64; box[1] = 64; box[2] = 1;
+      dims[0] = 64; dims[1] = (uint64_t)g.K; dims[2] = (uint64_t)g.rows[src] / 64; dims[3] = (uint64_t)g.Z;
+      strides[0] = (uint64_t)g.ldw * 2; strides[1] = 128; strides[2] = zstride;
+      box[0] = 64; box[1] = (uint32_t)(cpb * BK); box[2] = 2; box[3] = 1;
     } else {
-      dims[0] = (uint64_t)g.K; dims[1] = (uint64_t)g.rows[src]; dims[2] = (uint64_t)g.Z;
-      box[0] = 64; box[1] = BM; box[2] = 1;
+      dims[0] = 64; dims[1] = (uint64_t)g.rows[src]; dims[2] = (uint64_t)kchunks; dims[3] = (uint64_t)g.Z;
+      strides[0] = (uint64_t)g.ldw * 2; strides[1] = 128; strides[2] = zstride;
+      box[0] = 64; box[1] = BM; box[2] = (uint32_t)cpb; box[3] = 1;
     }
-    strides[0] = (uint64_t)g.ldw * 2;
-    strides[1] = g.Z > 1 ? (uint64_t)g.bw * 2 : strides[0] * dims[1];
-    if (!make_tmap_3d_bf16_sw128(&mw[sg], g.w[src], dims, strides, box)) return cudaErrorInvalidValue;
+    if (!make_tmap_4d_bf16_sw128(&mw[sg], g.w[src], dims, strides, box)) return cudaErrorInvalidValue;
   }
   {
-    uint64_t dims[3], strides[2];
-    uint32_t box[3];
-    p.x_swapped = g.Z > 1 && g.bx < g.ldx;
-    if (p.x_swapped) {
-      dims[0] = (uint64_t)g.K; dims[1] = (uint64_t)g.Z; dims[2] = (uint64_t)g.N;
-      strides[0] = (uint64_t)g.bx * 2; strides[1] = (uint64_t)g.ldx * 2;
-      box[0] = 64; box[1] = 1; box[2] = (uint32_t)p.n_tile;
-    } else {
-      dims[0] = (uint64_t)g.K; dims[1] = (uint64_t)g.N; dims[2] = (uint64_t)g.Z;
-      strides[0] = (uint64_t)g.ldx * 2;
-      strides[1] = g.Z > 1 ? (uint64_t)g.bx * 2 : strides[0] * dims[1];
-      box[0] = 64; box[1] = (uint32_t)p.n_tile; box[2] = 1;
-    }
-    if (!make_tmap_3d_bf16_sw128(&mx, g.x, dims, strides, box)) return cudaErrorInvalidValue;
+    uint64_t dims[4] = {64, (uint64_t)g.N, (uint64_t)kchunks, (uint64_t)g.Z};
+    uint64_t strides[3] = {(uint64_t)g.ldx * 2, 128, g.Z > 1 ? (uint64_t)g.bx * 2 : (uint64_t)g.N * g.ldx * 2};
+    uint32_t box[4] = {64, (uint32_t)p.n_tile, (uint32_t)cpb, 1};
+    if (!make_tmap_4d_bf16_sw128(&mx, g.x, dims, strides, box)) return cudaErrorInvalidValue;
   }
 
-  static int smem_set = 0;  // largest dynamic shared-memory size requested so far
-  cudaError_t e = cudaSuccess;
-  if ((int)smem_dyn > smem_set) {
-    e = cudaFuncSetAttribute(gemm_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, 200 * 1024 + 2048);
-    if (e != cudaSuccess) return e;
-    smem_set = 200 * 1024 + 2048;
+  const dim3 grid((unsigned)(p.mtiles_total / mt * S), (unsigned)n_tiles, (unsigned)g.Z);
+  if (g.w_transposed) {
+    if (cpb == 4) return launch_typed<4, true>(mw, mx, p, grid, smem_dyn, s);
+    if (cpb == 2) return launch_typed<2, true>(mw, mx, p, grid, smem_dyn, s);
+    return launch_typed<1, true>(mw, mx, p, grid, smem_dyn, s);
   }
-  cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3((unsigned)(p.mtiles_total * S), (unsigned)n_tiles, (unsigned)g.Z);
-  cfg.blockDim = dim3(NTHREADS);
-  cfg.dynamicSmemBytes = smem_dyn;
-  cfg.stream = s;
-  cudaLaunchAttribute attr[1];
-  attr[0].id = cudaLaunchAttributeClusterDimension;
-  attr[0].val.clusterDim.x = (unsigned)S;
-  attr[0].val.clusterDim.y = 1;
-  attr[0].val.clusterDim.z = 1;
-  cfg.attrs = attr;
-  cfg.numAttrs = 1;
-  e = cudaLaunchKernelEx(&cfg, gemm_tc_kernel, mw[0], mw[1], mx, p);
-  if (e != cudaSuccess) return e;
-  return cudaGetLastError();
+  if (cpb == 4) return launch_typed<4, false>(mw, mx, p, grid, smem_dyn, s);
+  if (cpb == 2) return launch_typed<2, false>(mw, mx, p, grid, smem_dyn, s);
+  return launch_typed<1, false>(mw, mx, p, grid, smem_dyn, s);
 }
 
 }  // namespace mla

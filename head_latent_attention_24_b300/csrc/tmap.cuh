@@ -17,4 +17,7 @@ bool make_tmap_2d_bf16_sw128(CUtensorMap* map, const void* base, uint64_t inner,
 // rejects the map.
 bool make_tmap_3d_bf16_sw128(CUtensorMap* map, const void* base, const uint64_t dims[3],
                              const uint64_t strides[2], const uint32_t box[3]);
+// 4-D form of the above: byte strides strides[0..2] between steps of dims 1..3.
+bool make_tmap_4d_bf16_sw128(CUtensorMap* map, const void* base, const uint64_t dims[4],
+                             const uint64_t strides[3], const uint32_t box[4]);
 }  // namespace mla
