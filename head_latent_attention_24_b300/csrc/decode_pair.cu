@@ -253,6 +253,8 @@ __global__ void __launch_bounds__(NTHREADS, 1)
   cluster_sync();  // both CTAs' barriers are initialised before any remote arrive
   tc_fence_after();
   const uint32_t tbase = ctl.tmem_base;
+  pdl_trigger();
+  pdl_wait();      // the plan, the queries and the cache come from earlier kernels
   const uint32_t sbase = smem_u32(smem);
   const float sl2 = a.scale_log2;
 
@@ -705,19 +707,8 @@ cudaError_t launch_decode_tc(const mla_handle_s* h, const DecodeArgs& a, cudaStr
     if (e != cudaSuccess) return e;
     attr_set = true;
   }
-  cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3((unsigned)(2 * a.grid_chunks));
-  cfg.blockDim = dim3(NTHREADS);
-  cfg.dynamicSmemBytes = SMEM_DYN;
-  cfg.stream = s;
-  cudaLaunchAttribute attr[1];
-  attr[0].id = cudaLaunchAttributeClusterDimension;
-  attr[0].val.clusterDim.x = 2;
-  attr[0].val.clusterDim.y = 1;
-  attr[0].val.clusterDim.z = 1;
-  cfg.attrs = attr;
-  cfg.numAttrs = 1;
-  e = cudaLaunchKernelEx(&cfg, decode_pair_kernel, map_kv0, map_kv1, a);
+  LaunchCfg lc(dim3((unsigned)(2 * a.grid_chunks)), dim3(NTHREADS), SMEM_DYN, s, 2);
+  e = cudaLaunchKernelEx(&lc.cfg, decode_pair_kernel, map_kv0, map_kv1, a);
   if (e != cudaSuccess) return e;
   e = cudaGetLastError();
   if (e != cudaSuccess) return e;

@@ -67,6 +67,8 @@ __global__ void __launch_bounds__(1024) decode_plan_kernel(const int32_t* __rest
                                                            int32_t* __restrict__ status) {
   __shared__ int warp_tot[32];
   __shared__ int carry;
+  pdl_trigger();
+  pdl_wait();
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   if (tid == 0) { carry = 0; plan[0] = 0; }
   __syncthreads();
@@ -271,6 +273,8 @@ __global__ void __launch_bounds__(NT) decode_simt_kernel(const DecodeArgs a) {
 // contiguous bytes per load), writing o_lat = sum_j e^{lse_j - lse} o_j.
 template <typename T>
 __global__ void __launch_bounds__(256) decode_combine_kernel(const DecodeArgs a) {
+  pdl_trigger();
+  pdl_wait();
   const int b = blockIdx.x, warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int h = blockIdx.y * 8 + warp;
   const int B = a.B, d_c = a.d_c;
@@ -323,7 +327,9 @@ int decode_simt_chunks(const mla_handle_s* h) {
 
 cudaError_t launch_decode_plan(const int32_t* seqlens, int B, int max_len, int chunks, int granule,
                                int32_t* plan, int32_t* status, cudaStream_t s) {
-  decode_plan_kernel<<<1, 1024, 0, s>>>(seqlens, B, max_len, chunks, granule, plan, status);
+  LaunchCfg lc(dim3(1), dim3(1024), 0, s);
+  cudaError_t e = cudaLaunchKernelEx(&lc.cfg, decode_plan_kernel, seqlens, B, max_len, chunks, granule, plan, status);
+  if (e != cudaSuccess) return e;
   return cudaGetLastError();
 }
 
@@ -349,11 +355,10 @@ cudaError_t launch_decode_simt(const DecodeArgs& a, int dtype, cudaStream_t s, i
 }
 
 cudaError_t launch_decode_combine(const DecodeArgs& a, int dtype, cudaStream_t s) {
-  dim3 grid(a.B, (a.n_h + 7) / 8);
-  if (dtype == MLA_BF16)
-    decode_combine_kernel<__nv_bfloat16><<<grid, 256, 0, s>>>(a);
-  else
-    decode_combine_kernel<float><<<grid, 256, 0, s>>>(a);
+  LaunchCfg lc(dim3(a.B, (a.n_h + 7) / 8), dim3(256), 0, s);
+  cudaError_t e = dtype == MLA_BF16 ? cudaLaunchKernelEx(&lc.cfg, decode_combine_kernel<__nv_bfloat16>, a)
+                                    : cudaLaunchKernelEx(&lc.cfg, decode_combine_kernel<float>, a);
+  if (e != cudaSuccess) return e;
   return cudaGetLastError();
 }
 

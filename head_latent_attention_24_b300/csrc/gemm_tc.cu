@@ -121,6 +121,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tbase = ctl.tmem_base;
+  pdl_trigger();
 
   if (warp == 0) {
     // ------------------------------------------------------------ TMA producer
@@ -128,17 +129,34 @@ __global__ void __launch_bounds__(NTHREADS, 1)
       prefetch_tensormap(map_w);
       prefetch_tensormap(&map_x);
       const uint32_t bytes = (uint32_t)p.stage_bytes;
-      for (int i = 0; i < nk; ++i) {
+      auto load_w = [&](int i) {
         const int st = i % p.nstage;
-        if (i >= p.nstage && !wait_bar(&ctl.empty[st], ((i / p.nstage) - 1) & 1, ctl, p.status)) break;
         uint8_t* sa = smem + st * p.stage_bytes;
         const int kc = (ks0 + i) * CPB;   // first column chunk of the stage
-        mbar_arrive_expect_tx(&ctl.full[st], bytes);
         for (int t = 0; t < MT; ++t) {
           if (TRANS) tma_load_4d(sa + t * A_TILE, map_w, &ctl.full[st], 0, kc * BK, (m0 + t * BM) / 64, z);
           else tma_load_4d(sa + t * A_TILE, map_w, &ctl.full[st], 0, m0 + t * BM, kc, z);
         }
-        tma_load_4d(sa + MT * A_TILE, &map_x, &ctl.full[st], 0, n0, kc, z);
+      };
+      auto load_x = [&](int i) {
+        const int st = i % p.nstage;
+        tma_load_4d(smem + st * p.stage_bytes + MT * A_TILE, &map_x, &ctl.full[st], 0, n0, (ks0 + i) * CPB, z);
+      };
+      // The weights of the first stages are read-only inputs: they stream in
+      // while the previous kernel finishes; the activations wait for it.
+      const int pre = nk < p.nstage ? nk : p.nstage;
+      for (int i = 0; i < pre; ++i) {
+        mbar_arrive_expect_tx(&ctl.full[i], bytes);
+        load_w(i);
+      }
+      pdl_wait();
+      for (int i = 0; i < pre; ++i) load_x(i);
+      for (int i = pre; i < nk; ++i) {
+        const int st = i % p.nstage;
+        if (!wait_bar(&ctl.empty[st], ((i / p.nstage) - 1) & 1, ctl, p.status)) break;
+        mbar_arrive_expect_tx(&ctl.full[st], bytes);
+        load_w(i);
+        load_x(i);
       }
     }
   } else if (warp == 1) {
@@ -175,6 +193,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
     const int quarter = warp & 3;
     const int m = quarter * 32 + lane;           // this thread's TMEM lane = tile row
     float* cs = reinterpret_cast<float*>(smem);  // [MT][n_tile][BM] partials, reuses the stages
+    pdl_wait();   // before the epilogue reads indices or writes the output
     const bool ok = nk > 0 && wait_bar(&ctl.acc_full, 0, ctl, p.status);
     if (ok) tc_fence_after();
     for (int t = 0; t < MT; ++t) {
@@ -226,47 +245,79 @@ __global__ void __launch_bounds__(NTHREADS, 1)
     const int et = threadIdx.x - 64;
     const float* cs = reinterpret_cast<const float*>(smem);
     __nv_bfloat16* out = static_cast<__nv_bfloat16*>(p.out);
+    // Each thread stores 8 consecutive output columns (one 16-byte vector)
+    // of one activation row per pass: 16 threads span a 128-row tile, the 128
+    // epilogue threads 8 rows n. Rows owned by this CTA: n = split + S j.
+    const int cg = et & 15, jr = et >> 4;
+    const int n_own = (n_valid - split + S - 1) / S;
     for (int t = 0; t < MT; ++t) {
-      // reduced rows: own rows n = split + S*j sit at (n_tile + j) rows when S > 1
-      const int mm = m0 + t * BM + et;  // row within the segment
-      if (mm >= p.rows[seg]) continue;
-      for (int n = split; n < n_valid; n += S) {
-        const float* row = S > 1 ? cs + (p.n_tile + n / S) * BM : cs + (t * p.n_tile + n) * BM;
+      const int mb = m0 + t * BM + cg * 8;  // first of this thread's 8 rows within the segment
+      if (mb >= p.rows[seg]) continue;
+      const int mcount = min(8, p.rows[seg] - mb);
+      for (int j = jr; j < n_own; j += 8) {
+        const int n = split + S * j;
+        const float* row = S > 1 ? cs + (p.n_tile + j) * BM : cs + (t * p.n_tile + n) * BM;
         const long long gn = (long long)n0 + n;
-        const float v = row[et];
+        float v[8];
+        {
+          const float4 a0 = *reinterpret_cast<const float4*>(row + cg * 8);
+          const float4 a1 = *reinterpret_cast<const float4*>(row + cg * 8 + 4);
+          v[0] = a0.x; v[1] = a0.y; v[2] = a0.z; v[3] = a0.w; v[4] = a1.x; v[5] = a1.y; v[6] = a1.z; v[7] = a1.w;
+        }
+        __nv_bfloat16* dst;
         if (p.epi == EPI_STORE) {
-          out[z * p.bo + gn * p.ldo + p.col0[seg] + mm] = __float2bfloat16_rn(v);
+          dst = out + z * p.bo + gn * p.ldo + p.col0[seg] + mb;
         } else if (p.epi == EPI_ROPE_SEGS) {
+          // 8 rows of one rotated segment, all in one half of it (d_r % 16 == 0)
           const int half = p.d_r / 2;
-          const int sg = mm / p.d_r, j = mm % p.d_r;
+          const int sg = mb / p.d_r, j0 = mb % p.d_r;
           int ps = p.pos[gn];
           if (ps < 0 || ps >= p.max_pos) {
-            if (j == 0 && sg == 0) atomicOr(p.status, MLA_DEV_QPOS_RANGE);
+            if (j0 == 0 && sg == 0) atomicOr(p.status, MLA_DEV_QPOS_RANGE);
             ps = ps < 0 ? 0 : p.max_pos - 1;
           }
-          const int jj = j < half ? j : j - half;
-          const float c = p.rope_cos[(long long)ps * half + jj], sn = p.rope_sin[(long long)ps * half + jj];
-          const float partner = j < half ? row[et + half] : row[et - half];
-          out[gn * p.ldo + sg * p.seg_stride + p.seg_off + j] = __float2bfloat16_rn(rope_apply(v, partner, j < half, c, sn));
+          const bool first = j0 < half;
+          const int jj = first ? j0 : j0 - half;
+          const float* pr = row + cg * 8 + (first ? half : -half);
+#pragma unroll
+          for (int e = 0; e < 8; ++e) {
+            const float c = p.rope_cos[(long long)ps * half + jj + e], sn = p.rope_sin[(long long)ps * half + jj + e];
+            v[e] = rope_apply(v[e], pr[e], first, c, sn);
+          }
+          dst = out + gn * p.ldo + sg * p.seg_stride + p.seg_off + j0;
         } else {  // EPI_APPEND
           const int sq = p.tok_seq[gn], ps = p.tok_pos[gn];
           const bool seq_ok = sq >= 0 && sq < p.cache_batch;
           const bool pos_ok = ps >= 0 && ps < p.max_len && ps < p.max_pos;
-          const int gm = p.col0[seg] + mm;
+          const int gm = p.col0[seg] + mb;
           if (!seq_ok || !pos_ok) {
             if (gm == 0) atomicOr(p.status, (seq_ok ? 0 : MLA_DEV_SEQ_RANGE) | (pos_ok ? 0 : MLA_DEV_POS_RANGE));
             continue;
           }
-          float r = v;
           if (gm >= p.d_c) {
             const int half = p.d_r / 2;
-            const int j = gm - p.d_c;
-            const int jj = j < half ? j : j - half;
-            const float c = p.rope_cos[(long long)ps * half + jj], sn = p.rope_sin[(long long)ps * half + jj];
-            const float partner = j < half ? row[et + half] : row[et - half];
-            r = rope_apply(v, partner, j < half, c, sn);
+            const int j0 = gm - p.d_c;
+            const bool first = j0 < half;
+            const int jj = first ? j0 : j0 - half;
+            const float* pr = row + cg * 8 + (first ? half : -half);
+#pragma unroll
+            for (int e = 0; e < 8; ++e) {
+              const float c = p.rope_cos[(long long)ps * half + jj + e], sn = p.rope_sin[(long long)ps * half + jj + e];
+              v[e] = rope_apply(v[e], pr[e], first, c, sn);
+            }
           }
-          out[((long long)sq * p.max_len + ps) * p.row_width + gm] = __float2bfloat16_rn(r);
+          dst = out + ((long long)sq * p.max_len + ps) * p.row_width + gm;
+        }
+        if (mcount == 8) {
+          uint32_t pk[4];
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            __nv_bfloat162 b2 = __floats2bfloat162_rn(v[2 * e], v[2 * e + 1]);
+            pk[e] = *reinterpret_cast<uint32_t*>(&b2);
+          }
+          *reinterpret_cast<uint4*>(dst) = make_uint4(pk[0], pk[1], pk[2], pk[3]);
+        } else {
+          for (int e = 0; e < mcount; ++e) dst[e] = __float2bfloat16_rn(v[e]);
         }
       }
     }
@@ -294,19 +345,8 @@ cudaError_t launch_typed(const CUtensorMap* mw, const CUtensorMap& mx, const Par
     if (e != cudaSuccess) return e;
     smem_set = smem_dyn;
   }
-  cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = grid;
-  cfg.blockDim = dim3(NTHREADS);
-  cfg.dynamicSmemBytes = smem_dyn;
-  cfg.stream = s;
-  cudaLaunchAttribute attr[1];
-  attr[0].id = cudaLaunchAttributeClusterDimension;
-  attr[0].val.clusterDim.x = (unsigned)p.splits;
-  attr[0].val.clusterDim.y = 1;
-  attr[0].val.clusterDim.z = 1;
-  cfg.attrs = attr;
-  cfg.numAttrs = 1;
-  cudaError_t e = cudaLaunchKernelEx(&cfg, gemm_tc_kernel<CPB, TRANS>, mw[0], mw[1], mx, p);
+  LaunchCfg lc(grid, dim3(NTHREADS), smem_dyn, s, (unsigned)p.splits);
+  cudaError_t e = cudaLaunchKernelEx(&lc.cfg, gemm_tc_kernel<CPB, TRANS>, mw[0], mw[1], mx, p);
   if (e != cudaSuccess) return e;
   return cudaGetLastError();
 }
@@ -327,6 +367,13 @@ bool gemm_tc_shape_ok(const TcGemm& g) {
   // RoPE partners must share a tile: segments of d_r rows must tile 128 rows.
   if ((g.epi == EPI_ROPE_SEGS || g.epi == EPI_APPEND) && (g.d_r <= 0 || (BM % g.d_r) || (g.d_r & 1))) return false;
   if (g.epi == EPI_APPEND && (g.nseg != 2 || g.rows[1] != g.d_r || g.col0[1] != g.d_c)) return false;
+  // The epilogue stores 8 consecutive bf16 outputs (16 bytes) at a time; RoPE
+  // keeps each group of 8 inside one half of a rotated segment.
+  if (reinterpret_cast<uintptr_t>(g.out) & 15) return false;
+  if ((g.ldo % 8) || (g.bo % 8) || (g.col0[0] % 8) || (g.nseg == 2 && (g.col0[1] % 8))) return false;
+  if ((g.epi == EPI_ROPE_SEGS || g.epi == EPI_APPEND) && (g.d_r % 16)) return false;
+  if (g.epi == EPI_ROPE_SEGS && ((g.seg_stride % 8) || (g.seg_off % 8))) return false;
+  if (g.epi == EPI_APPEND && ((g.row_width % 8) || (g.d_c % 8))) return false;
   return true;
 }
 

@@ -34,6 +34,46 @@ template <> __device__ __forceinline__ __nv_bfloat16 from_f32<__nv_bfloat16>(flo
 
 inline size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 
+// ------------------------------------------------------------ launch overlap
+// Programmatic dependent launch: a kernel launched with the programmatic
+// stream-serialization attribute may start while the previous kernel on the
+// stream is still running. pdl_trigger lets the next kernel start; pdl_wait
+// blocks until the previous kernel has completed and its writes are visible
+// (a no-op for a kernel launched without the attribute). Every kernel that
+// uses them waits before it reads what earlier kernels wrote and before it
+// writes global memory; only work on read-only inputs (weights) or on its own
+// shared memory and TMEM comes before the wait. Since each kernel completes
+// only after the one before it, the order is transitive along the stream.
+__device__ __forceinline__ void pdl_trigger() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+
+// A launch configuration with programmatic dependent launch, and a cluster
+// of `cluster_x` CTAs when cluster_x > 0.
+struct LaunchCfg {
+  cudaLaunchConfig_t cfg;
+  cudaLaunchAttribute attr[2];
+  LaunchCfg(dim3 grid, dim3 block, size_t smem, cudaStream_t s, unsigned cluster_x = 0) {
+    cfg = cudaLaunchConfig_t{};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = s;
+    int n = 0;
+    attr[n].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[n].val.programmaticStreamSerializationAllowed = 1;
+    ++n;
+    if (cluster_x > 0) {
+      attr[n].id = cudaLaunchAttributeClusterDimension;
+      attr[n].val.clusterDim.x = cluster_x;
+      attr[n].val.clusterDim.y = 1;
+      attr[n].val.clusterDim.z = 1;
+      ++n;
+    }
+    cfg.attrs = attr;
+    cfg.numAttrs = n;
+  }
+};
+
 // ------------------------------------------------------------- CUDA-core GEMM
 // out[n, map(m)] = epilogue( sum_k X[n, k] * W'[m, k] ) for n < N, m < M, batch z.
 // W'[m, k] = W[m*ldw + k] (W_NORMAL) or W[k*ldw + m] (W_TRANSPOSED).
