@@ -124,7 +124,9 @@ struct Ctl {
   // PV(u + NPB) needs its unit_ready, so each barrier is within one phase of
   // what its waiter expects (a single barrier could run two phases behind).
   uint64_t pv_done[NPB];
-  uint64_t o_free;
+  uint64_t o_free;            // O read out by the 8 epilogue warps
+  uint64_t epi_go;            // a piece's last PV is done and inv_l is in shared memory
+  float inv_l[NH];            // CTA 1: 1 / softmax denominator of the piece being written
   uint32_t tmem_base;
   int abort;
   float mx[2][2][NH];         // CTA 0: per-half tile maxima, double-buffered by tile
@@ -198,6 +200,63 @@ struct Pieces {
   }
 };
 
+// One half (256 columns) of the epilogue of a piece: this thread's head row of
+// O, scaled by 1/l, to o_lat (a whole sequence) or to the piece's fp32 partial
+// slot. TMEM is read 64 columns at a time; the warp releases O (o_free) as soon
+// as its last read is done, before its last stores.
+__device__ __forceinline__ void store_o_half(const DecodeArgs& a, uint32_t taddr, int c0, int seq, int chunk, int h,
+                                             bool whole, float inv_l, uint64_t* o_free, int lane) {
+  const bool v8_out = (reinterpret_cast<uintptr_t>(a.o_lat) & 31) == 0;
+  const bool v8_part = (reinterpret_cast<uintptr_t>(a.part_o) & 31) == 0;
+#pragma unroll 1
+  for (int r = 0; r < 4; ++r) {
+    float v[64];
+    tmem_ld32(taddr + r * 64, v);
+    tmem_ld32(taddr + r * 64 + 32, v + 32);
+    tmem_ld_wait();
+    if (r == 3) {
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(o_free);
+    }
+    const int c = c0 + r * 64;
+    if (whole) {
+      uint32_t pk[32];
+#pragma unroll
+      for (int i = 0; i < 32; ++i) {
+        __nv_bfloat162 pr = __floats2bfloat162_rn(v[2 * i] * inv_l, v[2 * i + 1] * inv_l);
+        pk[i] = *reinterpret_cast<uint32_t*>(&pr);
+      }
+      __nv_bfloat16* dst = static_cast<__nv_bfloat16*>(a.o_lat) + ((size_t)seq * NH + h) * DC + c;
+      if (v8_out) {
+#pragma unroll
+        for (int q = 0; q < 4; ++q)
+          st_global_v8(dst + q * 16, pk[8 * q], pk[8 * q + 1], pk[8 * q + 2], pk[8 * q + 3], pk[8 * q + 4],
+                       pk[8 * q + 5], pk[8 * q + 6], pk[8 * q + 7]);
+      } else {
+#pragma unroll
+        for (int q = 0; q < 8; ++q)
+          reinterpret_cast<uint4*>(dst)[q] = make_uint4(pk[4 * q], pk[4 * q + 1], pk[4 * q + 2], pk[4 * q + 3]);
+      }
+    } else {
+      float* dst = a.part_o + ((size_t)(seq + chunk) * NH + h) * DC + c;
+      if (v8_part) {
+#pragma unroll
+        for (int q = 0; q < 8; ++q)
+          st_global_v8(dst + q * 8, __float_as_uint(v[8 * q] * inv_l), __float_as_uint(v[8 * q + 1] * inv_l),
+                       __float_as_uint(v[8 * q + 2] * inv_l), __float_as_uint(v[8 * q + 3] * inv_l),
+                       __float_as_uint(v[8 * q + 4] * inv_l), __float_as_uint(v[8 * q + 5] * inv_l),
+                       __float_as_uint(v[8 * q + 6] * inv_l), __float_as_uint(v[8 * q + 7] * inv_l));
+      } else {
+#pragma unroll
+        for (int q = 0; q < 16; ++q)
+          reinterpret_cast<float4*>(dst)[q] = make_float4(v[4 * q] * inv_l, v[4 * q + 1] * inv_l,
+                                                          v[4 * q + 2] * inv_l, v[4 * q + 3] * inv_l);
+      }
+    }
+  }
+}
+
 __device__ __forceinline__ bool wait_or_abort(uint64_t* bar, uint32_t parity, Ctl& ctl, int32_t* status) {
   if (*reinterpret_cast<volatile int*>(&ctl.abort)) return false;
   if (mbar_wait(bar, parity, WAIT_CYCLES)) return true;
@@ -238,7 +297,8 @@ __global__ void __launch_bounds__(NTHREADS, 1)
     }
     for (int i = 0; i < S1_RING; ++i) { mbar_init(&ctl.r1_full[i], 1); mbar_init(&ctl.r1_empty[i], 1); }
     for (int i = 0; i < NPB; ++i) mbar_init(&ctl.pv_done[i], 1);
-    mbar_init(&ctl.o_free, 4);
+    mbar_init(&ctl.o_free, 8);
+    mbar_init(&ctl.epi_go, 4);
     ctl.abort = 0;
     if (cluster_rank() == 1)  // arm the first use of every P buffer
       for (int i = 0; i < NPB; ++i) mbar_arrive_expect_tx(&ctl.p_full[i], P_COPY_BYTES);
@@ -630,40 +690,37 @@ __global__ void __launch_bounds__(NTHREADS, 1)
           }
           first = false;
           if (flags & FLAG_LAST) {
-            // ------------------------------------------------ epilogue of the piece
+            // ------------------------------------------------ epilogue of the piece: columns 0..255 here,
+            // 256..511 in warps 6..9
             ok = wait_or_abort(&ctl.pv_done[pb], (u / NPB) & 1, ctl, a.status);
             ok = !cw_any(!ok);
             if (!ok) break;
-            tc_fence_after();
-#pragma unroll 1
-            for (int c = 0; c < DC; c += 16) {
-              float v[16];
-              tmem_ld16(tbase + lane_base + c, v);
-              tmem_ld_wait();
-              if (whole) {
-                uint32_t pk[8];
-#pragma unroll
-                for (int i2 = 0; i2 < 8; ++i2) {
-                  __nv_bfloat162 pr = __floats2bfloat162_rn(v[2 * i2] * inv_l, v[2 * i2 + 1] * inv_l);
-                  pk[i2] = *reinterpret_cast<uint32_t*>(&pr);
-                }
-                uint4* dst = reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(a.o_lat) +
-                                                      ((size_t)seq * NH + h) * DC + c);
-                dst[0] = make_uint4(pk[0], pk[1], pk[2], pk[3]);
-                dst[1] = make_uint4(pk[4], pk[5], pk[6], pk[7]);
-              } else {
-                float4* dst = reinterpret_cast<float4*>(a.part_o + ((size_t)(seq + chunk) * NH + h) * DC + c);
-#pragma unroll
-                for (int i2 = 0; i2 < 4; ++i2)
-                  dst[i2] = make_float4(v[4 * i2] * inv_l, v[4 * i2 + 1] * inv_l, v[4 * i2 + 2] * inv_l,
-                                        v[4 * i2 + 3] * inv_l);
-              }
-            }
-            tc_fence_before();
+            ctl.inv_l[h] = inv_l;
             __syncwarp();
-            if (lane == 0) mbar_arrive(&ctl.o_free);
+            if (lane == 0) mbar_arrive(&ctl.epi_go);
+            tc_fence_after();
+            store_o_half(a, tbase + lane_base, 0, seq, chunk, h, whole, inv_l, &ctl.o_free, lane);
           }
         }
+        ++piece;
+      }
+    } else {
+      // ---------------------------------------------------------- epilogue warps 6..9: columns 256..511
+      const int quarter = warp & 3;
+      const int h = quarter * 32 + lane;
+      const uint32_t lane_base = static_cast<uint32_t>(quarter * 32) << 16;
+      Pieces it;
+      it.init(a.plan, B, chunk);
+      int seq, t0, t1;
+      bool whole;
+      int piece = 0;
+      bool ok = true;
+      while (ok && it.next(seq, t0, t1, whole)) {
+        ok = __all_sync(0xffffffffu, wait_or_abort(&ctl.epi_go, piece & 1, ctl, a.status));
+        if (!ok) break;
+        const float inv_l = ctl.inv_l[h];
+        tc_fence_after();
+        store_o_half(a, tbase + lane_base + 256, 256, seq, chunk, h, whole, inv_l, &ctl.o_free, lane);
         ++piece;
       }
     }
