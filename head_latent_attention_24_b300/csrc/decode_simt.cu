@@ -301,19 +301,34 @@ __global__ void __launch_bounds__(256) decode_combine_kernel(const DecodeArgs a)
   const float inv = 1.f / sum;
   const float* po = a.part_o + ((long long)(b + c0) * a.n_h + h) * d_c;
   const long long pstride = (long long)a.n_h * d_c;
-  for (int e0 = lane * 4; e0 < d_c; e0 += 128) {
-    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-    for (int j = 0; j < np; ++j) {
-      const float w = expf(plse[(long long)j * a.n_h] - mx) * inv;
-      const float4 v = *reinterpret_cast<const float4*>(po + j * pstride + e0);
-      acc.x = fmaf(w, v.x, acc.x); acc.y = fmaf(w, v.y, acc.y);
-      acc.z = fmaf(w, v.z, acc.z); acc.w = fmaf(w, v.w, acc.w);
-    }
-    o_out[e0] = from_f32<T>(acc.x);
-    o_out[e0 + 1] = from_f32<T>(acc.y);
-    o_out[e0 + 2] = from_f32<T>(acc.z);
-    o_out[e0 + 3] = from_f32<T>(acc.w);
+  // d_c <= 512: each lane owns up to 4 groups of 4 columns (e = lane*4 + 128 q).
+  // All of a piece's loads are issued before any of them is used.
+  const int nq = (d_c - lane * 4 + 127) / 128;
+  float4 acc[4];
+#pragma unroll
+  for (int q = 0; q < 4; ++q) acc[q] = make_float4(0.f, 0.f, 0.f, 0.f);
+  for (int j = 0; j < np; ++j) {
+    const float w = expf(plse[(long long)j * a.n_h] - mx) * inv;
+    float4 v[4];
+#pragma unroll
+    for (int q = 0; q < 4; ++q)
+      if (q < nq) v[q] = __ldg(reinterpret_cast<const float4*>(po + j * pstride + lane * 4 + q * 128));
+#pragma unroll
+    for (int q = 0; q < 4; ++q)
+      if (q < nq) {
+        acc[q].x = fmaf(w, v[q].x, acc[q].x); acc[q].y = fmaf(w, v[q].y, acc[q].y);
+        acc[q].z = fmaf(w, v[q].z, acc[q].z); acc[q].w = fmaf(w, v[q].w, acc[q].w);
+      }
   }
+#pragma unroll
+  for (int q = 0; q < 4; ++q)
+    if (q < nq) {
+      T* o = o_out + lane * 4 + q * 128;
+      o[0] = from_f32<T>(acc[q].x);
+      o[1] = from_f32<T>(acc[q].y);
+      o[2] = from_f32<T>(acc[q].z);
+      o[3] = from_f32<T>(acc[q].w);
+    }
   if (lane == 0) a.lse[(long long)b * a.n_h + h] = mx + logf(sum);
 }
 
