@@ -275,7 +275,7 @@ __device__ __forceinline__ bool wait_cluster_or_abort(uint64_t* bar, uint32_t pa
 
 __global__ void __launch_bounds__(NTHREADS, 1)
     decode_pair_kernel(const __grid_constant__ CUtensorMap map_kv0, const __grid_constant__ CUtensorMap map_kv1,
-                       const DecodeArgs a) {
+                       const __grid_constant__ CUtensorMap map_q, const DecodeArgs a) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   __shared__ Ctl ctl;
@@ -324,6 +324,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
       // ---------------------------------------------------------- TMA producer
       if (lane == 0) {
         prefetch_tensormap(&map_kv0);
+        prefetch_tensormap(&map_q);
         Pieces it;
         it.init(a.plan, B, chunk);
         int seq, t0, t1;
@@ -331,6 +332,14 @@ __global__ void __launch_bounds__(NTHREADS, 1)
         int i = 0;
         bool ok = true;
         while (ok && it.next(seq, t0, t1, whole)) {
+          // the piece's absorbed queries (128 heads x 576) through the ring, three boxes
+          for (int c = 0; c < NCH && ok; c += S0_CPB, ++i) {
+            const int sl = i % S0_RING;
+            if (i >= S0_RING) ok = wait_or_abort(&ctl.r0_empty[sl], ((i / S0_RING) - 1) & 1, ctl, a.status);
+            if (!ok) break;
+            mbar_arrive_expect_tx(&ctl.r0_full[sl], S0_SLOT);
+            tma_load_3d(smem + S0_RING_OFF + sl * S0_SLOT, &map_q, &ctl.r0_full[sl], 0, seq * NH, c);
+          }
           for (int r = t0; r < t1 && ok; r += TR) {
             const int row = seq * a.max_len + r;
             for (int c = 0; c < NCH; c += S0_CPB, ++i) {
@@ -360,6 +369,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
         const uint64_t ring_desc = sdesc_sw128(sbase + S0_RING_OFF, 16, 1024);
         const uint64_t qr_desc = sdesc_sw128(qr, 16, 1024);
         while (ok && it.next(seq, t0, t1, whole)) {
+          i += NCH / S0_CPB;   // the query boxes: the softmax warps take them
           ok = wait_or_abort(&ctl.q_ready, piece & 1, ctl, a.status);
           if (!ok) break;
           tc_fence_after();
@@ -408,10 +418,16 @@ __global__ void __launch_bounds__(NTHREADS, 1)
       it.init(a.plan, B, chunk);
       int seq, t0, t1;
       bool whole;
-      int piece = 0, g = 0, u = 0;
+      int piece = 0, g = 0, u = 0, iring = 0;
       bool ok = true;
       while (ok && it.next(seq, t0, t1, whole)) {
-        // q~ of this piece's sequence into TMEM (this warp's lanes, its 128 of 256 columns)
+        // q~ of this piece's sequence into TMEM (this warp's lanes, its 128 of
+        // 256 columns) and q_R into shared memory, from the three ring slots
+        // the producer filled with the piece's queries.
+        const int len = t1 - t0;
+        const int ntiles = (len + TR - 1) / TR;
+        const int iq = iring;
+        iring += (NCH / S0_CPB) * (1 + ntiles);
         if (piece >= 1) {
           ok = wait_or_abort(&ctl.q_free, (piece - 1) & 1, ctl, a.status);
           ok = !sm_any(!ok);
@@ -419,34 +435,45 @@ __global__ void __launch_bounds__(NTHREADS, 1)
           tc_fence_after();
         }
         {
-          const uint4* qrow = reinterpret_cast<const uint4*>(static_cast<const __nv_bfloat16*>(a.q_abs) +
-                                                             ((size_t)seq * NH + h) * DD);
-          // q_R row h into shared memory (K-major, 128-byte swizzle): this half
-          // writes 16-byte units 4*hf .. 4*hf+3 of the row's 8
-          uint8_t* qr_row = smem + S0_QR_OFF + (h >> 3) * 1024 + (h & 7) * 128;
+          bool w = true;
+          for (int j = 0; j < NCH / S0_CPB; ++j)
+            w = w && wait_or_abort(&ctl.r0_full[(iq + j) % S0_RING], ((iq + j) / S0_RING) & 1, ctl, a.status);
+          ok = !sm_any(!w);
+          if (!ok) break;
+          const int roff = (h >> 3) * 1024 + (h & 7) * 128;   // row h of a 128-row chunk (128-byte swizzle)
 #pragma unroll
-          for (int v = 4 * hf; v < 4 * hf + 4; ++v)
-            *reinterpret_cast<uint4*>(qr_row + ((v ^ (h & 7)) << 4)) = __ldg(qrow + DC / 8 + v);
-          fence_proxy_async_smem();
-          const uint4* src = qrow + hf * 32;
-#pragma unroll 1
-          for (int j = 0; j < 4; ++j) {
+          for (int jj = 0; jj < 4; ++jj) {
+            const int c = hf * 4 + jj;
+            const uint8_t* rowp = smem + S0_RING_OFF + ((iq + c / S0_CPB) % S0_RING) * S0_SLOT + (c % S0_CPB) * S0_CHUNK + roff;
             uint32_t r[32];
 #pragma unroll
             for (int v = 0; v < 8; ++v) {
-              const uint4 x = __ldg(src + j * 8 + v);
+              const uint4 x = *reinterpret_cast<const uint4*>(rowp + ((v ^ (h & 7)) << 4));
               r[4 * v] = x.x; r[4 * v + 1] = x.y; r[4 * v + 2] = x.z; r[4 * v + 3] = x.w;
             }
-            tmem_st32(tbase + lane_base + QL_COL + hf * 128 + j * 32, r);
+            tmem_st32(tbase + lane_base + QL_COL + hf * 128 + jj * 32, r);
           }
+          // q_R: the last chunk, same layout; this half copies 16-byte units 4*hf .. 4*hf+3 of row h
+          {
+            const uint8_t* src = smem + S0_RING_OFF + ((iq + (NCH - 1) / S0_CPB) % S0_RING) * S0_SLOT +
+                                 ((NCH - 1) % S0_CPB) * S0_CHUNK + roff;
+            uint8_t* dst = smem + S0_QR_OFF + roff;
+#pragma unroll
+            for (int v = 4 * hf; v < 4 * hf + 4; ++v) {
+              const int o = (v ^ (h & 7)) << 4;
+              *reinterpret_cast<uint4*>(dst + o) = *reinterpret_cast<const uint4*>(src + o);
+            }
+          }
+          fence_proxy_async_smem();
           tmem_st_wait();
           tc_fence_before();
+          sm_sync();   // every softmax thread is done with the query slots
+          if (threadIdx.x == 64)
+            for (int j = 0; j < NCH / S0_CPB; ++j) mbar_arrive(&ctl.r0_empty[(iq + j) % S0_RING]);
           __syncwarp();
           if (lane == 0) mbar_arrive(&ctl.q_ready);
         }
         float m_ref = -INFINITY, l_part = 0.f;
-        const int len = t1 - t0;
-        const int ntiles = (len + TR - 1) / TR;
         for (int k = 0; k < ntiles; ++k, ++g) {
           const int nvalid = min(TR, len - k * TR);
           const bool has_unit = hf == 0 || nvalid > UR;
@@ -750,12 +777,15 @@ int decode_tc_chunks(const mla_handle_s* h, int) {
 cudaError_t launch_decode_tc(const mla_handle_s* h, const DecodeArgs& a, cudaStream_t s, int* launches) {
   // Cache viewed as {64 columns, rows, 9 column chunks}: row stride 1152 B,
   // chunk stride 128 B (the chunk is the outer box dimension).
-  CUtensorMap map_kv0, map_kv1;
+  CUtensorMap map_kv0, map_kv1, map_q;
   const uint64_t dims[3] = {64, (uint64_t)a.B * a.max_len, NCH};
   const uint64_t strides[2] = {DD * 2, 128};
   const uint32_t box0[3] = {64, TR, S0_CPB}, box1[3] = {64, UR, S1_CPB};
   if (!make_tmap_3d_bf16_sw128(&map_kv0, a.cache, dims, strides, box0)) return cudaErrorInvalidValue;
   if (!make_tmap_3d_bf16_sw128(&map_kv1, a.cache, dims, strides, box1)) return cudaErrorInvalidValue;
+  // The absorbed queries [B * 128 heads][576] through the same chunk-outer view.
+  const uint64_t qdims[3] = {64, (uint64_t)a.B * NH, NCH};
+  if (!make_tmap_3d_bf16_sw128(&map_q, a.q_abs, qdims, strides, box0)) return cudaErrorInvalidValue;
   cudaError_t e = launch_decode_plan(a.seqlens, a.B, a.max_len, a.grid_chunks, UR, a.plan, a.status, s);
   if (e != cudaSuccess) return e;
   static bool attr_set = false;
@@ -765,7 +795,7 @@ cudaError_t launch_decode_tc(const mla_handle_s* h, const DecodeArgs& a, cudaStr
     attr_set = true;
   }
   LaunchCfg lc(dim3((unsigned)(2 * a.grid_chunks)), dim3(NTHREADS), SMEM_DYN, s, 2);
-  e = cudaLaunchKernelEx(&lc.cfg, decode_pair_kernel, map_kv0, map_kv1, a);
+  e = cudaLaunchKernelEx(&lc.cfg, decode_pair_kernel, map_kv0, map_kv1, map_q, a);
   if (e != cudaSuccess) return e;
   e = cudaGetLastError();
   if (e != cudaSuccess) return e;
