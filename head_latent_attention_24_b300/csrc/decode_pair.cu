@@ -85,12 +85,14 @@ constexpr int S0_STG_OFF = S0_RING_OFF + S0_RING * S0_SLOT;   // P staging buffe
 constexpr int S0_END = S0_STG_OFF + NPB * P_STRIDE;
 // CTA 1 shared-memory layout
 constexpr int S1_CPB = 4;                         // latent chunks per value box
-constexpr int S1_RING = 5;
+constexpr int S1_RING = 4;
 constexpr int S1_CHUNK = UR * 128;                // 8 KB: 64 rows x 64 latent columns
 constexpr int S1_SLOT = S1_CPB * S1_CHUNK;        // 32 KB: 64 rows x 256 latent columns
 constexpr int S1_P_OFF = 0;
 constexpr int S1_RING_OFF = NPB * P_STRIDE;
-constexpr int S1_END = S1_RING_OFF + S1_RING * S1_SLOT;
+constexpr int S1_STG_OFF = S1_RING_OFF + S1_RING * S1_SLOT;   // epilogue staging, 16 KB per column half
+constexpr int S1_STG = 16 * 1024;
+constexpr int S1_END = S1_STG_OFF + 2 * S1_STG;
 constexpr int SMEM_DYN = (S0_END > S1_END ? S0_END : S1_END) + 1024;
 
 // TMEM columns
@@ -200,14 +202,20 @@ struct Pieces {
   }
 };
 
+__device__ __forceinline__ void half_bar(int id) { asm volatile("bar.sync %0, 128;" ::"r"(id) : "memory"); }
+
 // One half (256 columns) of the epilogue of a piece: this thread's head row of
-// O, scaled by 1/l, to o_lat (a whole sequence) or to the piece's fp32 partial
-// slot. TMEM is read 64 columns at a time; the warp releases O (o_free) as soon
-// as its last read is done, before its last stores.
-__device__ __forceinline__ void store_o_half(const DecodeArgs& a, uint32_t taddr, int c0, int seq, int chunk, int h,
-                                             bool whole, float inv_l, uint64_t* o_free, int lane) {
-  const bool v8_out = (reinterpret_cast<uintptr_t>(a.o_lat) & 31) == 0;
-  const bool v8_part = (reinterpret_cast<uintptr_t>(a.part_o) & 31) == 0;
+// O, scaled by 1/l, to o_lat (a whole sequence, bf16) or to the piece's fp32
+// partial slot. TMEM is read 64 columns at a time; each 128-byte-wide column
+// block of the half's 128 rows is written to a swizzled shared staging buffer
+// and sent out as one TMA tensor store, so the stores do not queue in the
+// threads' load/store path behind the cache stream. The warps release O
+// (o_free) after their last TMEM read, before the last stores.
+__device__ __forceinline__ void store_o_half(const CUtensorMap* map_ol, const CUtensorMap* map_po, uint32_t taddr,
+                                             int half, int row0, int h, bool whole, float inv_l, uint64_t* o_free,
+                                             int lane, uint8_t* stg, int bar_id, bool issuer) {
+  uint8_t* srow = stg + (h >> 3) * 1024 + (h & 7) * 128;
+  const int sw = h & 7;
 #pragma unroll 1
   for (int r = 0; r < 4; ++r) {
     float v[64];
@@ -219,42 +227,39 @@ __device__ __forceinline__ void store_o_half(const DecodeArgs& a, uint32_t taddr
       __syncwarp();
       if (lane == 0) mbar_arrive(o_free);
     }
-    const int c = c0 + r * 64;
-    if (whole) {
-      uint32_t pk[32];
 #pragma unroll
-      for (int i = 0; i < 32; ++i) {
-        __nv_bfloat162 pr = __floats2bfloat162_rn(v[2 * i] * inv_l, v[2 * i + 1] * inv_l);
-        pk[i] = *reinterpret_cast<uint32_t*>(&pr);
-      }
-      __nv_bfloat16* dst = static_cast<__nv_bfloat16*>(a.o_lat) + ((size_t)seq * NH + h) * DC + c;
-      if (v8_out) {
+    for (int bx = 0; bx < 2; ++bx) {
+      if (whole && bx == 1) break;
+      if (issuer) bulk_wait_read<0>();   // the buffer's previous box has been read out
+      half_bar(bar_id);
+      if (whole) {
 #pragma unroll
-        for (int q = 0; q < 4; ++q)
-          st_global_v8(dst + q * 16, pk[8 * q], pk[8 * q + 1], pk[8 * q + 2], pk[8 * q + 3], pk[8 * q + 4],
-                       pk[8 * q + 5], pk[8 * q + 6], pk[8 * q + 7]);
+        for (int u = 0; u < 8; ++u) {
+          uint32_t pk[4];
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            __nv_bfloat162 pr = __floats2bfloat162_rn(v[8 * u + 2 * e] * inv_l, v[8 * u + 2 * e + 1] * inv_l);
+            pk[e] = *reinterpret_cast<uint32_t*>(&pr);
+          }
+          *reinterpret_cast<uint4*>(srow + ((u ^ sw) << 4)) = make_uint4(pk[0], pk[1], pk[2], pk[3]);
+        }
       } else {
 #pragma unroll
-        for (int q = 0; q < 8; ++q)
-          reinterpret_cast<uint4*>(dst)[q] = make_uint4(pk[4 * q], pk[4 * q + 1], pk[4 * q + 2], pk[4 * q + 3]);
+        for (int u = 0; u < 8; ++u) {
+          const float* x = v + 32 * bx + 4 * u;
+          *reinterpret_cast<float4*>(srow + ((u ^ sw) << 4)) =
+              make_float4(x[0] * inv_l, x[1] * inv_l, x[2] * inv_l, x[3] * inv_l);
+        }
       }
-    } else {
-      float* dst = a.part_o + ((size_t)(seq + chunk) * NH + h) * DC + c;
-      if (v8_part) {
-#pragma unroll
-        for (int q = 0; q < 8; ++q)
-          st_global_v8(dst + q * 8, __float_as_uint(v[8 * q] * inv_l), __float_as_uint(v[8 * q + 1] * inv_l),
-                       __float_as_uint(v[8 * q + 2] * inv_l), __float_as_uint(v[8 * q + 3] * inv_l),
-                       __float_as_uint(v[8 * q + 4] * inv_l), __float_as_uint(v[8 * q + 5] * inv_l),
-                       __float_as_uint(v[8 * q + 6] * inv_l), __float_as_uint(v[8 * q + 7] * inv_l));
-      } else {
-#pragma unroll
-        for (int q = 0; q < 16; ++q)
-          reinterpret_cast<float4*>(dst)[q] = make_float4(v[4 * q] * inv_l, v[4 * q + 1] * inv_l,
-                                                          v[4 * q + 2] * inv_l, v[4 * q + 3] * inv_l);
+      fence_proxy_async_smem();
+      half_bar(bar_id);
+      if (issuer) {
+        tma_store_2d(whole ? map_ol : map_po, stg, half * 256 + r * 64 + bx * 32, row0);
+        bulk_commit();
       }
     }
   }
+  if (issuer) bulk_wait_all();   // complete before the buffer is reused or the CTA exits
 }
 
 __device__ __forceinline__ bool wait_or_abort(uint64_t* bar, uint32_t parity, Ctl& ctl, int32_t* status) {
@@ -275,7 +280,8 @@ __device__ __forceinline__ bool wait_cluster_or_abort(uint64_t* bar, uint32_t pa
 
 __global__ void __launch_bounds__(NTHREADS, 1)
     decode_pair_kernel(const __grid_constant__ CUtensorMap map_kv0, const __grid_constant__ CUtensorMap map_kv1,
-                       const __grid_constant__ CUtensorMap map_q, const DecodeArgs a) {
+                       const __grid_constant__ CUtensorMap map_q, const __grid_constant__ CUtensorMap map_ol,
+                       const __grid_constant__ CUtensorMap map_po, const DecodeArgs a) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   __shared__ Ctl ctl;
@@ -726,7 +732,8 @@ __global__ void __launch_bounds__(NTHREADS, 1)
             __syncwarp();
             if (lane == 0) mbar_arrive(&ctl.epi_go);
             tc_fence_after();
-            store_o_half(a, tbase + lane_base, 0, seq, chunk, h, whole, inv_l, &ctl.o_free, lane);
+            store_o_half(&map_ol, &map_po, tbase + lane_base, 0, whole ? seq * NH : (seq + chunk) * NH, h, whole,
+                         inv_l, &ctl.o_free, lane, smem + S1_STG_OFF, 2, threadIdx.x == 64);
           }
         }
         ++piece;
@@ -747,7 +754,8 @@ __global__ void __launch_bounds__(NTHREADS, 1)
         if (!ok) break;
         const float inv_l = ctl.inv_l[h];
         tc_fence_after();
-        store_o_half(a, tbase + lane_base + 256, 256, seq, chunk, h, whole, inv_l, &ctl.o_free, lane);
+        store_o_half(&map_ol, &map_po, tbase + lane_base + 256, 1, whole ? seq * NH : (seq + chunk) * NH, h, whole,
+                     inv_l, &ctl.o_free, lane, smem + S1_STG_OFF + S1_STG, 3, threadIdx.x == 192);
         ++piece;
       }
     }
@@ -777,7 +785,7 @@ int decode_tc_chunks(const mla_handle_s* h, int) {
 cudaError_t launch_decode_tc(const mla_handle_s* h, const DecodeArgs& a, cudaStream_t s, int* launches) {
   // Cache viewed as {64 columns, rows, 9 column chunks}: row stride 1152 B,
   // chunk stride 128 B (the chunk is the outer box dimension).
-  CUtensorMap map_kv0, map_kv1, map_q;
+  CUtensorMap map_kv0, map_kv1, map_q, map_ol, map_po;
   const uint64_t dims[3] = {64, (uint64_t)a.B * a.max_len, NCH};
   const uint64_t strides[2] = {DD * 2, 128};
   const uint32_t box0[3] = {64, TR, S0_CPB}, box1[3] = {64, UR, S1_CPB};
@@ -786,6 +794,11 @@ cudaError_t launch_decode_tc(const mla_handle_s* h, const DecodeArgs& a, cudaStr
   // The absorbed queries [B * 128 heads][576] through the same chunk-outer view.
   const uint64_t qdims[3] = {64, (uint64_t)a.B * NH, NCH};
   if (!make_tmap_3d_bf16_sw128(&map_q, a.q_abs, qdims, strides, box0)) return cudaErrorInvalidValue;
+  // Epilogue stores: o_lat [B * 128][512] bf16 in 64-column boxes, partials
+  // [(B + chunks) * 128][512] fp32 in 32-column boxes, 128 rows each.
+  if (!make_tmap_2d_bf16_sw128(&map_ol, a.o_lat, DC, (uint64_t)a.B * NH, DC * 2, 64, NH)) return cudaErrorInvalidValue;
+  if (!make_tmap_2d_f32_sw128(&map_po, a.part_o, DC, (uint64_t)(a.B + a.grid_chunks) * NH, DC * 4, 32, NH))
+    return cudaErrorInvalidValue;
   cudaError_t e = launch_decode_plan(a.seqlens, a.B, a.max_len, a.grid_chunks, UR, a.plan, a.status, s);
   if (e != cudaSuccess) return e;
   static bool attr_set = false;
@@ -795,7 +808,7 @@ cudaError_t launch_decode_tc(const mla_handle_s* h, const DecodeArgs& a, cudaStr
     attr_set = true;
   }
   LaunchCfg lc(dim3((unsigned)(2 * a.grid_chunks)), dim3(NTHREADS), SMEM_DYN, s, 2);
-  e = cudaLaunchKernelEx(&lc.cfg, decode_pair_kernel, map_kv0, map_kv1, map_q, a);
+  e = cudaLaunchKernelEx(&lc.cfg, decode_pair_kernel, map_kv0, map_kv1, map_q, map_ol, map_po, a);
   if (e != cudaSuccess) return e;
   e = cudaGetLastError();
   if (e != cudaSuccess) return e;

@@ -150,6 +150,20 @@ __device__ __forceinline__ float ld_shared_cluster_f32(uint32_t addr) {
 // CTA's shared memory to shared::cluster address `dst` in another CTA of the
 // cluster; completion is signalled on that CTA's mbarrier `remote_bar` as
 // transaction bytes.
+// Shared -> global tensor store (2-D box), in the calling thread's bulk group.
+__device__ __forceinline__ void tma_store_2d(const CUtensorMap* map, const void* src, int x, int y) {
+  asm volatile("cp.async.bulk.tensor.2d.global.shared::cta.bulk_group [%0, {%2, %3}], [%1];" ::"l"(
+                   reinterpret_cast<uint64_t>(map)),
+               "r"(smem_u32(src)), "r"(x), "r"(y)
+               : "memory");
+}
+__device__ __forceinline__ void bulk_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
+// Wait until the calling thread's bulk groups have finished reading their
+// shared-memory sources (all but the newest N), or have completed (all).
+template <int N> __device__ __forceinline__ void bulk_wait_read() {
+  asm volatile("cp.async.bulk.wait_group.read %0;" ::"n"(N) : "memory");
+}
+__device__ __forceinline__ void bulk_wait_all() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
 __device__ __forceinline__ void bulk_copy_to_cluster(uint32_t dst, const void* src, uint32_t bytes,
                                                      uint32_t remote_bar) {
   asm volatile(

@@ -10,6 +10,9 @@ namespace mla {
 // Returns false if the driver rejects the map.
 bool make_tmap_2d_bf16_sw128(CUtensorMap* map, const void* base, uint64_t inner, uint64_t outer,
                              uint64_t row_bytes, uint32_t box_inner, uint32_t box_outer);
+// The same for fp32 elements (box_inner * 4 <= 128).
+bool make_tmap_2d_f32_sw128(CUtensorMap* map, const void* base, uint64_t inner, uint64_t outer,
+                            uint64_t row_bytes, uint32_t box_inner, uint32_t box_outer);
 // 3-D bf16 tensor with extents dims[0] (contiguous), dims[1], dims[2] and byte
 // strides strides[0] (between dim-1 steps) and strides[1] (between dim-2
 // steps); box box[0] x box[1] x box[2], 128-byte swizzle (box[0] * 2 <= 128).
