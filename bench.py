@@ -281,6 +281,8 @@ def run_ours(args, rank, world, local_rank):
     total_ms = start.elapsed_time(end)
     attn_ms = [e[1].elapsed_time(e[2]) for e in evs]
     step_ms = [e[0].elapsed_time(e[3]) for e in evs]
+    s12_ms = [e[0].elapsed_time(e[1]) for e in evs]
+    s45_ms = [e[2].elapsed_time(e[3]) for e in evs]
     total_ms = max_over_ranks(total_ms, device)
 
     # ---- end to end through the public API: pinned host in, host out, every step
@@ -373,6 +375,9 @@ def run_ours(args, rank, world, local_rank):
         "clocks": clocks,
         "kernel_source_hash": kh,
         "step_ms_median": round(statistics.median(step_ms), 4),
+        "step_breakdown_us": {"append_and_absorb": round(1e3 * statistics.median(s12_ms), 1),
+                              "attention": round(1e3 * statistics.median(attn_ms), 1),
+                              "out_proj": round(1e3 * statistics.median(s45_ms), 1)},
     }
     if world == 1 and not args.no_cpu_baseline:
         import mla_synth as S

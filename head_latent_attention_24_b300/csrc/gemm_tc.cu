@@ -50,15 +50,17 @@ constexpr int SMEM_BUDGET = 200 * 1024;
 constexpr long long WAIT_CYCLES = 4000000000LL;  // ~2 s
 
 struct Params {
-  int mtiles0, mtiles_total;   // tiles of segment 0; of both segments
+  int mstart[4];               // first tile of each segment; mstart[nseg] = all tiles
+  int mtiles_total;
   int mt;                      // 128-row tiles per CTA (> 1 only without split-K)
-  int rows[2], col0[2];
+  int rows[3], col0[3];
   int N, K, Z;
   int n_tile, nstage, stage_bytes, splits, kstages;
   uint32_t tmem_cols, idesc;
-  int epi; void* out; long long ldo, bo;
+  int epi[3]; void* out[3]; long long ldo[3], bo[3];
+  long long seg_stride[3]; int seg_off[3];
   const float* rope_cos; const float* rope_sin; int d_r; int max_pos;
-  const int32_t* pos; long long seg_stride; int seg_off;
+  const int32_t* pos;
   const int32_t* tok_seq; const int32_t* tok_pos; int cache_batch; int max_len; int d_c; int row_width;
   int32_t* status;
 };
@@ -86,7 +88,8 @@ __device__ __forceinline__ float rope_apply(float v, float partner, bool first_h
 template <int CPB, bool TRANS>
 __global__ void __launch_bounds__(NTHREADS, 1)
     gemm_tc_kernel(const __grid_constant__ CUtensorMap map_w0, const __grid_constant__ CUtensorMap map_w1,
-                   const __grid_constant__ CUtensorMap map_x, const Params p) {
+                   const __grid_constant__ CUtensorMap map_w2, const __grid_constant__ CUtensorMap map_x,
+                   const Params p) {
   constexpr int A_TILE = CPB * CHUNK_A;   // one weight tile of one stage
   constexpr int KSTEPS = CPB * (BK / 16);
   extern __shared__ uint8_t smem_raw[];
@@ -97,13 +100,13 @@ __global__ void __launch_bounds__(NTHREADS, 1)
   const int S = p.splits, MT = p.mt;
   const int group = blockIdx.x / S, split = blockIdx.x % S;
   const int tile0 = group * MT;
-  const int seg = tile0 < p.mtiles0 ? 0 : 1;
-  const int m0 = (seg == 0 ? tile0 : tile0 - p.mtiles0) * BM;
+  const int seg = (tile0 >= p.mstart[1] ? 1 : 0) + (tile0 >= p.mstart[2] ? 1 : 0);
+  const int m0 = (tile0 - p.mstart[seg]) * BM;
   const int n0 = blockIdx.y * p.n_tile;
   const int z = blockIdx.z;
   const int ks0 = (int)((long long)split * p.kstages / S), ks1 = (int)((long long)(split + 1) * p.kstages / S);
   const int nk = ks1 - ks0;
-  const CUtensorMap* map_w = seg == 0 ? &map_w0 : &map_w1;
+  const CUtensorMap* map_w = seg == 0 ? &map_w0 : (seg == 1 ? &map_w1 : &map_w2);
 
   if (threadIdx.x == 0) {
     for (int i = 0; i < p.nstage; ++i) { mbar_init(&ctl.full[i], 1); mbar_init(&ctl.empty[i], 1); }
@@ -244,7 +247,9 @@ __global__ void __launch_bounds__(NTHREADS, 1)
   if (warp >= 2) {
     const int et = threadIdx.x - 64;
     const float* cs = reinterpret_cast<const float*>(smem);
-    __nv_bfloat16* out = static_cast<__nv_bfloat16*>(p.out);
+    __nv_bfloat16* out = static_cast<__nv_bfloat16*>(p.out[seg]);
+    const int epi = p.epi[seg];
+    const long long ldo = p.ldo[seg], bo = p.bo[seg];
     // Each thread stores 8 consecutive output columns (one 16-byte vector)
     // of one activation row per pass: 16 threads span a 128-row tile, the 128
     // epilogue threads 8 rows n. Rows owned by this CTA: n = split + S j.
@@ -265,9 +270,9 @@ __global__ void __launch_bounds__(NTHREADS, 1)
           v[0] = a0.x; v[1] = a0.y; v[2] = a0.z; v[3] = a0.w; v[4] = a1.x; v[5] = a1.y; v[6] = a1.z; v[7] = a1.w;
         }
         __nv_bfloat16* dst;
-        if (p.epi == EPI_STORE) {
-          dst = out + z * p.bo + gn * p.ldo + p.col0[seg] + mb;
-        } else if (p.epi == EPI_ROPE_SEGS) {
+        if (epi == EPI_STORE) {
+          dst = out + z * bo + gn * ldo + p.col0[seg] + mb;
+        } else if (epi == EPI_ROPE_SEGS) {
           // 8 rows of one rotated segment, all in one half of it (d_r % 16 == 0)
           const int half = p.d_r / 2;
           const int sg = mb / p.d_r, j0 = mb % p.d_r;
@@ -284,7 +289,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
             const float c = p.rope_cos[(long long)ps * half + jj + e], sn = p.rope_sin[(long long)ps * half + jj + e];
             v[e] = rope_apply(v[e], pr[e], first, c, sn);
           }
-          dst = out + gn * p.ldo + sg * p.seg_stride + p.seg_off + j0;
+          dst = out + gn * ldo + sg * p.seg_stride[seg] + p.seg_off[seg] + j0;
         } else {  // EPI_APPEND
           const int sq = p.tok_seq[gn], ps = p.tok_pos[gn];
           const bool seq_ok = sq >= 0 && sq < p.cache_batch;
@@ -337,7 +342,7 @@ uint32_t pow2_at_least(uint32_t x) {
 
 template <int CPB, bool TRANS>
 cudaError_t launch_typed(const CUtensorMap* mw, const CUtensorMap& mx, const Params& p, dim3 grid, size_t smem_dyn,
-                         cudaStream_t s) {
+                         cudaStream_t s) {  // mw: three weight maps
   static size_t smem_set = 0;  // per instantiation: the largest size requested so far
   if (smem_dyn > smem_set) {
     cudaError_t e = cudaFuncSetAttribute(gemm_tc_kernel<CPB, TRANS>, cudaFuncAttributeMaxDynamicSharedMemorySize,
@@ -346,7 +351,7 @@ cudaError_t launch_typed(const CUtensorMap* mw, const CUtensorMap& mx, const Par
     smem_set = smem_dyn;
   }
   LaunchCfg lc(grid, dim3(NTHREADS), smem_dyn, s, (unsigned)p.splits);
-  cudaError_t e = cudaLaunchKernelEx(&lc.cfg, gemm_tc_kernel<CPB, TRANS>, mw[0], mw[1], mx, p);
+  cudaError_t e = cudaLaunchKernelEx(&lc.cfg, gemm_tc_kernel<CPB, TRANS>, mw[0], mw[1], mw[2], mx, p);
   if (e != cudaSuccess) return e;
   return cudaGetLastError();
 }
@@ -354,36 +359,54 @@ cudaError_t launch_typed(const CUtensorMap* mw, const CUtensorMap& mx, const Par
 }  // namespace
 
 bool gemm_tc_shape_ok(const TcGemm& g) {
-  if (g.N <= 0 || g.K <= 0 || g.Z <= 0 || g.nseg < 1 || g.nseg > 2) return false;
+  if (g.N <= 0 || g.K <= 0 || g.Z <= 0 || g.nseg < 1 || g.nseg > 3) return false;
   // Column chunks of 64 must not run past a row: the chunked views have no
   // per-row bound inside a chunk.
   if ((g.K % BK) || (g.ldx % 8) || (g.bx % 8) || (g.ldw % 8) || (g.bw % 8)) return false;
+  if (reinterpret_cast<uintptr_t>(g.x) & 15) return false;
+  if (g.nseg > 1 && g.w_transposed) return false;
   for (int s = 0; s < g.nseg; ++s) {
     if (g.rows[s] <= 0 || !g.w[s] || (reinterpret_cast<uintptr_t>(g.w[s]) & 15)) return false;
     if (g.w_transposed && (g.rows[s] % 64)) return false;
+    // The epilogue stores 8 consecutive bf16 outputs (16 bytes) at a time;
+    // RoPE keeps each group of 8 inside one half of a rotated segment, whose
+    // partner rows share the 128-row tile.
+    const int e = g.epi[s];
+    if (!g.out[s] || (reinterpret_cast<uintptr_t>(g.out[s]) & 15)) return false;
+    if ((g.ldo[s] % 8) || (g.bo[s] % 8) || (g.col0[s] % 8)) return false;
+    if (e == EPI_ROPE_SEGS || e == EPI_APPEND) {
+      if (g.d_r <= 0 || (BM % g.d_r) || (g.d_r % 16)) return false;
+    }
+    if (e == EPI_ROPE_SEGS && ((g.seg_stride[s] % 8) || (g.seg_off[s] % 8))) return false;
+    if (e == EPI_APPEND) {
+      if ((g.row_width % 8) || (g.d_c % 8)) return false;
+      // a cache segment is either inside the latent columns or exactly the rotated ones
+      const bool latent = g.col0[s] + g.rows[s] <= g.d_c;
+      const bool rope = g.col0[s] == g.d_c && g.rows[s] == g.d_r;
+      if (!latent && !rope) return false;
+    }
+    if (e != EPI_STORE && e != EPI_ROPE_SEGS && e != EPI_APPEND) return false;
   }
-  if (reinterpret_cast<uintptr_t>(g.x) & 15) return false;
-  if (g.nseg == 2 && g.w_transposed) return false;
-  // RoPE partners must share a tile: segments of d_r rows must tile 128 rows.
-  if ((g.epi == EPI_ROPE_SEGS || g.epi == EPI_APPEND) && (g.d_r <= 0 || (BM % g.d_r) || (g.d_r & 1))) return false;
-  if (g.epi == EPI_APPEND && (g.nseg != 2 || g.rows[1] != g.d_r || g.col0[1] != g.d_c)) return false;
-  // The epilogue stores 8 consecutive bf16 outputs (16 bytes) at a time; RoPE
-  // keeps each group of 8 inside one half of a rotated segment.
-  if (reinterpret_cast<uintptr_t>(g.out) & 15) return false;
-  if ((g.ldo % 8) || (g.bo % 8) || (g.col0[0] % 8) || (g.nseg == 2 && (g.col0[1] % 8))) return false;
-  if ((g.epi == EPI_ROPE_SEGS || g.epi == EPI_APPEND) && (g.d_r % 16)) return false;
-  if (g.epi == EPI_ROPE_SEGS && ((g.seg_stride % 8) || (g.seg_off % 8))) return false;
-  if (g.epi == EPI_APPEND && ((g.row_width % 8) || (g.d_c % 8))) return false;
   return true;
 }
 
 cudaError_t launch_gemm_tc(const TcGemm& g, int num_sms, cudaStream_t s) {
   if (!gemm_tc_shape_ok(g)) return cudaErrorInvalidValue;
   Params p{};
-  p.rows[0] = g.rows[0]; p.rows[1] = g.nseg == 2 ? g.rows[1] : 0;
-  p.col0[0] = g.col0[0]; p.col0[1] = g.nseg == 2 ? g.col0[1] : 0;
-  p.mtiles0 = (g.rows[0] + BM - 1) / BM;
-  p.mtiles_total = p.mtiles0 + (g.nseg == 2 ? (g.rows[1] + BM - 1) / BM : 0);
+  p.mstart[0] = 0;
+  for (int sg = 0; sg < 3; ++sg) {
+    const bool on = sg < g.nseg;
+    p.rows[sg] = on ? g.rows[sg] : 0;
+    p.col0[sg] = on ? g.col0[sg] : 0;
+    p.epi[sg] = on ? g.epi[sg] : EPI_STORE;
+    p.out[sg] = on ? g.out[sg] : nullptr;
+    p.ldo[sg] = on ? g.ldo[sg] : 0;
+    p.bo[sg] = on ? g.bo[sg] : 0;
+    p.seg_stride[sg] = on ? g.seg_stride[sg] : 0;
+    p.seg_off[sg] = on ? g.seg_off[sg] : 0;
+    p.mstart[sg + 1] = p.mstart[sg] + (on ? (g.rows[sg] + BM - 1) / BM : 0);
+  }
+  p.mtiles_total = p.mstart[3];
   p.N = g.N; p.K = g.K; p.Z = g.Z;
   p.n_tile = g.N >= 256 ? 256 : ((g.N + 15) / 16) * 16;
   const int kchunks = g.K / BK;
@@ -395,7 +418,7 @@ cudaError_t launch_gemm_tc(const TcGemm& g, int num_sms, cudaStream_t s) {
   // split-K is therefore off (one segment; the tiles' accumulators fit TMEM).
   int mt = 1;
   const long long tiles1 = (long long)p.mtiles_total * n_tiles * g.Z;
-  if (tiles1 > num_sms && g.nseg == 1 && g.epi == EPI_STORE) {
+  if (tiles1 > num_sms && g.nseg == 1 && g.epi[0] == EPI_STORE) {
     for (int c = 2; c <= MAX_MT; c *= 2)
       if (p.mtiles_total % c == 0 && c * p.n_tile <= 512) {
         mt = c;
@@ -428,9 +451,8 @@ cudaError_t launch_gemm_tc(const TcGemm& g, int num_sms, cudaStream_t s) {
   const size_t smem_dyn = (cs_bytes > stages ? cs_bytes : stages) + 1024;
   p.tmem_cols = pow2_at_least((uint32_t)(mt * p.n_tile));
   p.idesc = idesc_bf16(BM, p.n_tile, g.w_transposed != 0, false);
-  p.epi = g.epi; p.out = g.out; p.ldo = g.ldo; p.bo = g.bo;
   p.rope_cos = g.rope_cos; p.rope_sin = g.rope_sin; p.d_r = g.d_r; p.max_pos = g.max_pos;
-  p.pos = g.pos; p.seg_stride = g.seg_stride; p.seg_off = g.seg_off;
+  p.pos = g.pos;
   p.tok_seq = g.tok_seq; p.tok_pos = g.tok_pos; p.cache_batch = g.cache_batch; p.max_len = g.max_len;
   p.d_c = g.d_c; p.row_width = g.row_width; p.status = g.status;
 
@@ -438,8 +460,8 @@ cudaError_t launch_gemm_tc(const TcGemm& g, int num_sms, cudaStream_t s) {
   //   weights    {64, rows, K/64, Z}   box {64, 128, CPB, 1}
   //   transposed {64, K, rows/64, Z}   box {64, 64 CPB, 2, 1}   (stored [K][rows])
   //   activation {64, N, K/64, Z}      box {64, n_tile, CPB, 1}
-  CUtensorMap mw[2], mx;
-  for (int sg = 0; sg < 2; ++sg) {
+  CUtensorMap mw[3], mx;
+  for (int sg = 0; sg < 3; ++sg) {
     const int src = sg < g.nseg ? sg : 0;
     uint64_t dims[4], strides[3];
     uint32_t box[4];

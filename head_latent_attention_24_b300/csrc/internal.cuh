@@ -109,17 +109,19 @@ cudaError_t launch_gemm_simt(const GemmArgs& a, int dtype, cudaStream_t s);
 // segments are stacked along m (S1: W_DKV rows, then W_KR rows); segment s
 // fills output columns [col0[s], col0[s] + rows[s]).
 struct TcGemm {
-  int nseg;
-  const void* w[2];            // segment base (batch 0)
-  int rows[2];                 // m extent of each segment
-  int col0[2];                 // first output column of each segment
+  int nseg;                    // weight segments stacked along M (1..3), sharing X and ldw/bw
+  const void* w[3];            // segment base (batch 0)
+  int rows[3];                 // m extent of each segment
+  int col0[3];                 // first output column of each segment
+  int epi[3];                  // epilogue of each segment
+  void* out[3]; long long ldo[3], bo[3];
+  long long seg_stride[3]; int seg_off[3];   // EPI_ROPE_SEGS output layout
   long long ldw, bw;           // element stride between W rows; between batches
   int w_transposed;            // W'[m, k] = W[k*ldw + m] (stored [K rows][M cols])
   const void* x; long long ldx, bx;
   int N, K, Z;                 // rows of X, reduction length, batch count
-  int epi; void* out; long long ldo, bo;
   const float* rope_cos; const float* rope_sin; int d_r; int max_pos;
-  const int32_t* pos; long long seg_stride; int seg_off;
+  const int32_t* pos;
   const int32_t* tok_seq; const int32_t* tok_pos; int cache_batch; int max_len; int d_c; int row_width;
   int32_t* status;
 };

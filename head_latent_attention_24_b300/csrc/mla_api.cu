@@ -27,9 +27,17 @@ bool use_tc_proj(const mla_handle_s* h, const TcGemm& g) {
   return gemm_tc_shape_ok(g);
 }
 
+// Segment s of a tensor-core projection: weight rows, output columns and epilogue.
+void tc_seg(TcGemm& g, int s, const void* w, int rows, int col0, int epi, void* out, long long ldo,
+            long long bo = 0, long long seg_stride = 0, int seg_off = 0) {
+  g.w[s] = w; g.rows[s] = rows; g.col0[s] = col0; g.epi[s] = epi; g.out[s] = out; g.ldo[s] = ldo; g.bo[s] = bo;
+  g.seg_stride[s] = seg_stride; g.seg_off[s] = seg_off;
+  if (s + 1 > g.nseg) g.nseg = s + 1;
+}
+
 TcGemm tc_base(const mla_handle_s* h) {
   TcGemm g{};
-  g.nseg = 1; g.Z = 1;
+  g.nseg = 0; g.Z = 1;
   g.rope_cos = h->rope_cos; g.rope_sin = h->rope_sin; g.d_r = h->cfg.d_r; g.max_pos = h->cfg.max_pos;
   g.status = h->status;
   return g;
@@ -183,10 +191,11 @@ mla_status_t mla_append_cache(mla_handle_t h, const void* x, int32_t n_tokens, c
   {
     // One launch: the W_DKV rows then the W_KR rows, scattered to the cache rows.
     TcGemm g = tc_base(h);
-    g.nseg = 2; g.w[0] = W_DKV; g.w[1] = W_KR; g.rows[0] = c.d_c; g.rows[1] = c.d_r;
-    g.col0[0] = 0; g.col0[1] = c.d_c; g.ldw = c.d; g.bw = 0;
+    tc_seg(g, 0, W_DKV, c.d_c, 0, EPI_APPEND, cache, 0);
+    tc_seg(g, 1, W_KR, c.d_r, c.d_c, EPI_APPEND, cache, 0);
+    g.ldw = c.d; g.bw = 0;
     g.x = x; g.ldx = c.d; g.bx = 0; g.K = c.d;
-    g.epi = EPI_APPEND; g.out = cache; g.tok_seq = tok_seq; g.tok_pos = tok_pos; g.cache_batch = batch;
+    g.tok_seq = tok_seq; g.tok_pos = tok_pos; g.cache_batch = batch;
     g.max_len = max_len; g.d_c = c.d_c; g.row_width = D;
     g.N = n_tokens;
     if (h->proj_path == MLA_PROJ_TCGEN05 && !use_tc_proj(h, g)) return MLA_ERR_UNSUPPORTED;
@@ -267,27 +276,24 @@ mla_status_t mla_absorb_q(mla_handle_t h, const void* x, int32_t batch, const vo
 
   {
     TcGemm g1 = tc_base(h);  // c_Q = W_DQ x
-    g1.w[0] = W_DQ; g1.rows[0] = c.d_cq; g1.ldw = c.d; g1.x = x; g1.ldx = c.d; g1.N = batch; g1.K = c.d;
-    g1.epi = EPI_STORE; g1.out = c_q; g1.ldo = c.d_cq;
-    TcGemm g2 = tc_base(h);  // q_C = W_UQ c_Q
-    g2.w[0] = W_UQ; g2.rows[0] = c.n_h * c.d_h; g2.ldw = c.d_cq; g2.x = c_q; g2.ldx = c.d_cq; g2.N = batch;
-    g2.K = c.d_cq; g2.epi = EPI_STORE; g2.out = q_c; g2.ldo = (long long)c.n_h * c.d_h;
-    TcGemm g3 = tc_base(h);  // q_R = RoPE(W_QR c_Q) -> q_abs[b, i, d_c:]
-    g3.w[0] = W_QR; g3.rows[0] = c.n_h * c.d_r; g3.ldw = c.d_cq; g3.x = c_q; g3.ldx = c.d_cq; g3.N = batch;
-    g3.K = c.d_cq; g3.epi = EPI_ROPE_SEGS; g3.out = q_abs; g3.ldo = (long long)c.n_h * D; g3.pos = pos;
-    g3.seg_stride = D; g3.seg_off = c.d_c;
+    tc_seg(g1, 0, W_DQ, c.d_cq, 0, EPI_STORE, c_q, c.d_cq);
+    g1.ldw = c.d; g1.x = x; g1.ldx = c.d; g1.N = batch; g1.K = c.d;
+    // q_C = W_UQ c_Q and q_R = RoPE(W_QR c_Q) -> q_abs[b, i, d_c:], one launch (same input)
+    TcGemm g2 = tc_base(h);
+    tc_seg(g2, 0, W_UQ, c.n_h * c.d_h, 0, EPI_STORE, q_c, (long long)c.n_h * c.d_h);
+    tc_seg(g2, 1, W_QR, c.n_h * c.d_r, 0, EPI_ROPE_SEGS, q_abs, (long long)c.n_h * D, 0, D, c.d_c);
+    g2.ldw = c.d_cq; g2.x = c_q; g2.ldx = c.d_cq; g2.N = batch; g2.K = c.d_cq; g2.pos = pos;
     TcGemm g4 = tc_base(h);  // q~_i = W_UK_i^T q_C_i -> q_abs[b, i, :d_c]
-    g4.w[0] = W_UK; g4.rows[0] = c.d_c; g4.w_transposed = 1; g4.ldw = c.d_c; g4.bw = (long long)c.d_h * c.d_c;
+    tc_seg(g4, 0, W_UK, c.d_c, 0, EPI_STORE, q_abs, (long long)c.n_h * D, D);
+    g4.w_transposed = 1; g4.ldw = c.d_c; g4.bw = (long long)c.d_h * c.d_c;
     g4.x = q_c; g4.ldx = (long long)c.n_h * c.d_h; g4.bx = c.d_h; g4.N = batch; g4.K = c.d_h; g4.Z = c.n_h;
-    g4.epi = EPI_STORE; g4.out = q_abs; g4.ldo = (long long)c.n_h * D; g4.bo = D;
-    const bool tc = use_tc_proj(h, g1) && use_tc_proj(h, g2) && use_tc_proj(h, g3) && use_tc_proj(h, g4);
+    const bool tc = use_tc_proj(h, g1) && use_tc_proj(h, g2) && use_tc_proj(h, g4);
     if (h->proj_path == MLA_PROJ_TCGEN05 && !tc) return MLA_ERR_UNSUPPORTED;
     if (tc) {
       if (launch_gemm_tc(g1, h->num_sms, s) != cudaSuccess) return MLA_ERR_CUDA;
       if (launch_gemm_tc(g2, h->num_sms, s) != cudaSuccess) return MLA_ERR_CUDA;
-      if (launch_gemm_tc(g3, h->num_sms, s) != cudaSuccess) return MLA_ERR_CUDA;
       if (launch_gemm_tc(g4, h->num_sms, s) != cudaSuccess) return MLA_ERR_CUDA;
-      h->last_launches = 4;
+      h->last_launches = 3;
       return MLA_OK;
     }
   }
@@ -384,13 +390,13 @@ mla_status_t mla_out_proj(mla_handle_t h, const void* o_lat, int32_t batch, cons
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   {
     TcGemm g1 = tc_base(h);  // o_i = W_UV_i o_lat_i
-    g1.w[0] = W_UV; g1.rows[0] = c.d_h; g1.ldw = c.d_c; g1.bw = (long long)c.d_h * c.d_c;
+    tc_seg(g1, 0, W_UV, c.d_h, 0, EPI_STORE, ws, (long long)c.n_h * c.d_h, c.d_h);
+    g1.ldw = c.d_c; g1.bw = (long long)c.d_h * c.d_c;
     g1.x = o_lat; g1.ldx = (long long)c.n_h * c.d_c; g1.bx = c.d_c; g1.N = batch; g1.K = c.d_c; g1.Z = c.n_h;
-    g1.epi = EPI_STORE; g1.out = ws; g1.ldo = (long long)c.n_h * c.d_h; g1.bo = c.d_h;
     TcGemm g2 = tc_base(h);  // u = W_O o
-    g2.w[0] = W_O; g2.rows[0] = c.d; g2.ldw = (long long)c.n_h * c.d_h; g2.x = ws;
-    g2.ldx = (long long)c.n_h * c.d_h; g2.N = batch; g2.K = c.n_h * c.d_h; g2.epi = EPI_STORE; g2.out = u;
-    g2.ldo = c.d;
+    tc_seg(g2, 0, W_O, c.d, 0, EPI_STORE, u, c.d);
+    g2.ldw = (long long)c.n_h * c.d_h; g2.x = ws; g2.ldx = (long long)c.n_h * c.d_h; g2.N = batch;
+    g2.K = c.n_h * c.d_h;
     const bool tc = use_tc_proj(h, g1) && use_tc_proj(h, g2);
     if (h->proj_path == MLA_PROJ_TCGEN05 && !tc) return MLA_ERR_UNSUPPORTED;
     if (tc) {
