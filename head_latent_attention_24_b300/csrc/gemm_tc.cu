@@ -200,17 +200,22 @@ __global__ void __launch_bounds__(NTHREADS, 1)
     const bool ok = nk > 0 && wait_bar(&ctl.acc_full, 0, ctl, p.status);
     if (ok) tc_fence_after();
     for (int t = 0; t < MT; ++t) {
-      for (int c = 0; c < p.n_tile; c += 16) {
-        float v[16];
+      for (int c = 0; c < p.n_tile; c += 64) {
+        float v[64];
+        const int nc = min(64, p.n_tile - c);   // n_tile is a multiple of 16
         if (ok) {
-          tmem_ld16(tbase + (static_cast<uint32_t>(quarter * 32) << 16) + (uint32_t)(t * p.n_tile + c), v);
+          const uint32_t ta = tbase + (static_cast<uint32_t>(quarter * 32) << 16) + (uint32_t)(t * p.n_tile + c);
+#pragma unroll
+          for (int q = 0; q < 4; ++q)
+            if (16 * q < nc) tmem_ld16(ta + 16 * q, *reinterpret_cast<float(*)[16]>(v + 16 * q));
           tmem_ld_wait();
         } else {
 #pragma unroll
-          for (int i = 0; i < 16; ++i) v[i] = 0.f;
+          for (int i = 0; i < 64; ++i) v[i] = 0.f;
         }
 #pragma unroll
-        for (int i = 0; i < 16; ++i) cs[(t * p.n_tile + c + i) * BM + m] = v[i];
+        for (int i = 0; i < 64; ++i)
+          if (i < nc) cs[(t * p.n_tile + c + i) * BM + m] = v[i];
       }
     }
   }
@@ -221,26 +226,39 @@ __global__ void __launch_bounds__(NTHREADS, 1)
   cluster_sync();  // every partial tile of the cluster is in shared memory
   const int n_valid = min(p.n_tile, p.N - n0);
   if (warp >= 2 && S > 1) {
-    // MT == 1 whenever S > 1
+    // MT == 1 whenever S > 1. Each warp sums rows n of the tile (this CTA's
+    // rows n = split + S j) over the S partials, in split order; the loads of
+    // two rows from all S CTAs are issued before any of them is used.
     const int et = threadIdx.x - 64;
     float* cs = reinterpret_cast<float*>(smem);
     const uint32_t cs_addr = smem_u32(cs);
     const int rgrp = et >> 5, m4 = (et & 31) * 4;
-    for (int n = split + S * rgrp; n < n_valid; n += 4 * S) {
-      float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-      const uint32_t off = (uint32_t)((n * BM + m4) * 4);
-      for (int r = 0; r < S; ++r) {
-        const uint32_t a = mapa_shared(cs_addr + off, (uint32_t)r);
-        float4 v;
-        asm volatile("ld.shared::cluster.v4.f32 {%0,%1,%2,%3}, [%4];"
-                     : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w)
-                     : "r"(a)
-                     : "memory");
-        acc.x += v.x; acc.y += v.y; acc.z += v.z; acc.w += v.w;
+    for (int nb = split + S * rgrp; nb < n_valid; nb += 8 * S) {
+      float4 v[2][MAX_SPLITS];
+#pragma unroll
+      for (int q = 0; q < 2; ++q) {
+        const int n = nb + q * 4 * S;
+#pragma unroll
+        for (int r = 0; r < MAX_SPLITS; ++r)
+          if (r < S && n < n_valid) {
+            const uint32_t a = mapa_shared(cs_addr + (uint32_t)((n * BM + m4) * 4), (uint32_t)r);
+            asm volatile("ld.shared::cluster.v4.f32 {%0,%1,%2,%3}, [%4];"
+                         : "=f"(v[q][r].x), "=f"(v[q][r].y), "=f"(v[q][r].z), "=f"(v[q][r].w)
+                         : "r"(a));
+          }
       }
-      // Peers may still be reading this CTA's partials: the sum goes to a
-      // separate region holding this CTA's own rows.
-      *reinterpret_cast<float4*>(cs + p.n_tile * BM + (n / S) * BM + m4) = acc;
+#pragma unroll
+      for (int q = 0; q < 2; ++q) {
+        const int n = nb + q * 4 * S;
+        if (n >= n_valid) continue;
+        float4 acc = v[q][0];
+#pragma unroll
+        for (int r = 1; r < MAX_SPLITS; ++r)
+          if (r < S) { acc.x += v[q][r].x; acc.y += v[q][r].y; acc.z += v[q][r].z; acc.w += v[q][r].w; }
+        // Peers may still be reading this CTA's partials: the sum goes to a
+        // separate region holding this CTA's own rows.
+        *reinterpret_cast<float4*>(cs + p.n_tile * BM + (n / S) * BM + m4) = acc;
+      }
     }
   }
   cluster_sync();  // all remote reads done: no CTA's shared memory is needed by a peer any more
