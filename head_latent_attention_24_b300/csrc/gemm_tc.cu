@@ -46,7 +46,8 @@ constexpr int CHUNK_A = BM * BK * 2;   // 16 KB: one chunk of a weight tile
 constexpr int NTHREADS = 192;
 constexpr int MAX_SPLITS = 8;
 constexpr int MAX_MT = 4;
-constexpr int SMEM_BUDGET = 200 * 1024;
+constexpr int SMEM_ONE = 200 * 1024;   // stage budget with one CTA per SM
+constexpr int SMEM_TWO = 100 * 1024;   // with two
 constexpr long long WAIT_CYCLES = 4000000000LL;  // ~2 s
 
 struct Params {
@@ -86,7 +87,7 @@ __device__ __forceinline__ float rope_apply(float v, float partner, bool first_h
 // CPB: column chunks per stage. TRANS: the weights are stored [K rows][M
 // columns] and read MN-major (A'[m, k] = W[k, m]).
 template <int CPB, bool TRANS>
-__global__ void __launch_bounds__(NTHREADS, 1)
+__global__ void __launch_bounds__(NTHREADS, 2)
     gemm_tc_kernel(const __grid_constant__ CUtensorMap map_w0, const __grid_constant__ CUtensorMap map_w1,
                    const __grid_constant__ CUtensorMap map_w2, const __grid_constant__ CUtensorMap map_x,
                    const Params p) {
@@ -431,6 +432,13 @@ cudaError_t launch_gemm_tc(const TcGemm& g, int num_sms, cudaStream_t s) {
   const long long n_tiles = (g.N + p.n_tile - 1) / p.n_tile;
   if (n_tiles > 65535 || g.Z > 65535) return cudaErrorInvalidValue;
   if (num_sms < 1) num_sms = 1;
+  // When the tiles outnumber the SMs, two CTAs share an SM (half the stage
+  // budget each) so that every tile is resident at once; otherwise one CTA
+  // per SM keeps the most bytes in flight per tile.
+  const long long tiles_all = (long long)p.mtiles_total * n_tiles * g.Z;
+  const int per_sm = tiles_all > num_sms ? 2 : 1;
+  const int budget = per_sm == 2 ? SMEM_TWO : SMEM_ONE;
+  num_sms *= per_sm;
 
   // Tiles per CTA: more than one only when the tiles outnumber the SMs and
   // split-K is therefore off (one segment; the tiles' accumulators fit TMEM).
@@ -448,13 +456,13 @@ cudaError_t launch_gemm_tc(const TcGemm& g, int num_sms, cudaStream_t s) {
   // stage if it is the only one), at most what the reduction has.
   auto stage_of = [&](int cpb) { return mt * cpb * CHUNK_A + cpb * p.n_tile * 128; };
   int cpb = 4;
-  while (cpb > 1 && (cpb > kchunks || 2 * stage_of(cpb) > SMEM_BUDGET) &&
-         !(cpb <= kchunks && (kchunks + cpb - 1) / cpb == 1 && stage_of(cpb) <= SMEM_BUDGET))
+  while (cpb > 1 && (cpb > kchunks || 2 * stage_of(cpb) > budget) &&
+         !(cpb <= kchunks && (kchunks + cpb - 1) / cpb == 1 && stage_of(cpb) <= budget))
     cpb >>= 1;
   p.stage_bytes = stage_of(cpb);
-  if (p.stage_bytes > SMEM_BUDGET) return cudaErrorInvalidValue;
+  if (p.stage_bytes > budget) return cudaErrorInvalidValue;
   p.kstages = (kchunks + cpb - 1) / cpb;
-  p.nstage = SMEM_BUDGET / p.stage_bytes;
+  p.nstage = budget / p.stage_bytes;
   if (p.nstage > 8) p.nstage = 8;
   if (p.nstage > p.kstages) p.nstage = p.kstages;
   const long long tiles = tiles1 / mt;
