@@ -293,3 +293,29 @@ class MLADecoder:
         n += mla_last_launch_count(self.handle)
         self.launches = n
         return self.u
+
+    def capture(self, cache):
+        """Record one decode step as a CUDA graph: the step reads its inputs
+        from the decoder's buffers h_in [B, d], pos_in [B] and seqlens_in [B]
+        (copy each step's values into them) and works on `cache`; replay()
+        then runs the whole step with one launch from the host. The graph
+        keeps this cache's and these buffers' addresses and the kernels'
+        launch parameters, so it is valid while they stay allocated. Run at
+        least one eager step first (it sets the kernels' launch attributes)."""
+        import torch
+        dev = self.u.device
+        self.h_in = torch.zeros((self.batch, self.shape.d), dtype=self.torch_dtype, device=dev)
+        self.pos_in = torch.zeros(self.batch, dtype=torch.int32, device=dev)
+        self.seqlens_in = torch.ones(self.batch, dtype=torch.int32, device=dev)
+        torch.cuda.synchronize(dev)
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graph):
+            self.step(self.h_in, self.pos_in, cache, self.seqlens_in)
+        self.graph = graph
+        self.graph_launches = self.launches
+        return graph
+
+    def replay(self):
+        """Run the captured step on the current stream; returns u [B, d]."""
+        self.graph.replay()
+        return self.u
