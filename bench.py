@@ -45,12 +45,13 @@ def load_peaks():
 
 
 def kernel_source_hash() -> str:
+    """Hash of the attention kernel's sources (the kernel the committed
+    traffic figure was measured on, and the headers it includes)."""
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "head_latent_attention_24_b300", "csrc")
-    for n in sorted(os.listdir(csrc)):
-        if n.startswith("decode"):
-            with open(os.path.join(csrc, n), "rb") as f:
-                h.update(n.encode() + f.read())
+    for n in ("decode_pair.cu", "decode_tc.cuh", "tc_ptx.cuh", "tmap.cuh", "internal.cuh"):
+        with open(os.path.join(csrc, n), "rb") as f:
+            h.update(n.encode() + f.read())
     return h.hexdigest()[:16]
 
 

@@ -268,8 +268,8 @@ __global__ void __launch_bounds__(NT) decode_simt_kernel(const DecodeArgs a) {
 
 // One CTA per (sequence, head): merges the partial results of a split sequence
 // and writes o_lat = 0, lse = -inf for an empty one.
-// One warp per (sequence, head): the lanes reduce the pieces' LSEs with
-// shuffles and stream the fp32 partials with 16-byte loads (a warp reads 512
+// One warp per (sequence, head): every lane reads the pieces' LSEs and its
+// columns of their fp32 partials with 16-byte loads (a warp reads 512
 // contiguous bytes per load), writing o_lat = sum_j e^{lse_j - lse} o_j.
 template <typename T>
 __global__ void __launch_bounds__(256) decode_combine_kernel(const DecodeArgs a) {
@@ -292,32 +292,56 @@ __global__ void __launch_bounds__(256) decode_combine_kernel(const DecodeArgs a)
   if (c0 == c1) return;  // written whole by the attention kernel
   const int np = c1 - c0 + 1;
   const float* plse = a.part_lse + (long long)(b + c0) * a.n_h + h;
-  float mx = -INFINITY;
-  for (int j = lane; j < np; j += 32) mx = fmaxf(mx, plse[(long long)j * a.n_h]);
-  mx = warp_max(mx);
-  float sum = 0.f;
-  for (int j = lane; j < np; j += 32) sum += expf(plse[(long long)j * a.n_h] - mx);
-  sum = warp_sum(sum);
-  const float inv = 1.f / sum;
   const float* po = a.part_o + ((long long)(b + c0) * a.n_h + h) * d_c;
   const long long pstride = (long long)a.n_h * d_c;
   // d_c <= 512: each lane owns up to 4 groups of 4 columns (e = lane*4 + 128 q).
-  // All of a piece's loads are issued before any of them is used.
+  // The LSEs and partial rows of up to four pieces are loaded together, before
+  // any of them is used (one memory round trip for the usual two pieces).
+  constexpr int PRE = 4;
   const int nq = (d_c - lane * 4 + 127) / 128;
+  float lj[PRE];
+  float4 v[PRE][4];
+#pragma unroll
+  for (int j = 0; j < PRE; ++j)
+    if (j < np) {
+      lj[j] = __ldg(plse + (long long)j * a.n_h);
+#pragma unroll
+      for (int q = 0; q < 4; ++q)
+        if (q < nq) v[j][q] = __ldg(reinterpret_cast<const float4*>(po + j * pstride + lane * 4 + q * 128));
+    }
+  float mx = -INFINITY;
+#pragma unroll
+  for (int j = 0; j < PRE; ++j)
+    if (j < np) mx = fmaxf(mx, lj[j]);
+  for (int j = PRE; j < np; ++j) mx = fmaxf(mx, __ldg(plse + (long long)j * a.n_h));
+  float sum = 0.f;
+#pragma unroll
+  for (int j = 0; j < PRE; ++j)
+    if (j < np) sum += expf(lj[j] - mx);
+  for (int j = PRE; j < np; ++j) sum += expf(__ldg(plse + (long long)j * a.n_h) - mx);
+  const float inv = 1.f / sum;
   float4 acc[4];
 #pragma unroll
   for (int q = 0; q < 4; ++q) acc[q] = make_float4(0.f, 0.f, 0.f, 0.f);
-  for (int j = 0; j < np; ++j) {
-    const float w = expf(plse[(long long)j * a.n_h] - mx) * inv;
-    float4 v[4];
 #pragma unroll
-    for (int q = 0; q < 4; ++q)
-      if (q < nq) v[q] = __ldg(reinterpret_cast<const float4*>(po + j * pstride + lane * 4 + q * 128));
+  for (int j = 0; j < PRE; ++j)
+    if (j < np) {
+      const float w = expf(lj[j] - mx) * inv;
+#pragma unroll
+      for (int q = 0; q < 4; ++q)
+        if (q < nq) {
+          acc[q].x = fmaf(w, v[j][q].x, acc[q].x); acc[q].y = fmaf(w, v[j][q].y, acc[q].y);
+          acc[q].z = fmaf(w, v[j][q].z, acc[q].z); acc[q].w = fmaf(w, v[j][q].w, acc[q].w);
+        }
+    }
+  for (int j = PRE; j < np; ++j) {
+    const float w = expf(__ldg(plse + (long long)j * a.n_h) - mx) * inv;
 #pragma unroll
     for (int q = 0; q < 4; ++q)
       if (q < nq) {
-        acc[q].x = fmaf(w, v[q].x, acc[q].x); acc[q].y = fmaf(w, v[q].y, acc[q].y);
-        acc[q].z = fmaf(w, v[q].z, acc[q].z); acc[q].w = fmaf(w, v[q].w, acc[q].w);
+        const float4 x = __ldg(reinterpret_cast<const float4*>(po + j * pstride + lane * 4 + q * 128));
+        acc[q].x = fmaf(w, x.x, acc[q].x); acc[q].y = fmaf(w, x.y, acc[q].y);
+        acc[q].z = fmaf(w, x.z, acc[q].z); acc[q].w = fmaf(w, x.w, acc[q].w);
       }
   }
 #pragma unroll
