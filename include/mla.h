@@ -39,6 +39,14 @@
  *     turned by pos * base^(-2j/d_r); cos/sin table built in fp64 on the host
  *     and rounded once to fp32.
  *   - Results are deterministic for a fixed (batch, seqlens, device SM count).
+ *   - The tensor-core kernels are launched with programmatic dependent launch:
+ *     each may start while the previous kernel on the stream drains, but it
+ *     reads nothing an earlier kernel wrote, and writes nothing, before that
+ *     kernel has completed, so stream order holds as for plain launches. The
+ *     calls make no allocation and no synchronisation, so a sequence of them
+ *     can be captured into a CUDA graph (after one eager call has set the
+ *     kernels' launch attributes); the graph keeps the pointers and sizes of
+ *     the captured calls.
  */
 #ifndef MLA_H_
 #define MLA_H_
