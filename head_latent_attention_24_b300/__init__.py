@@ -83,6 +83,7 @@ _c = {
     "mla_out_proj": _sig("mla_out_proj", [_P, _P, _I, _P, _P, _P, _P, _S, _P]),
     "mla_get_device_status": _sig("mla_get_device_status", [_P, _P, ctypes.POINTER(_I)]),
     "mla_set_decode_path": _sig("mla_set_decode_path", [_P, _I]),
+    "mla_set_decode_chunks": _sig("mla_set_decode_chunks", [_P, _I]),
     "mla_get_decode_path": _sig("mla_get_decode_path", [_P, ctypes.POINTER(_I)]),
     "mla_set_proj_path": _sig("mla_set_proj_path", [_P, _I]),
     "mla_last_launch_count": _sig("mla_last_launch_count", [_P, ctypes.POINTER(_I)]),
@@ -193,6 +194,10 @@ def mla_get_device_status(handle, stream=None):
 
 def mla_set_decode_path(handle, path):
     _check(_c["mla_set_decode_path"](handle, path), "mla_set_decode_path")
+
+
+def mla_set_decode_chunks(handle, chunks):
+    _check(_c["mla_set_decode_chunks"](handle, chunks), "mla_set_decode_chunks")
 
 
 def mla_get_decode_path(handle) -> int:

@@ -17,6 +17,7 @@ struct mla_handle_s {
   float* rope_sin;         // device [max_pos, d_r/2]
   int32_t* status;         // device status word
   int32_t decode_path;     // mla_decode_path_t requested
+  int32_t decode_chunks;   // split-KV chunk count requested (0 = automatic)
   int32_t proj_path;       // mla_proj_path_t requested
   int32_t last_launches;   // launches made by the last successful call
 };

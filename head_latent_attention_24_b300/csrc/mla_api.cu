@@ -92,6 +92,7 @@ mla_status_t mla_create(const mla_config_t* cfg, mla_handle_t* out) {
   h->num_sms = sms;
   h->scale = (float)(1.0 / sqrt((double)(c.d_h + c.d_r)));
   h->decode_path = MLA_DECODE_AUTO;
+  h->decode_chunks = 0;
 
   // RoPE table: angle pos * base^(-2j/d_r) in fp64, cos/sin rounded once to fp32.
   const int half = c.d_r / 2;
@@ -136,6 +137,12 @@ mla_status_t mla_set_decode_path(mla_handle_t h, int32_t path) {
   if (!h || path < MLA_DECODE_AUTO || path > MLA_DECODE_TCGEN05) return MLA_ERR_INVALID_ARG;
   if (path == MLA_DECODE_TCGEN05 && !decode_tc_supported(h)) return MLA_ERR_UNSUPPORTED;
   h->decode_path = path;
+  return MLA_OK;
+}
+
+mla_status_t mla_set_decode_chunks(mla_handle_t h, int32_t chunks) {
+  if (!h || chunks < 0 || chunks > 65535) return MLA_ERR_INVALID_ARG;
+  h->decode_chunks = chunks;
   return MLA_OK;
 }
 
@@ -327,9 +334,10 @@ mla_status_t mla_absorb_q(mla_handle_t h, const void* x, int32_t batch, const vo
 mla_status_t mla_decode_workspace_size(mla_handle_t h, int32_t batch, int32_t max_len, size_t* bytes) {
   if (!h || !bytes || batch <= 0 || max_len <= 0) return MLA_ERR_INVALID_ARG;
   const mla_config_t& c = h->cfg;
-  size_t b = decode_ws_bytes(batch, c.n_h, c.d_c, decode_simt_chunks(h));
+  size_t b = decode_ws_bytes(batch, c.n_h, c.d_c, h->decode_chunks > 0 ? h->decode_chunks : decode_simt_chunks(h));
   if (decode_tc_supported(h)) {
-    const size_t t = decode_ws_bytes(batch, c.n_h, c.d_c, decode_tc_chunks(h, batch));
+    const size_t t =
+        decode_ws_bytes(batch, c.n_h, c.d_c, h->decode_chunks > 0 ? h->decode_chunks : decode_tc_chunks(h, batch));
     if (t > b) b = t;
   }
   *bytes = b;
@@ -360,7 +368,8 @@ mla_status_t mla_decode_attn(mla_handle_t h, const void* q_abs, const void* cach
   a.B = batch; a.max_len = max_len; a.n_h = c.n_h; a.d_c = c.d_c; a.d_r = c.d_r;
   a.scale_log2 = h->scale * 1.4426950408889634f;
   a.status = h->status;
-  a.grid_chunks = path == MLA_DECODE_TCGEN05 ? decode_tc_chunks(h, batch) : decode_simt_chunks(h);
+  a.grid_chunks = h->decode_chunks > 0 ? h->decode_chunks
+                                        : (path == MLA_DECODE_TCGEN05 ? decode_tc_chunks(h, batch) : decode_simt_chunks(h));
   decode_ws_carve(ws, batch, c.n_h, c.d_c, a.grid_chunks, &a.plan, &a.part_o, &a.part_lse);
   int launches = 0;
   cudaError_t e = path == MLA_DECODE_TCGEN05 ? launch_decode_tc(h, a, s, &launches)

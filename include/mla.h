@@ -210,6 +210,15 @@ MLA_API mla_status_t mla_set_decode_path(mla_handle_t handle, int32_t path);
 /* The path AUTO resolves to for this handle (MLA_DECODE_SIMT or MLA_DECODE_TCGEN05). */
 MLA_API mla_status_t mla_get_decode_path(mla_handle_t handle, int32_t* path);
 
+/* Number of split-KV chunks mla_decode_attn cuts the batch's rows into (CTA
+   pairs of the tensor-core kernel, CTA columns of the CUDA-core one); 0 (the
+   default) = one per pair of SMs / the CUDA-core kernel's usual grid.
+   Results differ between chunk counts only by summation order. The decode
+   workspace size grows with the count: query mla_decode_workspace_size after
+   setting it. Returns MLA_ERR_INVALID_ARG for a negative count or one above
+   65535. */
+MLA_API mla_status_t mla_set_decode_chunks(mla_handle_t handle, int32_t chunks);
+
 /* Kernel family of the projections (mla_append_cache, mla_absorb_q,
    mla_out_proj). AUTO picks the tensor-core (tcgen05) kernel for bf16 layers
    whose strides it takes (every width a multiple of 8, d_r dividing 128), else

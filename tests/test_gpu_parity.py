@@ -159,6 +159,37 @@ def paths():
     return [None, M.MLA_DECODE_SIMT]
 
 
+@pytest.mark.parametrize("name", ["minimind", "v2"])
+@pytest.mark.parametrize("chunks", [1, 3, 40, 200])
+def test_decode_attn_any_chunk_count(name, chunks):
+    """Split-KV with a forced chunk count, from one chunk for the whole batch
+    to 64-row slivers (a 700-row sequence then spans 11 chunks and the merge
+    takes 11 partials; most of the 200 chunks are empty): matches the oracle."""
+    shp = S.workload(name)
+    max_len = 700
+    seqlens = np.array([700, 1, 0, 333, 690])
+    B = len(seqlens)
+    q = S.draw_absorbed_queries(shp, B)
+    rows = [S.draw_latent_rows(shp, int(seqlens[b]), sub=b) for b in range(B)]
+    ref_o, ref_l = oracle_decode(shp, q, rows, seqlens)
+    cache = np.zeros((B, max_len, shp.D))
+    for b, r in enumerate(rows):
+        cache[b, :len(r)] = r
+    dec = decoder(shp, {k: torch.zeros(1, device="cuda") for k in S.WEIGHT_NAMES}, B, max_len)
+    M.mla_set_decode_chunks(dec.handle, chunks)
+    ws = torch.empty(M.mla_decode_workspace_size(dec.handle, B, max_len), dtype=torch.uint8, device="cuda")
+    M.mla_decode_attn(dec.handle, dev(q, shp), dev(cache, shp), B, max_len, dev_i32(seqlens), dec.o_lat, dec.lse,
+                      ws, ws.numel())
+    st, bits = M.mla_get_device_status(dec.handle)
+    assert st == M.MLA_OK and bits == 0
+    got_o, got_l = host(dec.o_lat), dec.lse.cpu().numpy().astype(np.float64)
+    nz = seqlens > 0
+    assert_close(got_o[nz], ref_o[nz], shp.dtype, what="o_lat")
+    assert np.all(got_o[~nz] == 0) and np.all(np.isneginf(got_l[~nz]))
+    assert np.abs(got_l[nz] - ref_l[nz]).max() <= 2e-4 * max(1, np.abs(ref_l[nz]).max())
+    dec.close()
+
+
 @pytest.mark.parametrize("name", SMALL)
 @pytest.mark.parametrize("pattern", list(SEQLEN_PATTERNS))
 def test_decode_attn_matches_oracle(name, pattern):
