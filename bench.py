@@ -4,7 +4,9 @@ A step is the whole hot path over one batch: append the new token's cache row
 (S1), absorb the query (S2), latent split-KV attention (S3) and the W_UV / W_O
 expansion (S4/S5), for the DeepSeek-V2-shaped layer (d=5120, n_h=128, d_h=128,
 d_c=512, d_r=64, d_cq=1536, bf16) at batch 64 with 4096 cached tokens per
-sequence. Inputs are synthetic (h ~ N(0,1), W ~ N(0, 1/fan_in), seeded) and
+sequence, timed through mla_decode_step (one library call per step); the
+per-stage breakdown and the attention call's roofline come from a second loop
+through the four entry points. Inputs are synthetic (h ~ N(0,1), W ~ N(0, 1/fan_in), seeded) and
 resident in HBM; the cache (302 MB) and weights (298 MB) exceed the 126 MB L2,
 so no flush is needed between steps.
 
@@ -234,32 +236,28 @@ def run_ours(args, rank, world, local_rank):
     seqlens = pos + 1
     stream = torch.cuda.current_stream()
 
-    def step(evs=None):
-        if evs is None:
-            return dec.step(h_new, pos, cache, seqlens)
+    def step_calls(evs):
+        """The step through the four entry points, events between them."""
         evs[0].record(stream)
         M.mla_append_cache(dec.handle, h_new, B, dec.W["W_DKV"], dec.W["W_KR"], dec.tok_seq, pos, cache, B, max_len)
-        n = M.mla_last_launch_count(dec.handle)
         M.mla_absorb_q(dec.handle, h_new, B, dec.W["W_DQ"], dec.W["W_UQ"], dec.W["W_QR"], dec.W["W_UK"], pos,
                        dec.q_abs, dec.ws, dec.ws.numel())
-        n += M.mla_last_launch_count(dec.handle)
         evs[1].record(stream)
         M.mla_decode_attn(dec.handle, dec.q_abs, cache, B, max_len, seqlens, dec.o_lat, dec.lse, dec.ws,
                           dec.ws.numel())
-        n += M.mla_last_launch_count(dec.handle)
         evs[2].record(stream)
         M.mla_out_proj(dec.handle, dec.o_lat, B, dec.W["W_UV"], dec.W["W_O"], dec.u, dec.ws, dec.ws.numel())
-        n += M.mla_last_launch_count(dec.handle)
         evs[3].record(stream)
-        return n
 
     for _ in range(args.warmup):
-        step()
+        dec.step(h_new, pos, cache, seqlens)
+        step_calls([torch.cuda.Event(enable_timing=True) for _ in range(4)])
     torch.cuda.synchronize()
     st, bits = M.mla_get_device_status(dec.handle)
     if st != M.MLA_OK:
         raise RuntimeError(f"device status after warm-up: {st} bits={bits}")
 
+    # ---- the timed region: K steps through mla_decode_step (the product call)
     dist = None
     if world > 1:
         import torch.distributed as dist
@@ -267,24 +265,32 @@ def run_ours(args, rank, world, local_rank):
     torch.cuda.synchronize()
     sampler = ClockSampler(local_rank)
     sampler.start()
-    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(args.steps)]
     launches = 0
     start = torch.cuda.Event(enable_timing=True)
     end = torch.cuda.Event(enable_timing=True)
     start.record(stream)
     for k in range(args.steps):
-        launches += step(evs[k])
+        dec.step(h_new, pos, cache, seqlens)
+        launches += dec.launches
     end.record(stream)
     torch.cuda.synchronize()
     if world > 1:
         dist.barrier()
     clocks = sampler.stop()
     total_ms = start.elapsed_time(end)
+    total_ms = max_over_ranks(total_ms, device)
+
+    # ---- per-stage breakdown (and the attention call's time for the roofline):
+    # the same step through the four entry points, CUDA events between them
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(args.steps)]
+    torch.cuda.synchronize()
+    for k in range(args.steps):
+        step_calls(evs[k])
+    torch.cuda.synchronize()
     attn_ms = [e[1].elapsed_time(e[2]) for e in evs]
     step_ms = [e[0].elapsed_time(e[3]) for e in evs]
     s12_ms = [e[0].elapsed_time(e[1]) for e in evs]
     s45_ms = [e[2].elapsed_time(e[3]) for e in evs]
-    total_ms = max_over_ranks(total_ms, device)
 
     # ---- end to end through the public API: pinned host in, host out, every step
     h_host = torch.empty_like(h_new, device="cpu").pin_memory()
@@ -394,7 +400,7 @@ def run_ours(args, rank, world, local_rank):
         "gpu_launches": launches,
         "clocks": clocks,
         "kernel_source_hash": kh,
-        "step_ms_median": round(statistics.median(step_ms), 4),
+        "four_call_step_ms_median": round(statistics.median(step_ms), 4),
         "step_breakdown_us": {"append_and_absorb": round(1e3 * statistics.median(s12_ms), 1),
                               "attention": round(1e3 * statistics.median(attn_ms), 1),
                               "out_proj": round(1e3 * statistics.median(s45_ms), 1)},

@@ -81,6 +81,8 @@ _c = {
     "mla_decode_attn_noalloc": _sig("mla_decode_attn_noalloc", [_I, _I, _I, _I, _I, _P, _P, _I, _I, _P, _P, _P, _P]),
     "mla_out_proj_workspace_size": _sig("mla_out_proj_workspace_size", [_P, _I, ctypes.POINTER(_S)]),
     "mla_out_proj": _sig("mla_out_proj", [_P, _P, _I, _P, _P, _P, _P, _S, _P]),
+    "mla_decode_step_workspace_size": _sig("mla_decode_step_workspace_size", [_P, _I, _I, ctypes.POINTER(_S)]),
+    "mla_decode_step": _sig("mla_decode_step", [_P, _P, _I] + [_P] * 8 + [_P, _P, _P, _I, _P, _P, _S, _P]),
     "mla_get_device_status": _sig("mla_get_device_status", [_P, _P, ctypes.POINTER(_I)]),
     "mla_set_decode_path": _sig("mla_set_decode_path", [_P, _I]),
     "mla_set_decode_chunks": _sig("mla_set_decode_chunks", [_P, _I]),
@@ -183,6 +185,21 @@ def mla_out_proj(handle, o_lat, batch, W_UV, W_O, u, ws, ws_bytes, stream=None):
                               _stream(stream)), "mla_out_proj")
 
 
+def mla_decode_step_workspace_size(handle, batch, max_len) -> int:
+    n = _S()
+    _check(_c["mla_decode_step_workspace_size"](handle, batch, max_len, ctypes.byref(n)),
+           "mla_decode_step_workspace_size")
+    return n.value
+
+
+def mla_decode_step(handle, x, batch, W_DKV, W_KR, W_DQ, W_UQ, W_QR, W_UK, W_UV, W_O, pos, seqlens, cache,
+                    max_len, u, ws, ws_bytes, stream=None):
+    _check(_c["mla_decode_step"](handle, _ptr(x), batch, _ptr(W_DKV), _ptr(W_KR), _ptr(W_DQ), _ptr(W_UQ),
+                                 _ptr(W_QR), _ptr(W_UK), _ptr(W_UV), _ptr(W_O), _ptr(pos), _ptr(seqlens),
+                                 _ptr(cache), max_len, _ptr(u), _ptr(ws), ws_bytes, _stream(stream)),
+           "mla_decode_step")
+
+
 def mla_get_device_status(handle, stream=None):
     """Returns (status, bits); does not raise on device-side flags."""
     bits = _I()
@@ -253,7 +270,8 @@ class MLADecoder:
         dev = next(iter(self.W.values())).device
         ws = max(mla_absorb_q_workspace_size(self.handle, batch),
                  mla_decode_workspace_size(self.handle, batch, max_len),
-                 mla_out_proj_workspace_size(self.handle, batch))
+                 mla_out_proj_workspace_size(self.handle, batch),
+                 mla_decode_step_workspace_size(self.handle, batch, max_len))
         self.ws = torch.empty(ws, dtype=torch.uint8, device=dev)
         self.q_abs = torch.empty((batch, shape.n_h, shape.D), dtype=self.torch_dtype, device=dev)
         self.o_lat = torch.empty((batch, shape.n_h, shape.d_c), dtype=self.torch_dtype, device=dev)
@@ -281,7 +299,19 @@ class MLADecoder:
     def step(self, h_new, pos, cache, seqlens, stream=None):
         """One decode step for `batch` sequences: h_new [B, d] at positions
         pos [B] (int32, device); cache [B, max_len, D]; seqlens [B] = pos + 1.
-        Returns u [B, d] (the decoder's buffer)."""
+        One library call (mla_decode_step). Returns u [B, d] (the decoder's
+        buffer)."""
+        B = self.batch
+        mla_decode_step(self.handle, h_new, B, self.W["W_DKV"], self.W["W_KR"], self.W["W_DQ"], self.W["W_UQ"],
+                        self.W["W_QR"], self.W["W_UK"], self.W["W_UV"], self.W["W_O"], pos, seqlens, cache,
+                        self.max_len, self.u, self.ws, self.ws.numel(), stream)
+        self.launches = mla_last_launch_count(self.handle)
+        return self.u
+
+    def step_calls(self, h_new, pos, cache, seqlens, stream=None):
+        """The same step through the four entry points (append, absorb,
+        attention, output projection), with q_abs, o_lat and lse kept in the
+        decoder's buffers. Returns u [B, d]."""
         B = self.batch
         n = 0
         mla_append_cache(self.handle, h_new, B, self.W["W_DKV"], self.W["W_KR"], self.tok_seq, pos, cache, B,

@@ -106,7 +106,7 @@ __global__ void __launch_bounds__(NT) gemm_simt_kernel(const GemmArgs a) {
       const float r = j < half ? (v * c - partner * s) : (v * c + partner * s);
       out[gn * a.ldo + seg * a.seg_stride + a.seg_off + j] = from_f32<T>(r);
     } else {  // EPI_APPEND
-      const int sq = a.tok_seq[gn], p = a.tok_pos[gn];
+      const int sq = a.tok_seq ? a.tok_seq[gn] : (int)gn, p = a.tok_pos[gn];
       const bool seq_ok = sq >= 0 && sq < a.cache_batch;
       const bool pos_ok = p >= 0 && p < a.max_len && p < a.max_pos;
       if (!seq_ok || !pos_ok) {

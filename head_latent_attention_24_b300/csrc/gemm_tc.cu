@@ -310,7 +310,7 @@ __global__ void __launch_bounds__(NTHREADS, 2)
           }
           dst = out + gn * ldo + sg * p.seg_stride[seg] + p.seg_off[seg] + j0;
         } else {  // EPI_APPEND
-          const int sq = p.tok_seq[gn], ps = p.tok_pos[gn];
+          const int sq = p.tok_seq ? p.tok_seq[gn] : (int)gn, ps = p.tok_pos[gn];
           const bool seq_ok = sq >= 0 && sq < p.cache_batch;
           const bool pos_ok = ps >= 0 && ps < p.max_len && ps < p.max_pos;
           const int gm = p.col0[seg] + mb;

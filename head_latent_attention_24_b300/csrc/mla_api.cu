@@ -180,16 +180,10 @@ mla_status_t mla_get_device_status(mla_handle_t h, void* stream, int32_t* bits) 
 }
 
 // ------------------------------------------------------------------- S1
-mla_status_t mla_append_cache(mla_handle_t h, const void* x, int32_t n_tokens, const void* W_DKV,
-                              const void* W_KR, const int32_t* tok_seq, const int32_t* tok_pos,
-                              void* cache, int32_t batch, int32_t max_len, void* stream) {
-  if (!h || n_tokens < 0 || batch <= 0 || max_len <= 0) return MLA_ERR_INVALID_ARG;
-  if (n_tokens == 0) { h->last_launches = 0; return MLA_OK; }
-  if (!x || !W_DKV || !W_KR || !tok_seq || !tok_pos || !cache) return MLA_ERR_INVALID_ARG;
-  if (!aligned16(x) || !aligned16(W_DKV) || !aligned16(W_KR) || !aligned16(tok_seq) ||
-      !aligned16(tok_pos) || !aligned16(cache))
-    return MLA_ERR_INVALID_ARG;
-  if (!on_handle_device(h)) return MLA_ERR_INVALID_ARG;
+// S1 after argument checks; tok_seq == nullptr sends token n to sequence n.
+static mla_status_t append_impl(mla_handle_t h, const void* x, int32_t n_tokens, const void* W_DKV, const void* W_KR,
+                         const int32_t* tok_seq, const int32_t* tok_pos, void* cache, int32_t batch,
+                         int32_t max_len, void* stream) {
   const mla_config_t& c = h->cfg;
   if (c.d_r > 64) return MLA_ERR_UNSUPPORTED;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
@@ -212,7 +206,7 @@ mla_status_t mla_append_cache(mla_handle_t h, const void* x, int32_t n_tokens, c
         TcGemm gc = g;
         gc.N = n_tokens - t0 < chunk ? n_tokens - t0 : chunk;
         gc.x = static_cast<const char*>(x) + (size_t)t0 * c.d * esize(h);
-        gc.tok_seq = tok_seq + t0;
+        gc.tok_seq = tok_seq ? tok_seq + t0 : nullptr;
         gc.tok_pos = tok_pos + t0;
         if (launch_gemm_tc(gc, h->num_sms, s) != cudaSuccess) return MLA_ERR_CUDA;
         ++launches;
@@ -243,7 +237,7 @@ mla_status_t mla_append_cache(mla_handle_t h, const void* x, int32_t n_tokens, c
       GemmArgs ac = a;
       ac.N = n_tokens - t0 < chunk ? n_tokens - t0 : chunk;
       ac.X = static_cast<const char*>(x) + (size_t)t0 * c.d * esize(h);
-      ac.tok_seq = tok_seq + t0;
+      ac.tok_seq = tok_seq ? tok_seq + t0 : nullptr;
       ac.tok_pos = tok_pos + t0;
       e = launch_gemm_simt(ac, c.dtype, s);
       if (e != cudaSuccess) return MLA_ERR_CUDA;
@@ -252,6 +246,19 @@ mla_status_t mla_append_cache(mla_handle_t h, const void* x, int32_t n_tokens, c
   }
   h->last_launches = launches;
   return MLA_OK;
+}
+
+mla_status_t mla_append_cache(mla_handle_t h, const void* x, int32_t n_tokens, const void* W_DKV,
+                              const void* W_KR, const int32_t* tok_seq, const int32_t* tok_pos,
+                              void* cache, int32_t batch, int32_t max_len, void* stream) {
+  if (!h || n_tokens < 0 || batch <= 0 || max_len <= 0) return MLA_ERR_INVALID_ARG;
+  if (n_tokens == 0) { h->last_launches = 0; return MLA_OK; }
+  if (!x || !W_DKV || !W_KR || !tok_seq || !tok_pos || !cache) return MLA_ERR_INVALID_ARG;
+  if (!aligned16(x) || !aligned16(W_DKV) || !aligned16(W_KR) || !aligned16(tok_seq) ||
+      !aligned16(tok_pos) || !aligned16(cache))
+    return MLA_ERR_INVALID_ARG;
+  if (!on_handle_device(h)) return MLA_ERR_INVALID_ARG;
+  return append_impl(h, x, n_tokens, W_DKV, W_KR, tok_seq, tok_pos, cache, batch, max_len, stream);
 }
 
 // ------------------------------------------------------------------- S2
@@ -429,6 +436,104 @@ mla_status_t mla_out_proj(mla_handle_t h, const void* o_lat, int32_t batch, cons
   b.status = h->status;
   if (launch_gemm_simt(b, c.dtype, s) != cudaSuccess) return MLA_ERR_CUDA;
   h->last_launches = 2;
+  return MLA_OK;
+}
+
+// ------------------------------------------------------------------- S1..S5
+// Workspace of the whole step: q_abs, o_lat and lse, then one region the
+// stages use in turn (c_Q and q_C; the split plan and partials; o).
+static void step_layout(const mla_handle_s* h, int32_t batch, int32_t max_len, size_t* q_off, size_t* o_off,
+                        size_t* l_off, size_t* r_off, size_t* total) {
+  const mla_config_t& c = h->cfg;
+  size_t off = 0;
+  *q_off = off; off += align_up((size_t)batch * c.n_h * (c.d_c + c.d_r) * esize(h), 256);
+  *o_off = off; off += align_up((size_t)batch * c.n_h * c.d_c * esize(h), 256);
+  *l_off = off; off += align_up((size_t)batch * c.n_h * sizeof(float), 256);
+  *r_off = off;
+  size_t a = 0, d = 0, o = 0;
+  mla_absorb_q_workspace_size(const_cast<mla_handle_t>(h), batch, &a);
+  mla_decode_workspace_size(const_cast<mla_handle_t>(h), batch, max_len, &d);
+  mla_out_proj_workspace_size(const_cast<mla_handle_t>(h), batch, &o);
+  size_t r = a > d ? a : d;
+  r = r > o ? r : o;
+  *total = off + r;
+}
+
+mla_status_t mla_decode_step_workspace_size(mla_handle_t h, int32_t batch, int32_t max_len, size_t* bytes) {
+  if (!h || !bytes || batch <= 0 || max_len <= 0) return MLA_ERR_INVALID_ARG;
+  size_t q, o, l, r;
+  step_layout(h, batch, max_len, &q, &o, &l, &r, bytes);
+  return MLA_OK;
+}
+
+mla_status_t mla_decode_step(mla_handle_t h, const void* x, int32_t batch, const void* W_DKV, const void* W_KR,
+                             const void* W_DQ, const void* W_UQ, const void* W_QR, const void* W_UK,
+                             const void* W_UV, const void* W_O, const int32_t* pos, const int32_t* seqlens,
+                             void* cache, int32_t max_len, void* u, void* ws, size_t ws_bytes, void* stream) {
+  if (!h || batch <= 0 || max_len <= 0) return MLA_ERR_INVALID_ARG;
+  if (!x || !W_DKV || !W_KR || !W_DQ || !W_UQ || !W_QR || !W_UK || !W_UV || !W_O || !pos || !seqlens || !cache ||
+      !u)
+    return MLA_ERR_INVALID_ARG;
+  if (!aligned16(x) || !aligned16(W_DKV) || !aligned16(W_KR) || !aligned16(W_DQ) || !aligned16(W_UQ) ||
+      !aligned16(W_QR) || !aligned16(W_UK) || !aligned16(W_UV) || !aligned16(W_O) || !aligned16(pos) ||
+      !aligned16(seqlens) || !aligned16(cache) || !aligned16(u) || (ws && !aligned16(ws)))
+    return MLA_ERR_INVALID_ARG;
+  if ((long long)batch * max_len >= (1LL << 31)) return MLA_ERR_INVALID_ARG;
+  size_t q_off, o_off, l_off, r_off, need;
+  step_layout(h, batch, max_len, &q_off, &o_off, &l_off, &r_off, &need);
+  if (!ws || ws_bytes < need) return MLA_ERR_WORKSPACE;
+  if (!on_handle_device(h)) return MLA_ERR_INVALID_ARG;
+  const mla_config_t& c = h->cfg;
+  if (c.d_r > 64 || 64 % c.d_r != 0) return MLA_ERR_UNSUPPORTED;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  char* base = static_cast<char*>(ws);
+  void* q_abs = base + q_off;
+  void* o_lat = base + o_off;
+  float* lse = reinterpret_cast<float*>(base + l_off);
+  char* region = base + r_off;
+  const size_t region_bytes = ws_bytes - r_off;
+  const int D = c.d_c + c.d_r;
+  int launches = 0;
+
+  // S1 and c_Q = W_DQ x read the same x: one launch of three weight
+  // segments when the tensor-core kernel takes them all (and the rest of S2).
+  char* c_q = region;
+  char* q_c = c_q + align_up((size_t)batch * c.d_cq * esize(h), 256);
+  TcGemm f = tc_base(h);
+  tc_seg(f, 0, W_DKV, c.d_c, 0, EPI_APPEND, cache, 0);
+  tc_seg(f, 1, W_KR, c.d_r, c.d_c, EPI_APPEND, cache, 0);
+  tc_seg(f, 2, W_DQ, c.d_cq, 0, EPI_STORE, c_q, c.d_cq);
+  f.ldw = c.d; f.x = x; f.ldx = c.d; f.N = batch; f.K = c.d;
+  f.tok_seq = nullptr; f.tok_pos = pos; f.cache_batch = batch; f.max_len = max_len; f.d_c = c.d_c; f.row_width = D;
+  TcGemm g2 = tc_base(h);
+  tc_seg(g2, 0, W_UQ, c.n_h * c.d_h, 0, EPI_STORE, q_c, (long long)c.n_h * c.d_h);
+  tc_seg(g2, 1, W_QR, c.n_h * c.d_r, 0, EPI_ROPE_SEGS, q_abs, (long long)c.n_h * D, 0, D, c.d_c);
+  g2.ldw = c.d_cq; g2.x = c_q; g2.ldx = c.d_cq; g2.N = batch; g2.K = c.d_cq; g2.pos = pos;
+  TcGemm g4 = tc_base(h);
+  tc_seg(g4, 0, W_UK, c.d_c, 0, EPI_STORE, q_abs, (long long)c.n_h * D, D);
+  g4.w_transposed = 1; g4.ldw = c.d_c; g4.bw = (long long)c.d_h * c.d_c;
+  g4.x = q_c; g4.ldx = (long long)c.n_h * c.d_h; g4.bx = c.d_h; g4.N = batch; g4.K = c.d_h; g4.Z = c.n_h;
+  mla_status_t st;
+  if (batch <= 65535 * 256 && use_tc_proj(h, f) && use_tc_proj(h, g2) && use_tc_proj(h, g4)) {
+    if (launch_gemm_tc(f, h->num_sms, s) != cudaSuccess) return MLA_ERR_CUDA;
+    if (launch_gemm_tc(g2, h->num_sms, s) != cudaSuccess) return MLA_ERR_CUDA;
+    if (launch_gemm_tc(g4, h->num_sms, s) != cudaSuccess) return MLA_ERR_CUDA;
+    launches += 3;
+  } else {
+    st = append_impl(h, x, batch, W_DKV, W_KR, nullptr, pos, cache, batch, max_len, stream);
+    if (st != MLA_OK) return st;
+    launches += h->last_launches;
+    st = mla_absorb_q(h, x, batch, W_DQ, W_UQ, W_QR, W_UK, pos, q_abs, region, region_bytes, stream);
+    if (st != MLA_OK) return st;
+    launches += h->last_launches;
+  }
+  st = mla_decode_attn(h, q_abs, cache, batch, max_len, seqlens, o_lat, lse, region, region_bytes, stream);
+  if (st != MLA_OK) return st;
+  launches += h->last_launches;
+  st = mla_out_proj(h, o_lat, batch, W_UV, W_O, u, region, region_bytes, stream);
+  if (st != MLA_OK) return st;
+  launches += h->last_launches;
+  h->last_launches = launches;
   return MLA_OK;
 }
 

@@ -198,6 +198,23 @@ MLA_API mla_status_t mla_out_proj(mla_handle_t handle, const void* o_lat, int32_
                           const void* W_UV, const void* W_O, void* u,
                           void* ws, size_t ws_bytes, void* stream);
 
+/* S1..S5 in one call ([MLA] §3-§7; [MiniMind] §9-§12): the new token of
+   sequence b (x[b], position pos[b]) is written to cache[b, pos[b], :], the
+   absorbed queries are formed, attention covers seqlens[b] rows of sequence b
+   (pos[b] + 1 for an ordinary step), and u [batch, d] is written. Weights as
+   in the four calls above. The workspace (mla_decode_step_workspace_size)
+   holds q_abs, o_lat, lse and the stages' scratch; the call launches the same
+   kernels as the four calls in sequence, except that S1 and c_Q = W_DQ x share
+   one launch when the tensor-core projection kernel takes both. Errors as for
+   the four calls; nothing is launched if an argument is rejected. */
+MLA_API mla_status_t mla_decode_step_workspace_size(mla_handle_t handle, int32_t batch, int32_t max_len,
+                                                    size_t* bytes);
+MLA_API mla_status_t mla_decode_step(mla_handle_t handle, const void* x, int32_t batch, const void* W_DKV,
+                                     const void* W_KR, const void* W_DQ, const void* W_UQ, const void* W_QR,
+                                     const void* W_UK, const void* W_UV, const void* W_O, const int32_t* pos,
+                                     const int32_t* seqlens, void* cache, int32_t max_len, void* u, void* ws,
+                                     size_t ws_bytes, void* stream);
+
 /* Synchronise `stream`, return the status-word bits accumulated since the last
    call in *bits, and clear them. Returns MLA_ERR_DEVICE if any bit other than
    MLA_DEV_TIMEOUT was set, MLA_ERR_TIMEOUT if that one was, else MLA_OK. */

@@ -400,7 +400,9 @@ def end_to_end(shp, ctx_lens):
     pos = np.concatenate([np.arange(int(n)) for n in ctx_lens])
     if len(seq):
         dec.append(dev(np.concatenate(h_ctx), shp), dev_i32(seq), dev_i32(pos), cache)
-    u = dec.step(dev(h_new, shp), dev_i32(ctx_lens), cache, dev_i32(np.asarray(ctx_lens) + 1))
+    # the four entry points, so that o_lat and lse stay in the decoder's buffers
+    # (mla_decode_step is checked against this sequence of calls elsewhere)
+    u = dec.step_calls(dev(h_new, shp), dev_i32(ctx_lens), cache, dev_i32(np.asarray(ctx_lens) + 1))
     st, bits = M.mla_get_device_status(dec.handle)
     assert st == M.MLA_OK and bits == 0
     ref_u = O.decode_materialised(h_ctx, h_new, W, shp.n_h, shp.d_h, shp.d_r, shp.rope_base)
@@ -473,6 +475,33 @@ def test_captured_step_matches_eager():
     torch.cuda.synchronize()
     assert torch.equal(u_g, u_e)
     assert torch.equal(cache_g, cache_e)
+    st, bits = M.mla_get_device_status(dec.handle)
+    assert st == M.MLA_OK and bits == 0
+    dec.close()
+
+
+@pytest.mark.gpu
+@pytest.mark.parametrize("name", ["minimind", "v2"])
+def test_step_call_matches_four_calls(name):
+    """mla_decode_step (S1 and c_Q in one launch where the tensor-core kernel
+    takes both; MiniMind's W_UK^T falls back) writes the same cache rows and u
+    as the four entry points called in turn."""
+    shp = S.workload(name)
+    B, L = 6, 400
+    W = S.draw_weights(shp)
+    dec = decoder(shp, make_weights_dev(shp, W), B, L, max_pos=L)
+    rng = np.random.default_rng(12)
+    cache0 = dev(rng.standard_normal((B, L, shp.D)), shp)
+    h = dev(S.draw_context_h(shp, 2, B), shp)
+    pos = dev_i32(rng.integers(0, L - 1, size=B))
+    seqlens = dev_i32(host(pos) + 1)
+    cache_a = cache0.clone()
+    u_a = dec.step_calls(h, pos, cache_a, seqlens).clone()
+    cache_b = cache0.clone()
+    u_b = dec.step(h, pos, cache_b, seqlens).clone()
+    torch.cuda.synchronize()
+    assert torch.equal(cache_b, cache_a)
+    assert torch.equal(u_b, u_a)
     st, bits = M.mla_get_device_status(dec.handle)
     assert st == M.MLA_OK and bits == 0
     dec.close()
