@@ -67,3 +67,15 @@ def test_null_handle_is_rejected():
                      (m._c["mla_append_cache"], (None, None, 1, None, None, None, None, None, 1, 1, None)),
                      (m._c["mla_out_proj"], (None, None, 1, None, None, None, None, 0, None))):
         assert fn(*args) == m.MLA_ERR_INVALID_ARG
+    n = ctypes.c_size_t(0)
+    assert m._c["mla_decode_step_workspace_size"](None, 1, 1, ctypes.byref(n)) == m.MLA_ERR_INVALID_ARG
+    assert m._c["mla_decode_step"](None, None, 1, *([None] * 8), None, None, None, 1, None, None, 0,
+                                   None) == m.MLA_ERR_INVALID_ARG
+    assert m._c["mla_set_decode_chunks"](None, 4) == m.MLA_ERR_INVALID_ARG
+
+
+def test_binding_has_every_declared_function():
+    """The Python binding carries each C entry point under its own name."""
+    import head_latent_attention_24_b300 as m
+    missing = [n for n in declared_functions() if n not in m._c]
+    assert not missing, missing
