@@ -50,6 +50,21 @@ int resolve_decode_path(const mla_handle_s* h) {
   return tc_ok ? MLA_DECODE_TCGEN05 : MLA_DECODE_SIMT;
 }
 
+// The two tensor-core GEMMs of S4/S5: o_i = W_UV_i o_lat_i batched over the
+// heads into `o`, then u = W_O o.
+void out_proj_gemms(const mla_handle_s* h, const void* o_lat, int batch, const void* W_UV, const void* W_O,
+                    void* u, void* o, TcGemm& g1, TcGemm& g2) {
+  const mla_config_t& c = h->cfg;
+  g1 = tc_base(h);
+  tc_seg(g1, 0, W_UV, c.d_h, 0, EPI_STORE, o, (long long)c.n_h * c.d_h, c.d_h);
+  g1.ldw = c.d_c; g1.bw = (long long)c.d_h * c.d_c;
+  g1.x = o_lat; g1.ldx = (long long)c.n_h * c.d_c; g1.bx = c.d_c; g1.N = batch; g1.K = c.d_c; g1.Z = c.n_h;
+  g2 = tc_base(h);
+  tc_seg(g2, 0, W_O, c.d, 0, EPI_STORE, u, c.d);
+  g2.ldw = (long long)c.n_h * c.d_h; g2.x = o; g2.ldx = (long long)c.n_h * c.d_h; g2.N = batch;
+  g2.K = c.n_h * c.d_h;
+}
+
 }  // namespace
 
 extern "C" {
@@ -405,14 +420,8 @@ mla_status_t mla_out_proj(mla_handle_t h, const void* o_lat, int32_t batch, cons
   const mla_config_t& c = h->cfg;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   {
-    TcGemm g1 = tc_base(h);  // o_i = W_UV_i o_lat_i
-    tc_seg(g1, 0, W_UV, c.d_h, 0, EPI_STORE, ws, (long long)c.n_h * c.d_h, c.d_h);
-    g1.ldw = c.d_c; g1.bw = (long long)c.d_h * c.d_c;
-    g1.x = o_lat; g1.ldx = (long long)c.n_h * c.d_c; g1.bx = c.d_c; g1.N = batch; g1.K = c.d_c; g1.Z = c.n_h;
-    TcGemm g2 = tc_base(h);  // u = W_O o
-    tc_seg(g2, 0, W_O, c.d, 0, EPI_STORE, u, c.d);
-    g2.ldw = (long long)c.n_h * c.d_h; g2.x = ws; g2.ldx = (long long)c.n_h * c.d_h; g2.N = batch;
-    g2.K = c.n_h * c.d_h;
+    TcGemm g1, g2;
+    out_proj_gemms(h, o_lat, batch, W_UV, W_O, u, ws, g1, g2);
     const bool tc = use_tc_proj(h, g1) && use_tc_proj(h, g2);
     if (h->proj_path == MLA_PROJ_TCGEN05 && !tc) return MLA_ERR_UNSUPPORTED;
     if (tc) {
@@ -513,8 +522,17 @@ mla_status_t mla_decode_step(mla_handle_t h, const void* x, int32_t batch, const
   tc_seg(g4, 0, W_UK, c.d_c, 0, EPI_STORE, q_abs, (long long)c.n_h * D, D);
   g4.w_transposed = 1; g4.ldw = c.d_c; g4.bw = (long long)c.d_h * c.d_c;
   g4.x = q_c; g4.ldx = (long long)c.n_h * c.d_h; g4.bx = c.d_h; g4.N = batch; g4.K = c.d_h; g4.Z = c.n_h;
+  // Every rejection happens here, before the first launch: the decode kernel
+  // family, and a forced tensor-core projection path the shapes do not take.
+  const int dpath = resolve_decode_path(h);
+  if (dpath < 0 || (dpath == MLA_DECODE_SIMT && c.d_c > 512)) return MLA_ERR_UNSUPPORTED;
+  const bool tc_front = batch <= 65535 * 256 && use_tc_proj(h, f) && use_tc_proj(h, g2) && use_tc_proj(h, g4);
+  TcGemm o1, o2;
+  out_proj_gemms(h, o_lat, batch, W_UV, W_O, u, region, o1, o2);
+  if (h->proj_path == MLA_PROJ_TCGEN05 && !(tc_front && use_tc_proj(h, o1) && use_tc_proj(h, o2)))
+    return MLA_ERR_UNSUPPORTED;
   mla_status_t st;
-  if (batch <= 65535 * 256 && use_tc_proj(h, f) && use_tc_proj(h, g2) && use_tc_proj(h, g4)) {
+  if (tc_front) {
     if (launch_gemm_tc(f, h->num_sms, s) != cudaSuccess) return MLA_ERR_CUDA;
     if (launch_gemm_tc(g2, h->num_sms, s) != cudaSuccess) return MLA_ERR_CUDA;
     if (launch_gemm_tc(g4, h->num_sms, s) != cudaSuccess) return MLA_ERR_CUDA;
