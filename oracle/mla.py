@@ -18,13 +18,15 @@ Conventions: weights are stored row-major [out, in] as nn.Linear keeps them
 [i*d_h, (i+1)*d_h) of W_UQ, W_UK and W_UV, rows [i*d_r, (i+1)*d_r) of W_QR and
 columns [i*d_h, (i+1)*d_h) of W_O ([MLA] §4, the per-head form of u_t).
 
-Readings where the pages leave a step open (each also listed in the design
-notes): RoPE is the rotate-half form with inverse frequencies
+Readings where the pages leave a step open: RoPE is the rotate-half form with inverse frequencies
 base^(-2j/d_r), j < d_r/2 — the pages never define RoPE, and [MiniMind] §6/§9
 apply it through ``apply_rotary_pos_emb(q, k, cos, sin)`` on the rope slice
 only (§12 sizes the table by the rope width). The decode query attends to every
-cached row including its own ([MiniMind] §12, causal mask with cache). No
-RMSNorm is applied to the latent ([MLA] has none).
+cached row including its own ([MiniMind] §12, causal mask with cache). The
+latent is cached as projected ([MLA] has no norm); the variant that applies
+[MiniMind] §9's kv_norm (an RMSNorm over the kv_lora_rank latent before it is
+cached) takes its weight and epsilon as arguments (the pages give neither
+value).
 
 Pins: every function here is checked in tests/test_oracle_pins.py against
 something other than itself (closed forms, the pages' printed numbers, brute
@@ -81,16 +83,29 @@ def rope(x, pos, base: float) -> np.ndarray:
 # --------------------------------------------------------------------------
 # Step S1: what one token writes into the latent cache
 # --------------------------------------------------------------------------
-def cache_rows(h, W_DKV, W_KR, pos, base: float) -> np.ndarray:
+def rms_norm(x, weight, eps: float) -> np.ndarray:
+    """RMSNorm over the last axis: x / sqrt(mean(x^2) + eps) * weight
+    ([MiniMind] §9: ``self.kv_norm = RMSNorm(self.kv_lora_rank, eps=...)``,
+    applied as ``kv_latent = self.kv_norm(kv_latent)``)."""
+    x = _f64(x)
+    ms = np.mean(x * x, axis=-1, keepdims=True)
+    return x / np.sqrt(ms + F64(eps)) * _f64(weight)
+
+
+def cache_rows(h, W_DKV, W_KR, pos, base: float, kv_norm_weight=None, kv_norm_eps: float = 1e-5) -> np.ndarray:
     """Cache rows [c_KV ‖ k_R] for tokens h [N, d] at positions pos [N].
 
     c_KV = W_DKV h           ([MLA] §3 down-projection; [Latent] "MLA：latent 作为可缓存的 KV 表示")
     k_R  = RoPE(W_KR h)      ([MLA] §6, shared by all heads, computed from h directly)
     Row layout: latent first, then the rope key ([MiniMind] §9: kv_down_proj
     output split as [kv_lora_rank, qk_rope_head_dim], cache = (kv_latent, k_rope)).
+    With kv_norm_weight given, the latent is RMS-normalised before it is cached
+    ([MiniMind] §9, the kv_norm variant); the rope key is not.
     """
     h = _f64(h)
     c_kv = h @ _f64(W_DKV).T
+    if kv_norm_weight is not None:
+        c_kv = rms_norm(c_kv, kv_norm_weight, kv_norm_eps)
     k_r = rope(h @ _f64(W_KR).T, pos, base)
     return np.concatenate([c_kv, k_r], axis=-1)
 
@@ -166,9 +181,11 @@ def output_projection(o_lat, W_UV, W_O, n_h: int, d_h: int, return_o: bool = Fal
 # --------------------------------------------------------------------------
 # The whole step, two ways
 # --------------------------------------------------------------------------
-def decode_absorbed(h_ctx_list, h_new, W, n_h, d_h, d_r, base, pos=None):
+def decode_absorbed(h_ctx_list, h_new, W, n_h, d_h, d_r, base, pos=None, kv_norm_weight=None,
+                    kv_norm_eps: float = 1e-5):
     """The four steps chained (append every token, absorbed query, latent
-    attention over rows 0..pos, output projection). Returns (u, o_lat, lse, q_abs, rows)."""
+    attention over rows 0..pos, output projection). Returns (u, o_lat, lse, q_abs, rows).
+    kv_norm_weight: the [MiniMind] §9 variant that RMS-normalises the cached latent."""
     h_new = _f64(h_new)
     B = h_new.shape[0]
     d_c = W["W_DKV"].shape[0]
@@ -182,14 +199,15 @@ def decode_absorbed(h_ctx_list, h_new, W, n_h, d_h, d_r, base, pos=None):
     for b in range(B):
         L = int(pos[b])
         toks = np.concatenate([_f64(h_ctx_list[b])[:L], h_new[b:b + 1]], axis=0)
-        rows = cache_rows(toks, W["W_DKV"], W["W_KR"], np.arange(L + 1), base)
+        rows = cache_rows(toks, W["W_DKV"], W["W_KR"], np.arange(L + 1), base, kv_norm_weight, kv_norm_eps)
         rows_all.append(rows)
         o_lat[b], lse[b] = latent_attention(q_abs[b], rows, d_c, scale)
     u = output_projection(o_lat, W["W_UV"], W["W_O"], n_h, d_h)
     return u, o_lat, lse, q_abs, rows_all
 
 
-def decode_materialised(h_ctx_list, h_new, W, n_h, d_h, d_r, base, pos=None, return_parts=False):
+def decode_materialised(h_ctx_list, h_new, W, n_h, d_h, d_r, base, pos=None, return_parts=False,
+                        kv_norm_weight=None, kv_norm_eps: float = 1e-5):
     """The decode step as plain multi-head attention over materialised K and V.
 
     For every cached token (positions 0..pos-1) and the new token (position pos):
@@ -200,6 +218,8 @@ def decode_materialised(h_ctx_list, h_new, W, n_h, d_h, d_r, base, pos=None, ret
     a = softmax(q^T k / sqrt(d_h + d_r)) over all rows 0..pos   ([MLA] §7; [MiniMind] §12)
     o_i = sum_t a_t v_C,t ; u = W_O [o_1; ...; o_nh]            ([MLA] §7)
     Nothing is absorbed here: this is the definition the absorbed path must reach.
+    With kv_norm_weight, c_KV is RMS-normalised before K and V are expanded from it
+    ([MiniMind] §9: kv_latent = kv_norm(kv_latent), then kv_up_proj).
     Returns u [B, d] (and per-sequence o [B, n_h*d_h], lse [B, n_h] if asked).
     """
     h_new = _f64(h_new)
@@ -216,6 +236,8 @@ def decode_materialised(h_ctx_list, h_new, W, n_h, d_h, d_r, base, pos=None, ret
         L = int(pos[b])
         toks = np.concatenate([_f64(h_ctx_list[b])[:L], h_new[b:b + 1]], axis=0)   # [L+1, d]
         c_kv = toks @ W["W_DKV"].T                                                     # [L+1, d_c]
+        if kv_norm_weight is not None:
+            c_kv = rms_norm(c_kv, kv_norm_weight, kv_norm_eps)
         k_r = rope(toks @ W["W_KR"].T, np.arange(L + 1), base)                         # [L+1, d_r]
         # k_C = W_UK c_KV and v_C = W_UV c_KV for every row, all heads stacked ([MLA] §3)
         k_c = (c_kv @ W["W_UK"].T).reshape(L + 1, n_h, d_h).transpose(1, 0, 2)        # [n_h, L+1, d_h]

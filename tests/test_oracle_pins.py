@@ -481,3 +481,100 @@ def test_planted_attention_mistakes_are_caught(mutant):
 
 def test_planted_scale_mistake_is_caught():
     assert not check_materialised_vs_brute(_materialised_scale)
+
+
+# ---------------------------------------------------------------------------
+# pins: the kv_norm variant of S1 (MiniMind page §9: RMSNorm on the cached latent)
+# ---------------------------------------------------------------------------
+def check_rms_norm(fn):
+    rng = np.random.default_rng(21)
+    x = rng.standard_normal((6, 40)) * rng.uniform(0.1, 30.0, size=(6, 1))
+    ones = np.ones(40)
+    y = fn(x, ones, 0.0)
+    ok = np.allclose(np.mean(y * y, axis=-1), 1.0, atol=1e-12)               # unit RMS
+    ok &= np.allclose(np.abs(np.sum(y * x, -1)), np.linalg.norm(y, axis=-1) * np.linalg.norm(x, axis=-1),
+                      rtol=1e-12)                                              # parallel to x
+    ok &= bool(np.all(np.sum(y * x, -1) > 0))                                 # same direction
+    ok &= np.allclose(fn(7.5 * x, ones, 0.0), y, atol=1e-12)                  # scale invariant
+    w = rng.standard_normal(40)
+    ok &= np.allclose(fn(x, w, 0.0), y * w, atol=1e-12)                       # weight is elementwise
+    ok &= bool(np.all(fn(np.zeros((2, 40)), ones, 1e-5) == 0.0))              # zero row stays zero
+    return bool(ok)
+
+
+def test_rms_norm_pins():
+    assert check_rms_norm(O.rms_norm)
+
+
+def test_rms_norm_matches_library_routine():
+    torch = pytest.importorskip("torch")
+    rng = np.random.default_rng(22)
+    x, w = rng.standard_normal((5, 128)), rng.standard_normal(128)
+    for eps in (1e-5, 1e-2):
+        ref = torch.nn.functional.rms_norm(torch.from_numpy(x), (128,), torch.from_numpy(w), eps).numpy()
+        assert np.allclose(O.rms_norm(x, w, eps), ref, rtol=1e-12, atol=1e-14)
+
+
+def check_cache_rows_kv_norm(cache_rows):
+    rng = np.random.default_rng(23)
+    d, d_c, d_r = 32, 16, 8
+    h = rng.standard_normal((9, d))
+    Wd, Wr = rng.standard_normal((d_c, d)), rng.standard_normal((d_r, d))
+    pos = np.arange(9) * 5
+    plain = cache_rows(h, Wd, Wr, pos, 10000.0)
+    normed = cache_rows(h, Wd, Wr, pos, 10000.0, np.ones(d_c), 0.0)
+    lat, lat0 = normed[:, :d_c], plain[:, :d_c]
+    ok = np.allclose(np.mean(lat * lat, -1), 1.0, atol=1e-12)
+    ok &= np.allclose(lat * np.sqrt(np.mean(lat0 * lat0, -1, keepdims=True)), lat0, atol=1e-12)
+    ok &= np.array_equal(normed[:, d_c:], plain[:, d_c:])                    # the rope key is not normalised
+    return bool(ok)
+
+
+def test_cache_rows_kv_norm_pins():
+    assert check_cache_rows_kv_norm(O.cache_rows)
+
+
+def test_kv_norm_absorbed_equals_materialised():
+    # With the latent normalised before caching, the absorbed chain (latent
+    # cache, absorbed query, value deferral) still equals the materialised
+    # definition (K and V expanded from the normalised latent).
+    shp = S.workload("tiny")
+    W = S.draw_weights(shp)
+    rng = np.random.default_rng(24)
+    g = rng.uniform(0.5, 1.5, size=shp.d_c)
+    h_ctx = [S.draw_context_h(shp, b, n) for b, n in enumerate([40, 17])]
+    h_new = S.draw_new_tokens(shp, 2)
+    u_m = O.decode_materialised(h_ctx, h_new, W, shp.n_h, shp.d_h, shp.d_r, shp.rope_base, kv_norm_weight=g,
+                                kv_norm_eps=1e-6)
+    u_a = O.decode_absorbed(h_ctx, h_new, W, shp.n_h, shp.d_h, shp.d_r, shp.rope_base, kv_norm_weight=g,
+                            kv_norm_eps=1e-6)[0]
+    u_plain = O.decode_materialised(h_ctx, h_new, W, shp.n_h, shp.d_h, shp.d_r, shp.rope_base)
+    assert np.allclose(u_a, u_m, rtol=1e-10, atol=1e-12)
+    assert not np.allclose(u_m, u_plain, rtol=1e-3)                           # the norm changes the step
+
+
+def _rms_norm_sum_not_mean(x, weight, eps):
+    x = np.asarray(x, float)
+    return x / np.sqrt(np.sum(x * x, -1, keepdims=True) + eps) * weight
+
+
+def _rms_norm_eps_outside(x, weight, eps):
+    x = np.asarray(x, float)
+    return x / (np.sqrt(np.mean(x * x, -1, keepdims=True)) + 1e-3 + eps) * weight
+
+
+def _cache_rows_norm_whole_row(h, W_DKV, W_KR, pos, base, kv_norm_weight=None, kv_norm_eps=1e-5):
+    r = O.cache_rows(h, W_DKV, W_KR, pos, base)
+    if kv_norm_weight is None:
+        return r
+    w = np.concatenate([kv_norm_weight, np.ones(r.shape[1] - len(kv_norm_weight))])
+    return O.rms_norm(r, w, kv_norm_eps)
+
+
+@pytest.mark.parametrize("mutant", [_rms_norm_sum_not_mean, _rms_norm_eps_outside])
+def test_planted_rms_norm_mistakes_are_caught(mutant):
+    assert not check_rms_norm(mutant)
+
+
+def test_planted_kv_norm_row_mistake_is_caught():
+    assert not check_cache_rows_kv_norm(_cache_rows_norm_whole_row)
