@@ -51,7 +51,7 @@ def kernel_source_hash() -> str:
     traffic figure was measured on, and the headers it includes)."""
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "head_latent_attention_24_b300", "csrc")
-    for n in ("decode_pair.cu", "decode_tc.cuh", "tc_ptx.cuh", "tmap.cuh", "internal.cuh"):
+    for n in ("decode_pair.cu", "decode_pair.cuh", "tc_ptx.cuh", "tmap.cuh", "internal.cuh"):
         with open(os.path.join(csrc, n), "rb") as f:
             h.update(n.encode() + f.read())
     return h.hexdigest()[:16]
@@ -78,6 +78,18 @@ class ClockSampler:
 
     def __init__(self, gpu_index: int):
         self.gpu = gpu_index
+        self.ident = None
+        try:
+            import torch
+            props = torch.cuda.get_device_properties(gpu_index)
+            uuid = getattr(props, "uuid", None)
+            if uuid is not None:
+                self.ident = ("uuid", "GPU-" + str(uuid))
+            elif hasattr(props, "pci_bus_id"):
+                self.ident = ("pci", "%08x:%02x:%02x.0" % (getattr(props, "pci_domain_id", 0), props.pci_bus_id,
+                                                          getattr(props, "pci_device_id", 0)))
+        except Exception:  # noqa: BLE001
+            self.ident = None
         self.samples = []
         self.stop_flag = threading.Event()
         self.t = None
@@ -89,9 +101,17 @@ class ClockSampler:
             nv = ctypes.CDLL("libnvidia-ml.so.1")
             if nv.nvmlInit_v2() != 0:
                 raise RuntimeError("nvmlInit failed")
+            # NVML numbers GPUs without regard to CUDA_VISIBLE_DEVICES: find
+            # this process's device by its UUID (or PCI bus id) instead.
             h = ctypes.c_void_p()
-            if nv.nvmlDeviceGetHandleByIndex_v2(ctypes.c_uint(self.gpu), ctypes.byref(h)) != 0:
-                raise RuntimeError("nvmlDeviceGetHandleByIndex failed")
+            if self.ident and self.ident[0] == "uuid":
+                rc = nv.nvmlDeviceGetHandleByUUID(self.ident[1].encode(), ctypes.byref(h))
+            elif self.ident and self.ident[0] == "pci":
+                rc = nv.nvmlDeviceGetHandleByPciBusId_v2(self.ident[1].encode(), ctypes.byref(h))
+            else:
+                raise RuntimeError("no UUID or PCI bus id for the CUDA device")
+            if rc != 0:
+                raise RuntimeError(f"NVML handle lookup for {self.ident} failed ({rc})")
             clk, mx, reasons = ctypes.c_uint(), ctypes.c_uint(), ctypes.c_ulonglong()
             NVML_CLOCK_SM = 1
             if nv.nvmlDeviceGetMaxClockInfo(h, NVML_CLOCK_SM, ctypes.byref(mx)) == 0:
@@ -126,7 +146,104 @@ class ClockSampler:
                 if r & bit:
                     reasons.add(name)
         return {"sm_mhz": statistics.median(sm), "sm_max_mhz": getattr(self, "max_mhz", None),
-                "samples": len(sm), "sm_mhz_min": min(sm), "reasons": sorted(reasons)}
+                "samples": len(sm), "sm_mhz_min": min(sm), "reasons": sorted(reasons),
+                "device": self.ident[1] if self.ident else None}
+
+
+def roofline_of(nbytes: float, flops: float, seconds: float, peaks: dict) -> dict:
+    """Roofline of one call: the slower of its bytes at the measured HBM copy
+    bandwidth and its FLOPs at the measured burst bf16 rate (the call is timed
+    on its own), with the achieved rate in that bound's unit."""
+    hbm_t = nbytes / (peaks["hbm_gbs"] * 1e9)
+    tc_t = flops / (peaks["bf16_tflops"] * 1e12)
+    if hbm_t >= tc_t:
+        out = {"bound": "hbm", "achieved": round(nbytes / seconds / 1e9, 1), "peak": peaks["hbm_gbs"], "unit": "GB/s"}
+    else:
+        out = {"bound": "tensor", "achieved": round(flops / seconds / 1e12, 1), "peak": peaks["bf16_tflops"],
+               "unit": "TFLOP/s"}
+    out["frac"] = round(max(hbm_t, tc_t) / seconds, 4)
+    out["roofline_us"] = round(max(hbm_t, tc_t) * 1e6, 2)
+    sus = peaks.get("bf16_tflops_sustained")
+    if sus:
+        out["frac_vs_sustained_tensor_peak"] = round(max(hbm_t, flops / (sus * 1e12)) / seconds, 4)
+    return out
+
+
+def plan_balance(seqlens, chunks: int, granule: int):
+    """Rows per chunk of the equal-row split plan (the same rule the library's
+    plan kernel applies): max over mean of the busy chunks."""
+    total = int(np.sum(seqlens))
+    cl = -(-total // chunks)
+    cl = max(granule, -(-cl // granule) * granule)
+    rows = [min(cl, total - c * cl) for c in range(chunks) if c * cl < total]
+    return round(max(rows) / (sum(rows) / len(rows)), 4), len(rows)
+
+
+def attention_workloads(device, peaks, iters: int = 20):
+    """mla_decode_attn alone on the other decode workloads (random caches of
+    the workload's shape; CUDA events, median of `iters` calls)."""
+    import torch
+    import head_latent_attention_24_b300 as M
+    import mla_synth as S
+    out = {}
+    for name in ("minimind", "v2_ragged", "v2_long"):
+        shp = S.workload(name)
+        seqlens = (S.draw_context_lengths(shp) + 1).astype(np.int32)
+        B, max_len = len(seqlens), int(seqlens.max())
+        g = torch.Generator(device=device)
+        g.manual_seed(shp.seed)
+        cache = torch.randn((B, max_len, shp.D), generator=g, device=device, dtype=torch.bfloat16)
+        q = torch.randn((B, shp.n_h, shp.D), generator=g, device=device, dtype=torch.bfloat16)
+        q[..., :shp.d_c] *= (shp.d_h / shp.d_c) ** 0.5
+        h = M.mla_create(shp.d, shp.n_h, shp.d_h, shp.d_c, shp.d_r, shp.d_cq, M.MLA_BF16, max_len)
+        try:
+            ws = torch.empty(M.mla_decode_workspace_size(h, B, max_len), dtype=torch.uint8, device=device)
+            o = torch.empty((B, shp.n_h, shp.d_c), dtype=torch.bfloat16, device=device)
+            lse = torch.empty((B, shp.n_h), dtype=torch.float32, device=device)
+            sl = torch.as_tensor(seqlens).to(device)
+            flush = torch.empty(256 << 20, dtype=torch.uint8, device=device) if B * max_len * shp.D * 2 < (256 << 20) \
+                else None
+            for _ in range(3):
+                M.mla_decode_attn(h, q, cache, B, max_len, sl, o, lse, ws, ws.numel())
+            evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(iters)]
+            for e0, e1 in evs:
+                if flush is not None:
+                    flush.fill_(1)   # the cache is smaller than two L2s: start each call cold
+                e0.record()
+                M.mla_decode_attn(h, q, cache, B, max_len, sl, o, lse, ws, ws.numel())
+                e1.record()
+            torch.cuda.synchronize()
+            st, bits = M.mla_get_device_status(h)
+            if st != M.MLA_OK:
+                raise RuntimeError(f"{name}: device status {st} bits {bits}")
+            us = statistics.median(e0.elapsed_time(e1) * 1e3 for e0, e1 in evs)
+            rows = int(seqlens.sum())
+            nbytes = rows * shp.D * 2
+            flops = 2.0 * rows * shp.n_h * (shp.D + shp.d_c)
+            r = roofline_of(nbytes, flops, us * 1e-6, peaks)
+            r.update({"attn_us": round(us, 2), "GBps": round(nbytes / us / 1e3, 1), "cache_bytes": nbytes,
+                      "tokens_per_s": round(B / (us * 1e-6), 1), "batch": B, "rows": rows,
+                      "l2": "flushed before each call" if flush is not None else "cache larger than L2",
+                      "decode_path": {M.MLA_DECODE_SIMT: "simt", M.MLA_DECODE_TCGEN05: "tcgen05"}[
+                          M.mla_get_decode_path(h)]})
+            if name == "v2_ragged":
+                bal, busy = plan_balance(seqlens, h_chunks(M, h, B, max_len, device), 64)
+                r["split_rows_max_over_mean"] = bal
+                r["split_chunks_busy"] = busy
+                r["seqlen_min_max"] = [int(seqlens.min()), int(seqlens.max())]
+            out[name] = r
+        finally:
+            M.mla_destroy(h)
+            del cache
+            torch.cuda.empty_cache()
+    return out
+
+
+def h_chunks(M, h, B, max_len, device):
+    """Split-KV chunk count the attention call uses (CTA pairs of the
+    tensor-core kernel): from the SM count."""
+    import torch
+    return torch.cuda.get_device_properties(device).multi_processor_count // 2
 
 
 # --------------------------------------------------------------------------- workload
@@ -346,6 +463,7 @@ def run_ours(args, rank, world, local_rank):
     achieved_gbs = cache_bytes / attn_s / 1e9
     achieved_tf = flops / attn_s / 1e12
     hbm = peaks["hbm_gbs"]
+    roof = roofline_of(cache_bytes, flops, attn_s, peaks)
     kh = kernel_source_hash()
     traffic = committed_traffic(kh)
     tokens = B * world * args.steps
@@ -375,13 +493,15 @@ def run_ours(args, rank, world, local_rank):
         },
         "roofline": {
             "kernel": "mla_decode_attn (split plan + split-KV latent attention + LSE combine)",
-            "bound": "hbm",
-            "achieved": round(achieved_gbs, 1),
-            "peak": hbm,
-            "unit": "GB/s",
-            "frac": round(achieved_gbs / hbm, 4),
+            "bound": roof["bound"],
+            "achieved": roof["achieved"],
+            "peak": roof["peak"],
+            "unit": roof["unit"],
+            "frac": roof["frac"],
             "traffic": traffic,
-            "peak_source": f"{peaks_src} hbm_gbs",
+            "peak_source": f"{peaks_src} " + ("hbm_gbs" if roof["bound"] == "hbm" else "bf16_tflops (burst)"),
+            "roofline_us": roof["roofline_us"],
+            "frac_vs_sustained_tensor_peak": roof.get("frac_vs_sustained_tensor_peak"),
             "algorithmic_bytes_per_launch": cache_bytes,
             "launch_us": round(attn_s * 1e6, 2),
             "frac_of_nominal_8TBps": round(achieved_gbs / NOMINAL_HBM_GBS, 4),
@@ -405,6 +525,8 @@ def run_ours(args, rank, world, local_rank):
                               "attention": round(1e3 * statistics.median(attn_ms), 1),
                               "out_proj": round(1e3 * statistics.median(s45_ms), 1)},
     }
+    if world == 1 and not args.no_workloads:
+        out["attention_workloads"] = attention_workloads(device, peaks)
     if world == 1 and not args.no_cpu_baseline:
         import mla_synth as S
 
@@ -421,7 +543,11 @@ def run_ours(args, rank, world, local_rank):
 
 def run_reference(args, rank, world):
     """The oracle as it stands, on the host cores, over a bounded sample of the
-    same workload (rank 0 only)."""
+    same workload (rank 0 only). A reference step is one sequence of the batch:
+    its decode token over the full 4097-row context through the fp64
+    materialised definition (k_C, v_C per head, two-pass softmax, W_O). W
+    untimed and K timed steps run over the batch's sequences in turn, so
+    K x ms_per_step is the measured time."""
     if rank != 0:
         return None
     import torch
@@ -445,21 +571,26 @@ def run_reference(args, rank, world):
         O.decode_materialised([h_ctx], hn[b:b + 1], Wh, shp.n_h, shp.d_h, shp.d_r, shp.rope_base)
         return time.perf_counter() - t0
 
-    for w in range(min(args.warmup, 1)):
-        one(0)
-    times = [one(k % B) for k in range(max(1, min(args.steps, 3)))]
-    per_seq = statistics.mean(times)
+    for w in range(args.warmup):
+        one(w % B)
+    times = [one((args.warmup + k) % B) for k in range(args.steps)]
+    total_s = sum(times)
+    per_seq = total_s / len(times)
     value = 1.0 / per_seq
     return {
         "impl": "reference",
         "metric": METRIC, "value": round(value, 4), "unit": "tokens/s", "n_gpus": world, "steps": len(times),
-        "warmup": args.warmup, "ms_per_step": round(per_seq * B * 1e3, 1), "higher_is_better": True,
+        "warmup": args.warmup, "ms_per_step": round(per_seq * 1e3, 2), "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
         "config": {"workload": "DeepSeek-V2-shaped MLA decode: d=5120, n_h=128, d_h=128, d_c=512, d_r=64, "
                                "d_cq=1536; batch 64, context 4096 (+1), fp64 oracle on host cores",
-                   "batch_per_gpu": B, "context": ctx},
+                   "batch_per_gpu": B, "context": ctx,
+                   "step": "one sequence of the batch: its decode token over the full context"},
+        "measured_s": round(total_s, 3),
+        "full_batch_ms_extrapolated": round(per_seq * B * 1e3, 1),
         "cpu_baseline": {"value": round(value, 4), "unit": "tokens/s", "cores": threads, "kind": "oracle",
-                         "sample": f"{len(times)} sequence(s) of the batch, one decode token each, full context"},
+                         "sample": f"{len(times)} sequences of the {B}-sequence batch, one decode token each, "
+                                   f"full 4097-row context, measured in {total_s:.1f} s"},
         "e2e": {"value": round(value, 4), "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
 
@@ -472,6 +603,7 @@ def main():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--decode-path", default="auto", choices=["auto", "simt", "tc"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-workloads", action="store_true", help="skip the other workloads' attention timings")
     ap.add_argument("--cpu-budget", type=float, default=12.0)
     args = ap.parse_args()
     if args.warmup < 3 and args.impl == "ours":

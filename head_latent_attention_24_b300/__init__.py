@@ -89,6 +89,9 @@ _c = {
     "mla_get_decode_path": _sig("mla_get_decode_path", [_P, ctypes.POINTER(_I)]),
     "mla_set_proj_path": _sig("mla_set_proj_path", [_P, _I]),
     "mla_last_launch_count": _sig("mla_last_launch_count", [_P, ctypes.POINTER(_I)]),
+    "mla_set_wait_limit": _sig("mla_set_wait_limit", [_P, ctypes.c_int64]),
+    "mla_set_kv_norm": _sig("mla_set_kv_norm", [_P, _P, ctypes.c_float]),
+    "mla_set_fault_injection": _sig("mla_set_fault_injection", [_P, _I]),
 }
 
 
@@ -225,6 +228,19 @@ def mla_get_decode_path(handle) -> int:
 
 def mla_set_proj_path(handle, path):
     _check(_c["mla_set_proj_path"](handle, path), "mla_set_proj_path")
+
+
+def mla_set_kv_norm(handle, weight, eps=1e-5):
+    """weight: device tensor [d_c] in the handle's dtype, or None to turn the norm off."""
+    _check(_c["mla_set_kv_norm"](handle, _ptr(weight), eps), "mla_set_kv_norm")
+
+
+def mla_set_wait_limit(handle, cycles):
+    _check(_c["mla_set_wait_limit"](handle, cycles), "mla_set_wait_limit")
+
+
+def mla_set_fault_injection(handle, mode):
+    _check(_c["mla_set_fault_injection"](handle, mode), "mla_set_fault_injection")
 
 
 def mla_last_launch_count(handle) -> int:

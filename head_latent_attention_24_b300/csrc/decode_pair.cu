@@ -14,37 +14,43 @@
 // CTAs of a cluster divide the work:
 //   * CTA 0 ("score") holds q~ (the 512 latent columns of q_abs) in TMEM as
 //     the A operand and q_R in shared memory, streams full cache tiles
-//     (128 rows x 576) through a ring, and computes S = Q . C^T (M = 128
-//     heads, N = 128 rows, K = 576) into a double-buffered TMEM score block.
-//     Eight softmax warps (two per TMEM lane quarter, 64 rows each) turn each
-//     score tile into bf16 probabilities P and write them, 64 rows at a time,
-//     straight into CTA 1's shared memory.
+//     (128 rows x 576) through a four-slot ring of 48 KB boxes, and computes
+//     S = Q . C^T (M = 128 heads, N = 128 rows, K = 576) into a
+//     double-buffered TMEM score block. Eight softmax warps (two per TMEM
+//     lane quarter, 64 rows each) turn each score tile into bf16
+//     probabilities P and store them, 64 rows at a time, straight from
+//     registers into CTA 1's shared memory (st.async, completing on CTA 1's
+//     barrier), in the exact layout the MMA reads.
 //   * CTA 1 ("value") keeps O = sum_t P_t c_KV_t in all of its TMEM and
-//     streams only the latent part of the same rows (mostly from L2, where
-//     CTA 0's loads left them): O += P . C (M = 128 heads, N = 256 latent
-//     columns x 2, K = 64 rows per unit). Its four correction warps apply the
-//     rare softmax rescale to O, zero cache rows past a sequence end (P is 0
-//     there, but the rows may hold NaN), and write o_lat / partials at the end
-//     of each piece.
+//     streams the latent part of the same rows (mostly from L2, where CTA 0's
+//     loads left them): O += P . C (M = 128 heads, N = 256 latent columns x 2,
+//     K = 64 rows per unit). Its four correction warps apply the rare softmax
+//     rescale to O, zero cache rows past a sequence end (P is 0 there, but the
+//     rows may hold NaN), and write o_lat / partials at the end of each piece.
+// The score SM's copy engine is the scarce resource: it must bring in 1152
+// bytes per cached row, close to what one SM's TMA unit moves. So nothing else
+// rides on it: P leaves through the threads' asynchronous remote stores,
+// not through bulk copies. Only 2 bytes per head and row cross the pair.
 // Every MMA has M = 128 and N >= 128, the shapes that run at the full tensor
-// rate; only P (2 bytes per head and row) crosses between the SMs. One thread
-// issues each CTA's MMAs, and at this rate its instruction count matters: the
-// issue loops are unrolled over a tile's boxes and add compile-time offsets to
-// shared-memory descriptors built once per kernel.
+// rate. One thread issues each CTA's MMAs, and at this rate its instruction
+// count matters: the issue loops are unrolled over a tile's boxes and add
+// compile-time offsets to shared-memory descriptors built once per kernel.
 //
 // Softmax: online, in base 2, with a lazy reference maximum per head: the
 // reference moves (and O is rescaled) only when a tile's maximum rises more
 // than 8 above it, so P <= 256 and rescales are rare after the first tile.
 //
-// Work split: the plan of the CUDA-core kernel (all sequences' rows end to
-// end, cut into equal chunks, one per pair); a piece covering a whole
-// sequence writes o_lat/lse directly, any other piece a partial slot that
-// the LSE combine kernel merges.
+// Work split: the plan kernel either gives pair c the whole of sequence c
+// (when every sequence has a pair and the longest one costs little more than
+// an equal split: no partials, no merge), or lays all sequences' rows end to
+// end and cuts them into equal chunks, one per pair; a piece covering a whole
+// sequence writes o_lat/lse directly, any other piece a partial slot that the
+// LSE combine kernel merges.
 //
 // Every mbarrier wait is bounded; on expiry a CTA records MLA_DEV_TIMEOUT,
 // stops issuing work, waits (bounded) for its own copies in flight, joins the
 // final cluster barrier and frees its TMEM.
-#include "decode_tc.cuh"
+#include "decode_pair.cuh"
 #include "tc_ptx.cuh"
 #include "tmap.cuh"
 
@@ -67,22 +73,20 @@ constexpr float RESCALE_THRESHOLD = 8.0f;
 // 9 column chunks} with the chunk as the outermost dimension, so one TMA box
 // brings several 128-byte column chunks of many rows and lands them chunk-major
 // ([chunk][row][128 B], 128-byte swizzle): the K-major layout tcgen05 reads.
-// TMA throughput per SM is set by the number of boxes, so boxes are large.
 // CTA 0 shared-memory layout (bytes from the 1024-aligned base)
 constexpr int QR_BYTES = NH * 64 * 2;             // 16 KB: q_R of 128 heads
 constexpr int S0_CPB = 3;                         // column chunks per score box
-constexpr int S0_RING = 3;                        // score ring slots (one box each)
+constexpr int S0_RING = 4;                        // score ring slots (one box each)
 constexpr int S0_CHUNK = TR * 128;                // 16 KB: 128 rows x 64 columns
 constexpr int S0_SLOT = S0_CPB * S0_CHUNK;        // 48 KB
-// A P unit travels as one bulk copy: P (128 heads x 64 rows bf16, K-major,
-// 128-byte swizzle) followed by its Info block.
-constexpr int NPB = 3;                            // P buffers (one per value unit) on each side
-constexpr int P_BYTES = NH * UR * 2;              // 16 KB
-constexpr int P_STRIDE = 18 * 1024;               // P + Info, 1024-aligned buffers
 constexpr int S0_QR_OFF = 0;
 constexpr int S0_RING_OFF = QR_BYTES;
-constexpr int S0_STG_OFF = S0_RING_OFF + S0_RING * S0_SLOT;   // P staging buffers
-constexpr int S0_END = S0_STG_OFF + NPB * P_STRIDE;
+constexpr int S0_END = S0_RING_OFF + S0_RING * S0_SLOT;
+// A P unit: P (128 heads x 64 rows bf16, K-major, 128-byte swizzle) followed
+// by one 16-byte Info entry per head.
+constexpr int NPB = 3;                            // P buffers in CTA 1's shared memory
+constexpr int P_BYTES = NH * UR * 2;              // 16 KB
+constexpr int P_STRIDE = 18 * 1024;               // P + Info, 1024-aligned
 // CTA 1 shared-memory layout
 constexpr int S1_CPB = 4;                         // latent chunks per value box
 constexpr int S1_RING = 4;
@@ -103,23 +107,20 @@ constexpr uint32_t S_COL = 256;         // CTA 0: two score blocks of 128 column
 
 constexpr uint32_t FLAG_LAST = 1u;
 
-struct Info {                 // follows P in each buffer
-  float alpha[NH];            // factor O is rescaled by before this unit (1 = none)
-  float l[NH];                // softmax denominator of the piece (if FLAG_LAST)
-  uint32_t flags;
-  uint32_t pad[3];
-};
-constexpr int P_COPY_BYTES = P_BYTES + (int)sizeof(Info);
+// Info entry of head h (follows P): x = factor O is rescaled by before this
+// unit (1 = none), y = softmax denominator of the piece (if FLAG_LAST),
+// z = flags (bit pattern), w unused.
+constexpr int P_COPY_BYTES = P_BYTES + NH * 16;
 static_assert(P_COPY_BYTES % 16 == 0 && P_COPY_BYTES <= P_STRIDE, "P unit layout");
 
 struct Ctl {
   // CTA 0
   uint64_t r0_full[S0_RING], r0_empty[S0_RING];
   uint64_t q_free, q_ready, s_full[2], s_free[2];
-  uint64_t p_free[NPB];       // arrivals: CTA 1's MMA commit + CTA 1's info read
+  uint64_t p_free[NPB];       // arrivals: CTA 1's PV MMA commit + CTA 1's Info read
   // CTA 1
   uint64_t r1_full[S1_RING], r1_empty[S1_RING];
-  uint64_t p_full[NPB];       // CTA 1's own arming arrival + the bulk copy's bytes
+  uint64_t p_full[NPB];       // CTA 1's own arming arrival + the remote stores' bytes
   uint64_t unit_ready[NPB];   // CTA 1 correction warps -> MMA
   // PV of the unit in P buffer b complete. One barrier per buffer: a waiter
   // at unit u has seen p_full(u), which implies PV(u - NPB) completed, and
@@ -128,9 +129,11 @@ struct Ctl {
   uint64_t pv_done[NPB];
   uint64_t o_free;            // O read out by the 8 epilogue warps
   uint64_t epi_go;            // a piece's last PV is done and inv_l is in shared memory
+  uint64_t mma_done;          // every MMA this CTA issued has completed (teardown)
   float inv_l[NH];            // CTA 1: 1 / softmax denominator of the piece being written
   uint32_t tmem_base;
   int abort;
+  long long wait_limit;       // cycles before a wait gives up
   float mx[2][2][NH];         // CTA 0: per-half tile maxima, double-buffered by tile
   float lsum[2][NH];          // CTA 0: per-half softmax sums at a piece end
 };
@@ -157,7 +160,6 @@ __device__ __forceinline__ bool half_all(int hf, bool v) {
       : "memory");
   return out != 0;
 }
-__device__ __forceinline__ void cw_sync() { asm volatile("bar.sync 2, 128;" ::: "memory"); }
 __device__ __forceinline__ bool cw_any(bool v) {
   uint32_t out;
   asm volatile(
@@ -184,6 +186,12 @@ struct Pieces {
   const int32_t* cum; int B, start, end, b;
   __device__ void init(const int32_t* c, int B_, int chunk) {
     cum = c; B = B_;
+    if (cum[B + 3]) {            // whole-sequence plan: chunk c is sequence c
+      b = chunk < B ? chunk : B;
+      start = chunk < B ? cum[chunk] : 0;
+      end = chunk < B ? cum[chunk + 1] : 0;
+      return;
+    }
     const int cl = cum[B + 1], total = cum[B + 2];
     start = chunk * cl;
     end = min(start + cl, total);
@@ -262,20 +270,36 @@ __device__ __forceinline__ void store_o_half(const CUtensorMap* map_ol, const CU
   if (issuer) bulk_wait_all();   // complete before the buffer is reused or the CTA exits
 }
 
+// Every wait gives up after ctl.wait_limit cycles, or as soon as another role
+// of this CTA has given up; the first to expire records MLA_DEV_TIMEOUT.
 __device__ __forceinline__ bool wait_or_abort(uint64_t* bar, uint32_t parity, Ctl& ctl, int32_t* status) {
-  if (*reinterpret_cast<volatile int*>(&ctl.abort)) return false;
-  if (mbar_wait(bar, parity, WAIT_CYCLES)) return true;
-  atomicOr(status, MLA_DEV_TIMEOUT);
-  ctl.abort = 1;
+  volatile int* ab = reinterpret_cast<volatile int*>(&ctl.abort);
+  if (*ab) return false;
+  if (mbar_wait_abortable(bar, parity, ctl.wait_limit, ab)) return true;
+  if (!*ab) atomicOr(status, MLA_DEV_TIMEOUT);
+  *ab = 1;
   return false;
 }
 
 __device__ __forceinline__ bool wait_cluster_or_abort(uint64_t* bar, uint32_t parity, Ctl& ctl, int32_t* status) {
-  if (*reinterpret_cast<volatile int*>(&ctl.abort)) return false;
-  if (mbar_wait_cluster(bar, parity, WAIT_CYCLES)) return true;
-  atomicOr(status, MLA_DEV_TIMEOUT);
-  ctl.abort = 1;
+  volatile int* ab = reinterpret_cast<volatile int*>(&ctl.abort);
+  if (*ab) return false;
+  if (mbar_wait_cluster_abortable(bar, parity, ctl.wait_limit, ab)) return true;
+  if (!*ab) atomicOr(status, MLA_DEV_TIMEOUT);
+  *ab = 1;
   return false;
+}
+
+// After an abort: wait (bounded) until every TMA load this producer issued
+// into a ring of `ring` slots has landed, so that no copy writes shared memory
+// after the CTA has moved on. `issued` loads went to slots 0, 1, 2, ... in
+// turn; the last one into slot s filled that slot's phase (last / ring).
+__device__ __forceinline__ void drain_ring(uint64_t* full, int ring, int issued) {
+  for (int s = 0; s < ring; ++s) {
+    if (issued <= s) break;
+    const int last = s + ring * ((issued - 1 - s) / ring);
+    mbar_wait(&full[s], (uint32_t)((last / ring) & 1), WAIT_CYCLES / 8);
+  }
 }
 
 __global__ void __launch_bounds__(NTHREADS, 1)
@@ -296,16 +320,18 @@ __global__ void __launch_bounds__(NTHREADS, 1)
     for (int i = 0; i < 2; ++i) { mbar_init(&ctl.s_full[i], 1); mbar_init(&ctl.s_free[i], 8); }
     mbar_init(&ctl.q_free, 1);
     mbar_init(&ctl.q_ready, 8);
-    for (int i = 0; i < NPB; ++i) {
-      mbar_init(&ctl.p_free[i], 2);
-      mbar_init(&ctl.p_full[i], 1);
-      mbar_init(&ctl.unit_ready[i], 4);
-    }
     for (int i = 0; i < S1_RING; ++i) { mbar_init(&ctl.r1_full[i], 1); mbar_init(&ctl.r1_empty[i], 1); }
-    for (int i = 0; i < NPB; ++i) mbar_init(&ctl.pv_done[i], 1);
+    for (int i = 0; i < NPB; ++i) {
+      mbar_init(&ctl.p_full[i], 1);
+      mbar_init(&ctl.p_free[i], 2);
+      mbar_init(&ctl.unit_ready[i], 4);
+      mbar_init(&ctl.pv_done[i], 1);
+    }
     mbar_init(&ctl.o_free, 8);
     mbar_init(&ctl.epi_go, 4);
+    mbar_init(&ctl.mma_done, 1);
     ctl.abort = 0;
+    ctl.wait_limit = a.wait_cycles > 0 ? a.wait_cycles : WAIT_CYCLES;
     if (cluster_rank() == 1)  // arm the first use of every P buffer
       for (int i = 0; i < NPB; ++i) mbar_arrive_expect_tx(&ctl.p_full[i], P_COPY_BYTES);
     fence_mbar_init();
@@ -357,9 +383,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
             }
           }
         }
-        if (!ok) {  // let copies in flight land before the CTA can exit
-          for (int s = 0; s < S0_RING; ++s) mbar_wait(&ctl.r0_full[s], 0, WAIT_CYCLES / 8);
-        }
+        if (!ok) drain_ring(ctl.r0_full, S0_RING, i);  // no copy lands after the CTA moves on
       }
     } else if (warp == 1) {
       // ---------------------------------------------------------- MMA issuer (QK)
@@ -371,9 +395,8 @@ __global__ void __launch_bounds__(NTHREADS, 1)
         bool whole;
         int piece = 0, g = 0, i = 0;
         bool ok = true;
-        const uint32_t qr = sbase + S0_QR_OFF;
         const uint64_t ring_desc = sdesc_sw128(sbase + S0_RING_OFF, 16, 1024);
-        const uint64_t qr_desc = sdesc_sw128(qr, 16, 1024);
+        const uint64_t qr_desc = sdesc_sw128(sbase + S0_QR_OFF, 16, 1024);
         while (ok && it.next(seq, t0, t1, whole)) {
           i += NCH / S0_CPB;   // the query boxes: the softmax warps take them
           ok = wait_or_abort(&ctl.q_ready, piece & 1, ctl, a.status);
@@ -411,8 +434,11 @@ __global__ void __launch_bounds__(NTHREADS, 1)
           if (ok) mma_commit(&ctl.q_free);
           ++piece;
         }
+        // nothing of this CTA's reaches the tensor cores after it moves on
+        mma_commit(&ctl.mma_done);
+        mbar_wait(&ctl.mma_done, 0, WAIT_CYCLES / 8);
       }
-    } else {
+    } else if (warp < 10) {
       // ---------------------------------------------------------- softmax warps 2..9
       const int quarter = warp & 3;
       const int hf = (warp - 2) >> 2;                 // which 64 rows of a tile
@@ -477,7 +503,8 @@ __global__ void __launch_bounds__(NTHREADS, 1)
           if (threadIdx.x == 64)
             for (int j = 0; j < NCH / S0_CPB; ++j) mbar_arrive(&ctl.r0_empty[(iq + j) % S0_RING]);
           __syncwarp();
-          if (lane == 0) mbar_arrive(&ctl.q_ready);
+          // test hook: withhold the first piece's query-ready arrival
+          if (lane == 0 && !(a.fault == 1 && piece == 0)) mbar_arrive(&ctl.q_ready);
         }
         float m_ref = -INFINITY, l_part = 0.f;
         for (int k = 0; k < ntiles; ++k, ++g) {
@@ -540,35 +567,55 @@ __global__ void __launch_bounds__(NTHREADS, 1)
             sm_sync();
           }
           if (has_unit) {
+            // the P buffer in CTA 1: its previous unit's PV is done and its Info was read
             const int pb = my_u % NPB;
             bool wf = true;
             if (my_u >= NPB) wf = wait_cluster_or_abort(&ctl.p_free[pb], ((my_u / NPB) - 1) & 1, ctl, a.status);
-            // P row h of this unit (64 bf16 = 8 units of 16 B, 128-byte swizzle)
-            // and its Info into the local staging buffer, then one bulk copy
-            uint8_t* stg = smem + S0_STG_OFF + pb * P_STRIDE;
-            if (wf) {
-              uint8_t* row = stg + (h >> 3) * 1024 + (h & 7) * 128;
+            if (!half_all(hf, wf)) ok = false;
+            if (ok) {
+              // P row h of this unit (64 bf16 = 8 chunks of 16 B, 128-byte swizzle) and head h's
+              // Info entry, stored into CTA 1's buffer; their bytes complete CTA 1's p_full.
+              // Remote stores move twice as fast when each warp store covers whole 128-byte
+              // rows, so the 8 lanes of each group first transpose their 8 x 8 chunks
+              // (three butterfly stages): lane c of group g then holds chunk c of heads
+              // 8g .. 8g+7, and store j writes head 8g+j's row, all 8 chunks across the group.
+              const int cg = lane & 7;
 #pragma unroll
-              for (int v = 0; v < 8; ++v)
-                *reinterpret_cast<uint4*>(row + ((v ^ (h & 7)) << 4)) =
-                    make_uint4(packed[4 * v], packed[4 * v + 1], packed[4 * v + 2], packed[4 * v + 3]);
-              Info* inf = reinterpret_cast<Info*>(stg + P_BYTES);
+              for (int st = 4; st >= 1; st >>= 1) {
+                const bool up = (cg & st) != 0;
+#pragma unroll
+                for (int r = 0; r < 8; ++r) {
+                  if (r & st) continue;
+#pragma unroll
+                  for (int e = 0; e < 4; ++e) {
+                    const uint32_t send = up ? packed[4 * r + e] : packed[4 * (r + st) + e];
+                    const uint32_t recv = __shfl_xor_sync(0xffffffffu, send, st);
+                    if (up) packed[4 * r + e] = recv; else packed[4 * (r + st) + e] = recv;
+                  }
+                }
+              }
+              const uint32_t dst = peer_p + pb * P_STRIDE;
+              const uint32_t bar = peer_pfull + pb * 8;
+              const int hg = h & ~7;                // this lane's group of 8 heads
+#pragma unroll
+              for (int j = 0; j < 8; ++j) {
+                const int hh = hg + j;              // the head whose row store j writes
+                st_async_v4(dst + (hh >> 3) * 1024 + j * 128 + ((cg ^ j) << 4),
+                            make_uint4(packed[4 * j], packed[4 * j + 1], packed[4 * j + 2], packed[4 * j + 3]), bar);
+              }
               const bool last_unit = last_tile && (hf == 1 || nvalid <= UR);
-              inf->alpha[h] = hf == 0 ? alpha : 1.f;  // the rescale applies before the tile's first unit
+              float l = 0.f;
               if (last_unit) {
-                const float l = ctl.lsum[0][h] + ctl.lsum[1][h];
-                inf->l[h] = l;
+                l = ctl.lsum[0][h] + ctl.lsum[1][h];
                 const float lse = l > 0.f ? (m_ref + log2f(l)) * kLn2 : -INFINITY;
                 if (whole) a.lse[(size_t)seq * NH + h] = lse;
                 else a.part_lse[(size_t)(seq + chunk) * NH + h] = lse;
               }
-              if (h == 0) inf->flags = last_unit ? FLAG_LAST : 0u;
-              fence_proxy_async_smem();
+              // the rescale applies before the tile's first unit
+              st_async_v4(dst + P_BYTES + h * 16,
+                          make_uint4(__float_as_uint(hf == 0 ? alpha : 1.f), __float_as_uint(l),
+                                     last_unit ? FLAG_LAST : 0u, 0u), bar);
             }
-            // the half meets here: the copy is issued only if every thread wrote its row
-            const bool all = half_all(hf, wf);
-            if (!all) ok = false;
-            if (all && h == 0) bulk_copy_to_cluster(peer_p + pb * P_STRIDE, stg, P_COPY_BYTES, peer_pfull + pb * 8);
           }
           u += (nvalid > UR) ? 2 : 1;
         }
@@ -600,9 +647,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
             }
           }
         }
-        if (!ok) {
-          for (int s = 0; s < S1_RING; ++s) mbar_wait(&ctl.r1_full[s], 0, WAIT_CYCLES / 8);
-        }
+        if (!ok) drain_ring(ctl.r1_full, S1_RING, i);  // no copy lands after the CTA moves on
       }
     } else if (warp == 1) {
       // ---------------------------------------------------------- MMA issuer (PV)
@@ -647,6 +692,9 @@ __global__ void __launch_bounds__(NTHREADS, 1)
           }
           ++piece;
         }
+        // nothing of this CTA's reaches the tensor cores after it moves on
+        mma_commit(&ctl.mma_done);
+        mbar_wait(&ctl.mma_done, 0, WAIT_CYCLES / 8);
       }
     } else if (warp < 6) {
       // ---------------------------------------------------------- correction / epilogue warps 2..5
@@ -670,11 +718,11 @@ __global__ void __launch_bounds__(NTHREADS, 1)
           ok = wait_cluster_or_abort(&ctl.p_full[pb], (u / NPB) & 1, ctl, a.status);
           ok = !cw_any(!ok);
           if (!ok) break;
-          const Info* inf = reinterpret_cast<const Info*>(smem + S1_P_OFF + pb * P_STRIDE + P_BYTES);
-          const uint32_t flags = *reinterpret_cast<const volatile uint32_t*>(&inf->flags);
-          const float alpha = inf->alpha[h];
+          const float4 inf = *reinterpret_cast<const float4*>(smem + S1_P_OFF + pb * P_STRIDE + P_BYTES + h * 16);
+          const uint32_t flags = __float_as_uint(inf.z);
+          const float alpha = inf.x;
           if (flags & FLAG_LAST) {
-            const float l = inf->l[h];
+            const float l = inf.y;
             inv_l = l > 0.f ? 1.f / l : 0.f;
           }
           // Rescale this warp's 32 rows of O when any of them has alpha != 1
@@ -738,7 +786,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
         }
         ++piece;
       }
-    } else {
+    } else if (warp < 10) {
       // ---------------------------------------------------------- epilogue warps 6..9: columns 256..511
       const int quarter = warp & 3;
       const int h = quarter * 32 + lane;
@@ -799,7 +847,11 @@ cudaError_t launch_decode_tc(const mla_handle_s* h, const DecodeArgs& a, cudaStr
   if (!make_tmap_2d_bf16_sw128(&map_ol, a.o_lat, DC, (uint64_t)a.B * NH, DC * 2, 64, NH)) return cudaErrorInvalidValue;
   if (!make_tmap_2d_f32_sw128(&map_po, a.part_o, DC, (uint64_t)(a.B + a.grid_chunks) * NH, DC * 4, 32, NH))
     return cudaErrorInvalidValue;
-  cudaError_t e = launch_decode_plan(a.seqlens, a.B, a.max_len, a.grid_chunks, UR, a.plan, a.status, s);
+  // A split costs its pair about a thousand rows of streaming time (the
+  // partials' stores, the piece switch and the merge launch).
+  constexpr int kSplitCostRows = 1024;
+  cudaError_t e = launch_decode_plan(a.seqlens, a.B, a.max_len, a.grid_chunks, UR, a.allow_whole, kSplitCostRows,
+                                     a.plan, a.status, s);
   if (e != cudaSuccess) return e;
   static bool attr_set = false;
   if (!attr_set) {

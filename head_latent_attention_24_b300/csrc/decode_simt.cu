@@ -20,7 +20,7 @@ namespace mla {
 
 size_t decode_ws_bytes(int B, int n_h, int d_c, int chunks) {
   const size_t slots = (size_t)B + (size_t)chunks;
-  size_t b = align_up(sizeof(int32_t) * ((size_t)B + 3), 256);
+  size_t b = align_up(sizeof(int32_t) * ((size_t)B + PLAN_EXTRA), 256);
   b += align_up(sizeof(float) * slots * n_h * d_c, 256);
   b += align_up(sizeof(float) * slots * n_h, 256);
   return b;
@@ -31,7 +31,7 @@ void decode_ws_carve(void* ws, int B, int n_h, int d_c, int chunks, int32_t** pl
   const size_t slots = (size_t)B + (size_t)chunks;
   char* p = static_cast<char*>(ws);
   *plan = reinterpret_cast<int32_t*>(p);
-  p += align_up(sizeof(int32_t) * ((size_t)B + 3), 256);
+  p += align_up(sizeof(int32_t) * ((size_t)B + PLAN_EXTRA), 256);
   *part_o = reinterpret_cast<float*>(p);
   p += align_up(sizeof(float) * slots * n_h * d_c, 256);
   *part_lse = reinterpret_cast<float*>(p);
@@ -60,17 +60,21 @@ __device__ __forceinline__ int warp_iscan(int v, int lane) {
   return v;
 }
 
-// plan[0..B] = cumulative clamped lengths, plan[B+1] = chunk length, plan[B+2] = total rows.
+// plan[0..B] = cumulative clamped lengths, plan[B+1] = chunk length,
+// plan[B+2] = total rows, plan[B+3] = 1 when each chunk c < B takes sequence c
+// whole instead (see launch_decode_plan).
 __global__ void __launch_bounds__(1024) decode_plan_kernel(const int32_t* __restrict__ seqlens, int B,
                                                            int max_len, int chunks, int granule,
+                                                           int allow_whole, int split_cost_rows,
                                                            int32_t* __restrict__ plan,
                                                            int32_t* __restrict__ status) {
   __shared__ int warp_tot[32];
-  __shared__ int carry;
+  __shared__ int warp_max[32];
+  __shared__ int carry, longest;
   pdl_trigger();
   pdl_wait();
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  if (tid == 0) { carry = 0; plan[0] = 0; }
+  if (tid == 0) { carry = 0; longest = 0; plan[0] = 0; }
   __syncthreads();
   for (int base = 0; base < B; base += 1024) {
     const int b = base + tid;
@@ -83,11 +87,19 @@ __global__ void __launch_bounds__(1024) decode_plan_kernel(const int32_t* __rest
       }
     }
     int x = warp_iscan(v, lane);
+    int m = v;
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) m = max(m, __shfl_xor_sync(0xffffffffu, m, o));
     if (lane == 31) warp_tot[warp] = x;
+    if (lane == 0) warp_max[warp] = m;
     __syncthreads();
     if (warp == 0) {
       const int t = warp_iscan(warp_tot[lane], lane);
       warp_tot[lane] = t;
+      int mm = warp_max[lane];
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) mm = max(mm, __shfl_xor_sync(0xffffffffu, mm, o));
+      if (lane == 0) longest = max(longest, mm);
     }
     __syncthreads();
     if (warp > 0) x += warp_tot[warp - 1];
@@ -103,6 +115,10 @@ __global__ void __launch_bounds__(1024) decode_plan_kernel(const int32_t* __rest
     if (cl < granule) cl = granule;
     plan[B + 1] = (int)cl;
     plan[B + 2] = total;
+    // Whole sequences per chunk when every sequence has a chunk of its own and
+    // the longest one costs no more than an equal split plus the price of
+    // splitting (partial writes and their merge).
+    plan[B + 3] = (allow_whole && B <= chunks && (long long)longest <= cl + split_cost_rows) ? 1 : 0;
   }
 }
 
@@ -288,6 +304,7 @@ __global__ void __launch_bounds__(256) decode_combine_kernel(const DecodeArgs a)
     if (lane == 0) a.lse[(long long)b * a.n_h + h] = -INFINITY;
     return;
   }
+  if (cum[B + 3]) return;  // whole-sequence plan: written by the attention kernel
   const int c0 = s0 / chunk_len, c1 = (s1 - 1) / chunk_len;
   if (c0 == c1) return;  // written whole by the attention kernel
   const int np = c1 - c0 + 1;
@@ -365,9 +382,11 @@ int decode_simt_chunks(const mla_handle_s* h) {
 }
 
 cudaError_t launch_decode_plan(const int32_t* seqlens, int B, int max_len, int chunks, int granule,
-                               int32_t* plan, int32_t* status, cudaStream_t s) {
+                               int allow_whole, int split_cost_rows, int32_t* plan, int32_t* status,
+                               cudaStream_t s) {
   LaunchCfg lc(dim3(1), dim3(1024), 0, s);
-  cudaError_t e = cudaLaunchKernelEx(&lc.cfg, decode_plan_kernel, seqlens, B, max_len, chunks, granule, plan, status);
+  cudaError_t e = cudaLaunchKernelEx(&lc.cfg, decode_plan_kernel, seqlens, B, max_len, chunks, granule, allow_whole,
+                                     split_cost_rows, plan, status);
   if (e != cudaSuccess) return e;
   return cudaGetLastError();
 }
@@ -375,7 +394,7 @@ cudaError_t launch_decode_plan(const int32_t* seqlens, int B, int max_len, int c
 cudaError_t launch_decode_simt(const DecodeArgs& a, int dtype, cudaStream_t s, int* launches) {
   const int D = a.d_c + a.d_r;
   if (a.d_c > 512 || D % 8 != 0) return cudaErrorInvalidValue;
-  cudaError_t e = launch_decode_plan(a.seqlens, a.B, a.max_len, a.grid_chunks, TT, a.plan, a.status, s);
+  cudaError_t e = launch_decode_plan(a.seqlens, a.B, a.max_len, a.grid_chunks, TT, 0, 0, a.plan, a.status, s);
   if (e != cudaSuccess) return e;
   const size_t smem = sizeof(float) * ((size_t)HG * D + (size_t)TT * (D + 1) + HG * TT + 3 * HG);
   dim3 grid(a.grid_chunks, (a.n_h + HG - 1) / HG);

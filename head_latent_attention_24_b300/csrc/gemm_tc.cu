@@ -73,10 +73,10 @@ struct Ctl {
 };
 
 __device__ __forceinline__ bool wait_bar(uint64_t* bar, uint32_t parity, Ctl& ctl, int32_t* status) {
-  if (ctl.abort) return false;
+  if (*reinterpret_cast<volatile int*>(&ctl.abort)) return false;
   if (mbar_wait(bar, parity, WAIT_CYCLES)) return true;
   atomicOr(status, MLA_DEV_TIMEOUT);
-  ctl.abort = 1;
+  *reinterpret_cast<volatile int*>(&ctl.abort) = 1;
   return false;
 }
 
@@ -155,12 +155,23 @@ __global__ void __launch_bounds__(NTHREADS, 2)
       }
       pdl_wait();
       for (int i = 0; i < pre; ++i) load_x(i);
+      int issued = pre;
       for (int i = pre; i < nk; ++i) {
         const int st = i % p.nstage;
         if (!wait_bar(&ctl.empty[st], ((i / p.nstage) - 1) & 1, ctl, p.status)) break;
         mbar_arrive_expect_tx(&ctl.full[st], bytes);
         load_w(i);
         load_x(i);
+        issued = i + 1;
+      }
+      if (issued < nk) {
+        // Aborted: wait (bounded) until every stage loaded so far has landed,
+        // before the epilogue reuses the stage buffers or the CTA exits. The
+        // last load into stage s filled its phase (last / nstage).
+        for (int st = 0; st < p.nstage && st < issued; ++st) {
+          const int last = st + p.nstage * ((issued - 1 - st) / p.nstage);
+          mbar_wait(&ctl.full[st], (uint32_t)((last / p.nstage) & 1), WAIT_CYCLES / 8);
+        }
       }
     }
   } else if (warp == 1) {
@@ -191,6 +202,8 @@ __global__ void __launch_bounds__(NTHREADS, 2)
         mma_commit(&ctl.empty[st]);
       }
       mma_commit(&ctl.acc_full);
+      // no MMA of this CTA is still running when it frees its TMEM
+      mbar_wait(&ctl.acc_full, 0, WAIT_CYCLES / 8);
     }
   } else {
     // ------------------------------------------------------------ epilogue warps 2..5
@@ -198,21 +211,22 @@ __global__ void __launch_bounds__(NTHREADS, 2)
     const int m = quarter * 32 + lane;           // this thread's TMEM lane = tile row
     float* cs = reinterpret_cast<float*>(smem);  // [MT][n_tile][BM] partials, reuses the stages
     pdl_wait();   // before the epilogue reads indices or writes the output
-    const bool ok = nk > 0 && wait_bar(&ctl.acc_full, 0, ctl, p.status);
+    // warp-uniform: the TMEM loads below are warp-collective
+    const bool ok = __all_sync(0xffffffffu, nk > 0 && wait_bar(&ctl.acc_full, 0, ctl, p.status));
     if (ok) tc_fence_after();
-    for (int t = 0; t < MT; ++t) {
+    // After an abort the stage buffers may still be receiving loads (the
+    // producer drains them before the cluster barrier below): leave them
+    // alone; the result is void and the status word says so.
+    for (int t = 0; t < MT && ok; ++t) {
       for (int c = 0; c < p.n_tile; c += 64) {
         float v[64];
         const int nc = min(64, p.n_tile - c);   // n_tile is a multiple of 16
-        if (ok) {
+        {
           const uint32_t ta = tbase + (static_cast<uint32_t>(quarter * 32) << 16) + (uint32_t)(t * p.n_tile + c);
 #pragma unroll
           for (int q = 0; q < 4; ++q)
             if (16 * q < nc) tmem_ld16(ta + 16 * q, *reinterpret_cast<float(*)[16]>(v + 16 * q));
           tmem_ld_wait();
-        } else {
-#pragma unroll
-          for (int i = 0; i < 64; ++i) v[i] = 0.f;
         }
 #pragma unroll
         for (int i = 0; i < 64; ++i)

@@ -20,6 +20,10 @@ struct mla_handle_s {
   int32_t decode_chunks;   // split-KV chunk count requested (0 = automatic)
   int32_t proj_path;       // mla_proj_path_t requested
   int32_t last_launches;   // launches made by the last successful call
+  long long wait_cycles;   // mla_set_wait_limit (0 = kernel defaults)
+  int32_t fault;           // mla_set_fault_injection
+  const void* kv_norm_weight;  // mla_set_kv_norm: device [d_c] (NULL = no norm)
+  float kv_norm_eps;
 };
 
 namespace mla {
@@ -138,22 +142,37 @@ struct DecodeArgs {
   int B, max_len, n_h, d_c, d_r;
   float scale_log2;            // scale * log2(e)
   // workspace carve-up
-  int32_t* plan;               // [B+1] cumulative lengths, then [chunk_len, total]
+  int32_t* plan;               // [B+1] cumulative lengths, then [chunk_len, total, whole]
   float* part_o;               // [slots, n_h, d_c]
   float* part_lse;             // [slots, n_h]  (natural log)
   int grid_chunks;             // number of token chunks (CTAs along x)
+  int allow_whole;             // the plan may give each chunk one whole sequence
+  long long wait_cycles;       // bound of every mbarrier wait (0 = the kernel's default, ~2 s)
+  int fault;                   // 1: the tensor-core kernel withholds one internal arrival (test hook)
   int32_t* status;
 };
 
 // Workspace layout for decode: plan | partial O | partial LSE.
+constexpr int PLAN_EXTRA = 4;  // the plan holds B + PLAN_EXTRA int32 entries
 size_t decode_ws_bytes(int B, int n_h, int d_c, int chunks);
 void decode_ws_carve(void* ws, int B, int n_h, int d_c, int chunks,
                      int32_t** plan, float** part_o, float** part_lse);
 int decode_simt_chunks(const mla_handle_s* h);
 
+// Split plan: cumulative clamped lengths of the batch's sequences laid end to
+// end, cut into `chunks` equal row ranges rounded up to `granule`. With
+// allow_whole, the plan instead gives chunk c < B the whole of sequence c when
+// B <= chunks and the longest sequence is at most split_cost_rows longer than
+// an equal chunk (the estimated cost of splitting, in rows).
 cudaError_t launch_decode_plan(const int32_t* seqlens, int B, int max_len, int chunks, int granule,
-                               int32_t* plan, int32_t* status, cudaStream_t s);
+                               int allow_whole, int split_cost_rows, int32_t* plan, int32_t* status,
+                               cudaStream_t s);
 cudaError_t launch_decode_simt(const DecodeArgs& a, int dtype, cudaStream_t s, int* launches);
 cudaError_t launch_decode_combine(const DecodeArgs& a, int dtype, cudaStream_t s);
+
+// RMSNorm of the latent part of appended cache rows (kv_norm variant).
+cudaError_t launch_kv_norm_rows(void* cache, const void* weight, float eps, const int32_t* tok_seq,
+                                const int32_t* tok_pos, int n_tokens, int cache_batch, int max_len, int max_pos,
+                                int d_c, int row_width, int dtype, cudaStream_t s);
 
 }  // namespace mla

@@ -6,7 +6,8 @@
 #include <vector>
 
 #include "internal.cuh"
-#include "decode_tc.cuh"
+#include "decode_pair.cuh"
+#include "decode_narrow.cuh"
 
 using namespace mla;
 
@@ -43,9 +44,18 @@ TcGemm tc_base(const mla_handle_s* h) {
   return g;
 }
 
+// A tensor-core attention kernel takes this shape: the CTA-pair kernel (128
+// heads, d_c 512, d_r 64) or the few-head kernel (n_h <= 16).
+bool decode_tc_any(const mla_handle_s* h) { return decode_tc_supported(h) || decode_narrow_supported(h); }
+
+// Split-KV chunk count of the tensor-core family for this shape.
+int tc_chunks(const mla_handle_s* h, int batch) {
+  return decode_tc_supported(h) ? decode_tc_chunks(h, batch) : decode_narrow_chunks(h);
+}
+
 int resolve_decode_path(const mla_handle_s* h) {
   if (h->decode_path == MLA_DECODE_SIMT) return MLA_DECODE_SIMT;
-  const bool tc_ok = decode_tc_supported(h);
+  const bool tc_ok = decode_tc_any(h);
   if (h->decode_path == MLA_DECODE_TCGEN05) return tc_ok ? MLA_DECODE_TCGEN05 : -1;
   return tc_ok ? MLA_DECODE_TCGEN05 : MLA_DECODE_SIMT;
 }
@@ -150,7 +160,7 @@ mla_status_t mla_destroy(mla_handle_t h) {
 
 mla_status_t mla_set_decode_path(mla_handle_t h, int32_t path) {
   if (!h || path < MLA_DECODE_AUTO || path > MLA_DECODE_TCGEN05) return MLA_ERR_INVALID_ARG;
-  if (path == MLA_DECODE_TCGEN05 && !decode_tc_supported(h)) return MLA_ERR_UNSUPPORTED;
+  if (path == MLA_DECODE_TCGEN05 && !decode_tc_any(h)) return MLA_ERR_UNSUPPORTED;
   h->decode_path = path;
   return MLA_OK;
 }
@@ -171,6 +181,26 @@ mla_status_t mla_set_proj_path(mla_handle_t h, int32_t path) {
   if (!h || path < MLA_PROJ_AUTO || path > MLA_PROJ_TCGEN05) return MLA_ERR_INVALID_ARG;
   if (path == MLA_PROJ_TCGEN05 && h->cfg.dtype != MLA_BF16) return MLA_ERR_UNSUPPORTED;
   h->proj_path = path;
+  return MLA_OK;
+}
+
+mla_status_t mla_set_kv_norm(mla_handle_t h, const void* weight, float eps) {
+  if (!h || (weight && !aligned16(weight)) || !(eps >= 0.f) || !isfinite(eps)) return MLA_ERR_INVALID_ARG;
+  if (weight && h->cfg.d_c > 1024) return MLA_ERR_UNSUPPORTED;
+  h->kv_norm_weight = weight;
+  h->kv_norm_eps = eps;
+  return MLA_OK;
+}
+
+mla_status_t mla_set_wait_limit(mla_handle_t h, int64_t cycles) {
+  if (!h || cycles < 0) return MLA_ERR_INVALID_ARG;
+  h->wait_cycles = cycles;
+  return MLA_OK;
+}
+
+mla_status_t mla_set_fault_injection(mla_handle_t h, int32_t mode) {
+  if (!h || mode < 0 || mode > 1) return MLA_ERR_INVALID_ARG;
+  h->fault = mode;
   return MLA_OK;
 }
 
@@ -195,6 +225,18 @@ mla_status_t mla_get_device_status(mla_handle_t h, void* stream, int32_t* bits) 
 }
 
 // ------------------------------------------------------------------- S1
+// The kv_norm variant: RMS-normalise the latent of the rows just appended.
+static mla_status_t kv_norm_rows(const mla_handle_s* h, void* cache, const int32_t* tok_seq, const int32_t* tok_pos,
+                                 int n_tokens, int batch, int max_len, cudaStream_t s, int* launches) {
+  if (!h->kv_norm_weight || n_tokens <= 0) return MLA_OK;
+  const mla_config_t& c = h->cfg;
+  if (launch_kv_norm_rows(cache, h->kv_norm_weight, h->kv_norm_eps, tok_seq, tok_pos, n_tokens, batch, max_len,
+                          c.max_pos, c.d_c, c.d_c + c.d_r, c.dtype, s) != cudaSuccess)
+    return MLA_ERR_CUDA;
+  ++*launches;
+  return MLA_OK;
+}
+
 // S1 after argument checks; tok_seq == nullptr sends token n to sequence n.
 static mla_status_t append_impl(mla_handle_t h, const void* x, int32_t n_tokens, const void* W_DKV, const void* W_KR,
                          const int32_t* tok_seq, const int32_t* tok_pos, void* cache, int32_t batch,
@@ -226,6 +268,8 @@ static mla_status_t append_impl(mla_handle_t h, const void* x, int32_t n_tokens,
         if (launch_gemm_tc(gc, h->num_sms, s) != cudaSuccess) return MLA_ERR_CUDA;
         ++launches;
       }
+      if (kv_norm_rows(h, cache, tok_seq, tok_pos, n_tokens, batch, max_len, s, &launches) != MLA_OK)
+        return MLA_ERR_CUDA;
       h->last_launches = launches;
       return MLA_OK;
     }
@@ -259,6 +303,7 @@ static mla_status_t append_impl(mla_handle_t h, const void* x, int32_t n_tokens,
       ++launches;
     }
   }
+  if (kv_norm_rows(h, cache, tok_seq, tok_pos, n_tokens, batch, max_len, s, &launches) != MLA_OK) return MLA_ERR_CUDA;
   h->last_launches = launches;
   return MLA_OK;
 }
@@ -357,9 +402,9 @@ mla_status_t mla_decode_workspace_size(mla_handle_t h, int32_t batch, int32_t ma
   if (!h || !bytes || batch <= 0 || max_len <= 0) return MLA_ERR_INVALID_ARG;
   const mla_config_t& c = h->cfg;
   size_t b = decode_ws_bytes(batch, c.n_h, c.d_c, h->decode_chunks > 0 ? h->decode_chunks : decode_simt_chunks(h));
-  if (decode_tc_supported(h)) {
-    const size_t t =
-        decode_ws_bytes(batch, c.n_h, c.d_c, h->decode_chunks > 0 ? h->decode_chunks : decode_tc_chunks(h, batch));
+  if (decode_tc_any(h)) {
+    const int ch = h->decode_chunks > 0 ? h->decode_chunks : tc_chunks(h, batch);
+    const size_t t = decode_ws_bytes(batch, c.n_h, c.d_c, ch);
     if (t > b) b = t;
   }
   *bytes = b;
@@ -391,11 +436,17 @@ mla_status_t mla_decode_attn(mla_handle_t h, const void* q_abs, const void* cach
   a.scale_log2 = h->scale * 1.4426950408889634f;
   a.status = h->status;
   a.grid_chunks = h->decode_chunks > 0 ? h->decode_chunks
-                                        : (path == MLA_DECODE_TCGEN05 ? decode_tc_chunks(h, batch) : decode_simt_chunks(h));
+                                        : (path == MLA_DECODE_TCGEN05 ? tc_chunks(h, batch) : decode_simt_chunks(h));
+  a.allow_whole = h->decode_chunks == 0;   // a forced chunk count always splits
+  a.wait_cycles = h->wait_cycles;
+  a.fault = h->fault;
   decode_ws_carve(ws, batch, c.n_h, c.d_c, a.grid_chunks, &a.plan, &a.part_o, &a.part_lse);
   int launches = 0;
-  cudaError_t e = path == MLA_DECODE_TCGEN05 ? launch_decode_tc(h, a, s, &launches)
-                                             : launch_decode_simt(a, c.dtype, s, &launches);
+  cudaError_t e;
+  if (path == MLA_DECODE_TCGEN05)
+    e = decode_tc_supported(h) ? launch_decode_tc(h, a, s, &launches) : launch_decode_narrow(h, a, s, &launches);
+  else
+    e = launch_decode_simt(a, c.dtype, s, &launches);
   if (e != cudaSuccess) return MLA_ERR_CUDA;
   h->last_launches = launches;
   return MLA_OK;
@@ -534,6 +585,7 @@ mla_status_t mla_decode_step(mla_handle_t h, const void* x, int32_t batch, const
   mla_status_t st;
   if (tc_front) {
     if (launch_gemm_tc(f, h->num_sms, s) != cudaSuccess) return MLA_ERR_CUDA;
+    if (kv_norm_rows(h, cache, nullptr, pos, batch, batch, max_len, s, &launches) != MLA_OK) return MLA_ERR_CUDA;
     if (launch_gemm_tc(g2, h->num_sms, s) != cudaSuccess) return MLA_ERR_CUDA;
     if (launch_gemm_tc(g4, h->num_sms, s) != cudaSuccess) return MLA_ERR_CUDA;
     launches += 3;

@@ -36,6 +36,28 @@ bool make_tmap_2d_bf16_sw128(CUtensorMap* map, const void* base, uint64_t inner,
   return r == CUDA_SUCCESS;
 }
 
+bool make_tmap_2d_bf16(CUtensorMap* map, const void* base, uint64_t inner, uint64_t outer, uint64_t row_bytes,
+                       uint32_t box_inner, uint32_t box_outer, int swizzle_bytes) {
+  auto fn = encode_fn();
+  if (!fn) return false;
+  CUtensorMapSwizzle sw;
+  switch (swizzle_bytes) {
+    case 128: sw = CU_TENSOR_MAP_SWIZZLE_128B; break;
+    case 64: sw = CU_TENSOR_MAP_SWIZZLE_64B; break;
+    case 32: sw = CU_TENSOR_MAP_SWIZZLE_32B; break;
+    default: return false;
+  }
+  if (box_inner * 2 > (uint32_t)swizzle_bytes) return false;
+  cuuint64_t dims[2] = {inner, outer};
+  cuuint64_t strides[1] = {row_bytes};
+  cuuint32_t box[2] = {box_inner, box_outer};
+  cuuint32_t estr[2] = {1, 1};
+  CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box, estr,
+                  CU_TENSOR_MAP_INTERLEAVE_NONE, sw, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                  CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
 bool make_tmap_2d_f32_sw128(CUtensorMap* map, const void* base, uint64_t inner, uint64_t outer,
                             uint64_t row_bytes, uint32_t box_inner, uint32_t box_outer) {
   auto fn = encode_fn();

@@ -10,6 +10,10 @@ namespace mla {
 // Returns false if the driver rejects the map.
 bool make_tmap_2d_bf16_sw128(CUtensorMap* map, const void* base, uint64_t inner, uint64_t outer,
                              uint64_t row_bytes, uint32_t box_inner, uint32_t box_outer);
+// 2-D bf16 tensor with a chosen swizzle span (32, 64 or 128 bytes; box_inner * 2
+// must not exceed it).
+bool make_tmap_2d_bf16(CUtensorMap* map, const void* base, uint64_t inner, uint64_t outer, uint64_t row_bytes,
+                       uint32_t box_inner, uint32_t box_outer, int swizzle_bytes);
 // The same for fp32 elements (box_inner * 4 <= 128).
 bool make_tmap_2d_f32_sw128(CUtensorMap* map, const void* base, uint64_t inner, uint64_t outer,
                             uint64_t row_bytes, uint32_t box_inner, uint32_t box_outer);

@@ -19,8 +19,11 @@
  *
  * Conventions shared by every call
  *   - All tensor pointers are DEVICE pointers owned by the caller; the library
- *     never frees or keeps them. The only memory the library allocates is made
- *     in mla_create (RoPE table, status word) and freed in mla_destroy.
+ *     never frees or keeps them. The memory the library allocates itself is
+ *     made in mla_create (RoPE table, status word) and freed in mla_destroy,
+ *     plus one fixed 8 MiB scratch array in device global memory that backs
+ *     mla_decode_attn_noalloc (defined in the library, so every GPU that loads
+ *     it holds the array until the process exits).
  *   - Storage dtype of every activation / weight / cache tensor is the handle's
  *     dtype (MLA_BF16: bf16, MLA_F32: fp32). Arithmetic accumulates in fp32.
  *     LSE is always fp32.
@@ -180,7 +183,9 @@ MLA_API mla_status_t mla_decode_attn(mla_handle_t handle, const void* q_abs, con
    do not fit (roughly 4 * n_h * (d_c + 1) * (batch + 1) bytes at the fewest
    splits) return MLA_ERR_WORKSPACE; d_c above 512 returns MLA_ERR_UNSUPPORTED.
    The first call on each device looks up the array's device address (with
-   that device current); make that first call before any stream capture.
+   that device current); make that first call before any stream capture. The
+   address is kept for the life of the process: after cudaDeviceReset on a
+   device, do not call this function on that device again.
    Every call shares the one array, so calls that overlap on the GPU (other
    streams, other host threads on the same device) race and corrupt each
    other's results; serialise them. Out-of-range seqlens are clamped to
@@ -242,6 +247,30 @@ MLA_API mla_status_t mla_set_decode_chunks(mla_handle_t handle, int32_t chunks);
    the CUDA-core one; fp32 layers always use the CUDA-core kernel. */
 typedef enum { MLA_PROJ_AUTO = 0, MLA_PROJ_SIMT = 1, MLA_PROJ_TCGEN05 = 2 } mla_proj_path_t;
 MLA_API mla_status_t mla_set_proj_path(mla_handle_t handle, int32_t path);
+
+/* The kv_norm variant of the append ([MiniMind] §9: kv_norm = RMSNorm over the
+   kv_lora_rank latent, applied before it is cached): with `weight` non-NULL
+   (device [d_c], the handle's dtype, 16-byte aligned, owned by the caller and
+   read by every later append), mla_append_cache and mla_decode_step replace
+   the latent part of each row they append by c / sqrt(mean(c^2) + eps) *
+   weight, computed in fp32 from the stored row (so a bf16 row is rounded
+   twice); the RoPE key is not normalised. NULL (the default) turns it off.
+   Returns MLA_ERR_INVALID_ARG for a misaligned weight or a negative or
+   non-finite eps, MLA_ERR_UNSUPPORTED for d_c above 1024. */
+MLA_API mla_status_t mla_set_kv_norm(mla_handle_t handle, const void* weight, float eps);
+
+/* Failure-detection controls. Every wait inside the tensor-core kernels is
+   bounded: after `cycles` SM clocks without progress (0 restores the default,
+   about 2 s) the kernel stops issuing work, waits for its own copies in flight,
+   frees its TMEM, sets MLA_DEV_TIMEOUT in the status word and returns, leaving
+   the context usable; mla_get_device_status then returns MLA_ERR_TIMEOUT and the
+   call's outputs are void. Returns MLA_ERR_INVALID_ARG for a negative count. */
+MLA_API mla_status_t mla_set_wait_limit(mla_handle_t handle, int64_t cycles);
+/* Test hook for the path above (no GPU fault involved): mode 1 makes the next
+   tensor-core decode-attention calls withhold one internal arrival (a barrier
+   that nothing else completes), so that their bounded wait runs out; mode 0
+   (the default) turns it off. Returns MLA_ERR_INVALID_ARG for other modes. */
+MLA_API mla_status_t mla_set_fault_injection(mla_handle_t handle, int32_t mode);
 
 /* Number of kernel launches the last successful call of each entry point made
    (for launch accounting in benchmarks). */

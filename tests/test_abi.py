@@ -72,6 +72,9 @@ def test_null_handle_is_rejected():
     assert m._c["mla_decode_step"](None, None, 1, *([None] * 8), None, None, None, 1, None, None, 0,
                                    None) == m.MLA_ERR_INVALID_ARG
     assert m._c["mla_set_decode_chunks"](None, 4) == m.MLA_ERR_INVALID_ARG
+    assert m._c["mla_set_wait_limit"](None, 1000) == m.MLA_ERR_INVALID_ARG
+    assert m._c["mla_set_fault_injection"](None, 0) == m.MLA_ERR_INVALID_ARG
+    assert m._c["mla_set_kv_norm"](None, None, 1e-5) == m.MLA_ERR_INVALID_ARG
 
 
 def test_binding_has_every_declared_function():
