@@ -19,12 +19,13 @@
 // fp32 accumulator in registers, O = O * alpha + O_t, so TMEM never needs a
 // rescale and every MMA starts from zero.
 //
-// One CTA per SM streams its chunk of the plan (all sequences' rows laid end
-// to end and cut into equal chunks, as for every decode kernel here) through
-// a ring of 128-row tiles: the latent part as one box of d_c/64 chunks of
+// One CTA per SM streams its chunk of the plan (one whole sequence, or an
+// equal share of all sequences' rows laid end to end, as for every decode
+// kernel here) through a ring of 128-row tiles: the latent part as one box of d_c/64 chunks of
 // 64 columns (128-byte swizzle), the RoPE part as one box of its own
-// (64- or 128-byte swizzle). Warp 0 issues TMA, warp 1 the MMAs (QK of tile
-// g, then PV of tile g-1), warps 2-5 run the online softmax (base 2, lazy
+// (64- or 128-byte swizzle). Warp 0 issues TMA, warp 1 the QK MMAs, warp 2
+// the PV MMAs, and groups of four warps from warp 3 on run the online
+// softmax for four heads each (base 2, lazy
 // reference maximum as in the many-head kernel: it moves only when a tile's
 // maximum rises more than 8 above it), write P, and fold O. A piece that
 // covers a whole sequence writes o_lat/lse, any other piece a partial slot
@@ -49,10 +50,11 @@ constexpr int HPG = 4;                   // heads per softmax warp group (4 warp
 constexpr long long WAIT_CYCLES = 4000000000LL;  // ~2 s
 constexpr float kLn2 = 0.693147180559945309f;
 constexpr float RESCALE_THRESHOLD = 8.0f;
-constexpr int RING_BUDGET = 168 * 1024;
+constexpr int SMEM_LIMIT = 227 * 1024;    // opt-in shared memory per CTA
+constexpr int CTL_RESERVE = 2048;         // the static control block (Ctl), rounded up
 constexpr int MAX_SLOTS = 6;
 constexpr int NSB = 4;                   // S^T buffers in TMEM
-constexpr int NPP = 4;                   // P^T buffers in shared memory
+constexpr int NPP = 3;                   // P^T buffers in shared memory
 constexpr int NOB = 4;                   // O_t^T buffers in TMEM
 constexpr int FOLD = 2;                  // the softmax folds O_t of tile g - FOLD while at tile g
 static_assert(NPP >= FOLD + 1, "a P buffer is rewritten only after the PV that read it was folded");
@@ -77,7 +79,6 @@ struct Shape {
   static constexpr int ROPE_ROW = DR * 2;             // bytes of one row's RoPE part
   static constexpr int ROPE_BYTES = TR * ROPE_ROW;
   static constexpr int SLOT = NCL * LAT_CHUNK + ROPE_BYTES;
-  static constexpr int NSLOT = (RING_BUDGET / SLOT) < MAX_SLOTS ? (RING_BUDGET / SLOT) : MAX_SLOTS;
   static constexpr uint32_t ROPE_LAYOUT = DR == 64 ? 2u : 4u;   // 128- or 64-byte swizzle
   static constexpr int ROPE_SBO = 8 * ROPE_ROW;
   // Q (B operand of QK, K-major): [NCL chunks][16 rows][128 B], then the RoPE part [16 rows][ROPE_ROW]
@@ -86,6 +87,10 @@ struct Shape {
   static constexpr int Q_STRIDE = (Q_BYTES + 1023) / 1024 * 1024;
   // P^T (B operand of PV, K-major): [2 chunks of 64 rows][16 heads][128 B]
   static constexpr int P_BYTES = 2 * NPAD * 128;      // 4 KB
+  // as many ring slots as the rest leaves room for: the ring's depth is what
+  // hides the HBM latency at one CTA per SM
+  static constexpr int RING_BUDGET = SMEM_LIMIT - 1024 - 2 * Q_STRIDE - NPP * P_BYTES - CTL_RESERVE;
+  static constexpr int NSLOT = (RING_BUDGET / SLOT) < MAX_SLOTS ? (RING_BUDGET / SLOT) : MAX_SLOTS;
   static constexpr int RING_OFF = 0;
   static constexpr int Q_OFF = NSLOT * SLOT;           // two query buffers (piece parity)
   static constexpr int P_OFF = Q_OFF + 2 * Q_STRIDE;   // NPP P buffers (tile g in g % NPP)
@@ -100,9 +105,10 @@ struct Shape {
   static_assert(DR == 32 || DR == 64, "RoPE width");
   static_assert(NSLOT >= 3, "ring");
   static_assert(SLOT % 1024 == 0, "slot alignment");
+  static_assert(SMEM_DYN + CTL_RESERVE <= SMEM_LIMIT, "shared memory");
 };
 
-struct Ctl {
+struct Ctl {   // static shared memory: at most CTL_RESERVE bytes
   uint64_t full[MAX_SLOTS], empty[MAX_SLOTS];
   uint64_t q_full[2], q_free[2];
   uint64_t s_full[NSB], s_free[NSB];
@@ -111,10 +117,11 @@ struct Ctl {
   uint32_t tmem_base;
   int abort;
   long long wait_limit;       // cycles before a wait gives up
-  uint64_t mma_done;          // every MMA the issuer made has completed
+  uint64_t mma_done;          // every MMA of both issuers has completed (two arrivals)
   float wmax[2][4][NPAD];     // per tile parity, TMEM lane quarter and head: the tile's maximum
   float wsum[4][NPAD];        // per TMEM lane quarter and head: the piece's softmax sum
 };
+static_assert(sizeof(Ctl) <= CTL_RESERVE, "control block");
 
 // Every wait gives up after ctl.wait_limit cycles, or as soon as another role
 // of this CTA has given up; the first to expire records MLA_DEV_TIMEOUT.
@@ -189,7 +196,7 @@ __device__ __forceinline__ void drain_ring(uint64_t* full, int ring, int issued)
 
 // NGRP softmax groups of 4 warps, each owning HPG heads (n_h <= HPG * NGRP).
 template <int DC, int DR, int NGRP>
-__global__ void __launch_bounds__(64 + 128 * NGRP, 1)
+__global__ void __launch_bounds__(96 + 128 * NGRP, 1)
     decode_narrow_kernel(const __grid_constant__ CUtensorMap map_lat, const __grid_constant__ CUtensorMap map_rope,
                          const __grid_constant__ CUtensorMap map_qlat, const __grid_constant__ CUtensorMap map_qrope,
                          const DecodeArgs a) {
@@ -208,14 +215,14 @@ __global__ void __launch_bounds__(64 + 128 * NGRP, 1)
     for (int i = 0; i < NSB; ++i) { mbar_init(&ctl.s_full[i], 1); mbar_init(&ctl.s_free[i], 4 * NGRP); }
     for (int i = 0; i < NPP; ++i) mbar_init(&ctl.p_full[i], 4 * NGRP);
     for (int i = 0; i < NOB; ++i) { mbar_init(&ctl.o_full[i], 1); mbar_init(&ctl.o_free[i], 4 * NGRP); }
-    mbar_init(&ctl.mma_done, 1);
+    mbar_init(&ctl.mma_done, 2);
     ctl.abort = 0;
     ctl.wait_limit = a.wait_cycles > 0 ? a.wait_cycles : WAIT_CYCLES;
     fence_mbar_init();
   }
   // The padded head rows of Q and P feed only score / output columns that are
   // never read; zero them once so that no stale bits reach the tensor cores.
-  for (int i = threadIdx.x * 16; i < 2 * L::Q_STRIDE + NPP * L::P_BYTES; i += (64 + 128 * NGRP) * 16)
+  for (int i = threadIdx.x * 16; i < 2 * L::Q_STRIDE + NPP * L::P_BYTES; i += (96 + 128 * NGRP) * 16)
     *reinterpret_cast<uint4*>(smem + L::Q_OFF + i) = make_uint4(0, 0, 0, 0);
   fence_proxy_async_smem();
   if (warp == 1) {
@@ -270,115 +277,108 @@ __global__ void __launch_bounds__(64 + 128 * NGRP, 1)
       }
     }
   } else if (warp == 1) {
-    // ------------------------------------------------------------ MMA issuer
-    // Two cursors walk the chunk's tiles in order: QK runs ahead as tiles
-    // land (up to NSB tiles ahead of PV), and the PV of a tile is issued as
-    // soon as the softmax has written its P. Neither waits for the other:
-    // the thread polls both and gives up only when neither has moved for
-    // the wait limit.
+    // ------------------------------------------------------------ QK issuer
+    // S^T of tile g into TMEM buffer g % NSB as soon as the tile has landed
+    // and the softmax has read the buffer's previous tile. QK and PV have an
+    // issuing thread each: a small-N MMA costs its issuing thread about as
+    // long as the tensor core takes to run it, so one thread alone would
+    // leave the tensor core idle between the two streams.
     if (lane == 0) {
       constexpr uint32_t IDESC_QK = idesc_bf16(128, NPAD, false, false);
-      constexpr uint32_t IDESC_PV = idesc_bf16(128, NPAD, true, false);
-      struct Cursor {
-        Pieces it; int seq, t0, t1, r, piece; bool whole, valid;
-        __device__ void start(const int32_t* plan, int B_, int chunk_) {
-          it.init(plan, B_, chunk_);
-          piece = 0;
-          valid = it.next(seq, t0, t1, whole);
-          r = t0;
-        }
-        __device__ void advance() {
-          r += TR;
-          if (r >= t1) {
-            valid = it.next(seq, t0, t1, whole);
-            r = t0;
-            ++piece;
-          }
-        }
-      };
-      Cursor qc, pc;
-      qc.start(a.plan, B, chunk);
-      pc.start(a.plan, B, chunk);
-      int gq = 0, gp = 0;
+      // descriptors built once; each MMA adds a byte offset (>> 4) to the start address field
+      const uint64_t ring_k = sdesc(sbase + L::RING_OFF, 16, 1024, 2);
+      const uint64_t ring_r = sdesc(sbase + L::RING_OFF, 16, L::ROPE_SBO, L::ROPE_LAYOUT);
+      const uint64_t q_k = sdesc(sbase + L::Q_OFF, 16, 1024, 2);
+      const uint64_t q_r = sdesc(sbase + L::Q_OFF, 16, L::ROPE_SBO, L::ROPE_LAYOUT);
+      Pieces it;
+      it.init(a.plan, B, chunk);
+      int seq, t0, t1;
+      bool whole;
+      int piece = 0, g = 0;
       bool ok = true;
-      volatile int* ab = reinterpret_cast<volatile int*>(&ctl.abort);
-      long long last = clock64();
-      while (pc.valid && ok) {
-        bool moved = false;
-        if (qc.valid && gq - gp < NSB) {
-          const int qb = qc.piece & 1, sl = gq % L::NSLOT, sb = gq % NSB;
-          bool ready = qc.r != qc.t0 || mbar_test(&ctl.q_full[qb], (qc.piece >> 1) & 1);
-          ready = ready && mbar_test(&ctl.full[sl], (gq / L::NSLOT) & 1);
-          ready = ready && (gq < NSB || mbar_test(&ctl.s_free[sb], ((gq / NSB) - 1) & 1));
-          if (ready) {
-            tc_fence_after();
-            const uint32_t qs = sbase + L::Q_OFF + qb * L::Q_STRIDE;
-            const uint32_t slot = sbase + L::RING_OFF + sl * L::SLOT;
-            const uint32_t d = tbase + L::S_COL + sb * NPAD;
-            // S^T = C . Q^T over the latent chunks, then the RoPE part
+      while (ok && it.next(seq, t0, t1, whole)) {
+        const int qb = piece & 1;
+        ok = wait_or_abort(&ctl.q_full[qb], (piece >> 1) & 1, ctl, a.status);
+        for (int r = t0; r < t1 && ok; r += TR, ++g) {
+          const int sl = g % L::NSLOT, sb = g % NSB;
+          ok = wait_or_abort(&ctl.full[sl], (g / L::NSLOT) & 1, ctl, a.status) &&
+               (g < NSB || wait_or_abort(&ctl.s_free[sb], ((g / NSB) - 1) & 1, ctl, a.status));
+          if (!ok) break;
+          tc_fence_after();
+          const uint32_t d = tbase + L::S_COL + sb * NPAD;
+          const uint64_t a0 = ring_k + (uint64_t)((sl * L::SLOT) >> 4);
+          const uint64_t b0 = q_k + (uint64_t)((qb * L::Q_STRIDE) >> 4);
+          // S^T = C . Q^T over the latent chunks, then the RoPE part
 #pragma unroll
-            for (int c = 0; c < L::NCL; ++c)
+          for (int c = 0; c < L::NCL; ++c)
 #pragma unroll
-              for (int k = 0; k < 4; ++k)
-                mma_bf16(d, sdesc(slot + c * L::LAT_CHUNK + k * 32, 16, 1024, 2),
-                         sdesc(qs + c * L::QL_CHUNK + k * 32, 16, 1024, 2), IDESC_QK, (c > 0 || k > 0) ? 1u : 0u);
+            for (int k = 0; k < 4; ++k)
+              mma_bf16(d, a0 + (uint64_t)((c * L::LAT_CHUNK + k * 32) >> 4),
+                       b0 + (uint64_t)((c * L::QL_CHUNK + k * 32) >> 4), IDESC_QK, (c > 0 || k > 0) ? 1u : 0u);
+          const uint64_t ar = ring_r + (uint64_t)((sl * L::SLOT + L::NCL * L::LAT_CHUNK) >> 4);
+          const uint64_t br = q_r + (uint64_t)((qb * L::Q_STRIDE + L::NCL * L::QL_CHUNK) >> 4);
 #pragma unroll
-            for (int k = 0; k < DR / 16; ++k)
-              mma_bf16(d, sdesc(slot + L::NCL * L::LAT_CHUNK + k * 32, 16, L::ROPE_SBO, L::ROPE_LAYOUT),
-                       sdesc(qs + L::NCL * L::QL_CHUNK + k * 32, 16, L::ROPE_SBO, L::ROPE_LAYOUT), IDESC_QK, 1u);
-            mma_commit(&ctl.s_full[sb]);
-            // the piece's last QK: its query buffer may be refilled
-            if (qc.r + TR >= qc.t1) mma_commit(&ctl.q_free[qb]);
-            qc.advance();
-            ++gq;
-            moved = true;
-          }
+          for (int k = 0; k < DR / 16; ++k)
+            mma_bf16(d, ar + (uint64_t)((k * 32) >> 4), br + (uint64_t)((k * 32) >> 4), IDESC_QK, 1u);
+          mma_commit(&ctl.s_full[sb]);
         }
-        if (gp < gq) {
-          const int pb = gp % NPP, ob = gp % NOB, sl = gp % L::NSLOT;
-          bool ready = mbar_test(&ctl.p_full[pb], (gp / NPP) & 1);
-          ready = ready && (gp < NOB || mbar_test(&ctl.o_free[ob], ((gp / NOB) - 1) & 1));
-          if (ready) {
-            tc_fence_after();
-            // O_t^T[ob] = V^T . P^T over the tile's valid rows (16 per MMA)
-            const uint32_t slot = sbase + L::RING_OFF + sl * L::SLOT;
-            const uint32_t pbase = sbase + L::P_OFF + pb * L::P_BYTES;
-            const int ksteps = (min(TR, pc.t1 - pc.r) + 15) >> 4;
-#pragma unroll
-            for (int mb = 0; mb < L::NB; ++mb) {
-              const uint32_t d = tbase + L::O_COL + (uint32_t)(ob * L::NB + mb) * NPAD;
-              const uint64_t a0 = sdesc(slot + mb * 2 * L::LAT_CHUNK, L::LAT_CHUNK, 1024, 2);
-              for (int kk = 0; kk < ksteps; ++kk) {
-                const uint64_t ad = a0 + (uint64_t)((kk * 16 * 128) >> 4);
-                const uint64_t bd = sdesc(pbase + (kk >> 2) * (NPAD * 128) + (kk & 3) * 32, 16, 1024, 2);
-                mma_bf16(d, ad, bd, IDESC_PV, kk > 0 ? 1u : 0u);
-              }
-            }
-            mma_commit(&ctl.o_full[ob]);
-            mma_commit(&ctl.empty[sl]);   // the tile's slot: its QK and PV are done
-            pc.advance();
-            ++gp;
-            moved = true;
-          }
-        }
-        if (moved) {
-          last = clock64();
-        } else if (*ab || clock64() - last > ctl.wait_limit) {
-          if (!*ab) atomicOr(a.status, MLA_DEV_TIMEOUT);
-          *ab = 1;
-          ok = false;
-        }
+        // the piece's last QK: its query buffer may be refilled
+        if (ok) mma_commit(&ctl.q_free[qb]);
+        ++piece;
       }
       // nothing of this CTA's reaches the tensor cores after it moves on
       mma_commit(&ctl.mma_done);
       mbar_wait(&ctl.mma_done, 0, WAIT_CYCLES / 8);
     }
+  } else if (warp == 2) {
+    // ------------------------------------------------------------ PV issuer
+    // O_t^T of tile g into TMEM buffer g % NOB once the softmax has written
+    // P^T(g) and folded the buffer's previous tile; the tile's ring slot is
+    // released when this PV completes (its QK completed before P existed).
+    if (lane == 0) {
+      constexpr uint32_t IDESC_PV = idesc_bf16(128, NPAD, true, false);
+      const uint64_t ring_v = sdesc(sbase + L::RING_OFF, L::LAT_CHUNK, 1024, 2);
+      const uint64_t p_k = sdesc(sbase + L::P_OFF, 16, 1024, 2);
+      Pieces it;
+      it.init(a.plan, B, chunk);
+      int seq, t0, t1;
+      bool whole;
+      int g = 0;
+      bool ok = true;
+      while (ok && it.next(seq, t0, t1, whole)) {
+        for (int r = t0; r < t1 && ok; r += TR, ++g) {
+          const int pb = g % NPP, ob = g % NOB, sl = g % L::NSLOT;
+          ok = wait_or_abort(&ctl.p_full[pb], (g / NPP) & 1, ctl, a.status) &&
+               (g < NOB || wait_or_abort(&ctl.o_free[ob], ((g / NOB) - 1) & 1, ctl, a.status));
+          if (!ok) break;
+          tc_fence_after();
+          // O_t^T[ob] = V^T . P^T over the tile's valid rows, 16 per MMA
+          const int ksteps = (min(TR, t1 - r) + 15) >> 4;
+          const uint64_t a0 = ring_v + (uint64_t)((sl * L::SLOT) >> 4);
+          const uint64_t b0 = p_k + (uint64_t)((pb * L::P_BYTES) >> 4);
+#pragma unroll
+          for (int mb = 0; mb < L::NB; ++mb) {
+            const uint32_t d = tbase + L::O_COL + (uint32_t)(ob * L::NB + mb) * NPAD;
+#pragma unroll
+            for (int kk = 0; kk < TR / 16; ++kk)
+              if (kk < ksteps)
+                mma_bf16(d, a0 + (uint64_t)((mb * 2 * L::LAT_CHUNK + kk * 16 * 128) >> 4),
+                         b0 + (uint64_t)(((kk >> 2) * (NPAD * 128) + (kk & 3) * 32) >> 4), IDESC_PV,
+                         kk > 0 ? 1u : 0u);
+          }
+          mma_commit(&ctl.o_full[ob]);
+          mma_commit(&ctl.empty[sl]);   // the tile's slot: its QK and PV are done
+        }
+      }
+      mma_commit(&ctl.mma_done);
+      mbar_wait(&ctl.mma_done, 0, WAIT_CYCLES / 8);
+    }
   } else {
-    // ------------------------------------------------------------ softmax warps 2 .. 1 + 4 NGRP
-    // Group grp (warps 2+4grp .. 5+4grp) owns heads h0 .. h0+3: the online
+    // ------------------------------------------------------------ softmax warps 3 .. 2 + 4 NGRP
+    // Group grp (warps 3+4grp .. 6+4grp) owns heads h0 .. h0+3: the online
     // softmax of different heads shares nothing, so each group keeps its own
     // running maxima, sums and O columns and meets only its own four warps.
-    const int grp = (warp - 2) >> 2;
+    const int grp = (warp - 3) >> 2;
     const int h0 = grp * HPG;
     const int quarter = warp & 3;
     const int t = quarter * 32 + lane;                // TMEM lane: cache row of S, latent column of O
@@ -603,7 +603,7 @@ cudaError_t launch_typed(const DecodeArgs& a, cudaStream_t s) {
     if (e != cudaSuccess) return e;
     attr_set = true;
   }
-  LaunchCfg lc(dim3((unsigned)a.grid_chunks), dim3(64 + 128 * NGRP), L::SMEM_DYN, s);
+  LaunchCfg lc(dim3((unsigned)a.grid_chunks), dim3(96 + 128 * NGRP), L::SMEM_DYN, s);
   cudaError_t e = cudaLaunchKernelEx(&lc.cfg, decode_narrow_kernel<DC, DR, NGRP>, map_lat, map_rope, map_qlat,
                                      map_qrope, a);
   if (e != cudaSuccess) return e;
