@@ -179,6 +179,37 @@ def output_projection(o_lat, W_UV, W_O, n_h: int, d_h: int, return_o: bool = Fal
 
 
 # --------------------------------------------------------------------------
+# The pre-merged weight forms ([MLA] §4)
+# --------------------------------------------------------------------------
+def premerged_query_weights(W_UQ, W_UK, n_h: int, d_h: int):
+    """W_QK [n_h, d_c, d_cq] with W_QK_i = W_UK_i^T W_UQ_i.
+
+    [MLA] §4: W^{UQ T} W^{UK} can be merged ahead of time, so the content
+    score is c_Q^T (W_UQ_i^T W_UK_i) c_KV. Stored as the map that takes c_Q
+    straight to q~_i = W_QK_i c_Q.
+    """
+    W_UQ = _f64(W_UQ)
+    W_UK = _f64(W_UK)
+    d_cq, d_c = W_UQ.shape[1], W_UK.shape[1]
+    UQ = W_UQ.reshape(n_h, d_h, d_cq)
+    UK = W_UK.reshape(n_h, d_h, d_c)
+    return np.stack([UK[i].T @ UQ[i] for i in range(n_h)])
+
+
+def premerged_output_weights(W_UV, W_O, n_h: int, d_h: int):
+    """W_OUV [d, n_h * d_c] whose column block i is W_O_i W_UV_i.
+
+    [MLA] §4, the per-head u_t formula u = sum_i W_O_i W_UV_i o_lat_i: with the
+    product merged ahead of time u = W_OUV [o_lat_1; ...; o_lat_nh].
+    """
+    W_UV = _f64(W_UV)
+    W_O = _f64(W_O)
+    d_c = W_UV.shape[1]
+    UV = W_UV.reshape(n_h, d_h, d_c)
+    return np.concatenate([W_O[:, i * d_h:(i + 1) * d_h] @ UV[i] for i in range(n_h)], axis=1)
+
+
+# --------------------------------------------------------------------------
 # The whole step, two ways
 # --------------------------------------------------------------------------
 def decode_absorbed(h_ctx_list, h_new, W, n_h, d_h, d_r, base, pos=None, kv_norm_weight=None,

@@ -578,3 +578,92 @@ def test_planted_rms_norm_mistakes_are_caught(mutant):
 
 def test_planted_kv_norm_row_mistake_is_caught():
     assert not check_cache_rows_kv_norm(_cache_rows_norm_whole_row)
+
+
+# ---------------------------------------------------------------------------
+# pins: the pre-merged weight forms (MLA page §4)
+# ---------------------------------------------------------------------------
+def check_premerged_query(fn):
+    """Brute-force triple loop on tiny shapes; the merged map reaches the
+    two-step absorbed query; each head's merged map has rank <= d_h."""
+    rng = np.random.default_rng(31)
+    n_h, d_h, d_c, d_cq = 3, 2, 5, 4
+    W_UQ = rng.standard_normal((n_h * d_h, d_cq))
+    W_UK = rng.standard_normal((n_h * d_h, d_c))
+    got = np.asarray(fn(W_UQ, W_UK, n_h, d_h))
+    if got.shape != (n_h, d_c, d_cq):
+        return False
+    ok = True
+    for i in range(n_h):
+        for c in range(d_c):
+            for q in range(d_cq):
+                ref = sum(W_UK[i * d_h + k, c] * W_UQ[i * d_h + k, q] for k in range(d_h))
+                ok &= abs(got[i, c, q] - ref) <= 1e-12
+    # W_QK_i c_Q equals the absorbed query's latent part q~_i = W_UK_i^T (W_UQ_i c_Q)
+    m = MICRO
+    W, _, h_new = micro_inputs(32, L=3)
+    q_abs, parts = O.absorbed_query(h_new, W["W_DQ"], W["W_UQ"], W["W_QR"], W["W_UK"], np.array([3]),
+                                    m["n_h"], m["d_h"], m["d_r"], 10000.0, return_parts=True)
+    WQK = fn(W["W_UQ"], W["W_UK"], m["n_h"], m["d_h"])
+    ok &= np.allclose(np.einsum("icq,bq->bic", WQK, parts["c_Q"]), q_abs[..., :m["d_c"]], rtol=1e-12, atol=1e-12)
+    W_UQ = rng.standard_normal((2 * 3, 9))
+    W_UK = rng.standard_normal((2 * 3, 8))
+    for Wi in fn(W_UQ, W_UK, 2, 3):
+        sv = np.linalg.svd(Wi, compute_uv=False)
+        ok &= bool(np.all(sv[3:] <= 1e-10 * sv[0]))
+    return bool(ok)
+
+
+def check_premerged_output(fn):
+    """Brute-force loop on tiny shapes; the merged map reaches the two-step
+    output projection."""
+    rng = np.random.default_rng(33)
+    n_h, d_h, d_c, d = 3, 2, 4, 5
+    W_UV = rng.standard_normal((n_h * d_h, d_c))
+    W_O = rng.standard_normal((d, n_h * d_h))
+    got = np.asarray(fn(W_UV, W_O, n_h, d_h))
+    if got.shape != (d, n_h * d_c):
+        return False
+    ok = True
+    for r in range(d):
+        for i in range(n_h):
+            for c in range(d_c):
+                ref = sum(W_O[r, i * d_h + k] * W_UV[i * d_h + k, c] for k in range(d_h))
+                ok &= abs(got[r, i * d_c + c] - ref) <= 1e-12
+    o_lat = rng.standard_normal((2, n_h, d_c))
+    ok &= np.allclose(o_lat.reshape(2, -1) @ got.T, O.output_projection(o_lat, W_UV, W_O, n_h, d_h),
+                      rtol=1e-12, atol=1e-12)
+    return bool(ok)
+
+
+def test_premerged_query_weights():
+    assert check_premerged_query(O.premerged_query_weights)
+
+
+def test_premerged_output_weights():
+    assert check_premerged_output(O.premerged_output_weights)
+
+
+def _premerged_query_transposed(W_UQ, W_UK, n_h, d_h):
+    # W_UQ_i^T W_UK_i, the score's bilinear form, instead of the map applied to c_Q
+    return np.transpose(O.premerged_query_weights(W_UQ, W_UK, n_h, d_h), (0, 2, 1))
+
+
+def _premerged_query_head_mixed(W_UQ, W_UK, n_h, d_h):
+    W = O.premerged_query_weights(W_UQ, W_UK, n_h, d_h)
+    return np.roll(W, 1, axis=0)
+
+
+def _premerged_output_blocks_swapped(W_UV, W_O, n_h, d_h):
+    W = O.premerged_output_weights(W_UV, W_O, n_h, d_h)
+    d_c = np.asarray(W_UV).shape[1]
+    return np.concatenate([W[:, d_c:2 * d_c], W[:, :d_c], W[:, 2 * d_c:]], axis=1)
+
+
+@pytest.mark.parametrize("mutant", [_premerged_query_transposed, _premerged_query_head_mixed])
+def test_planted_premerged_query_mistakes_are_caught(mutant):
+    assert not check_premerged_query(mutant)
+
+
+def test_planted_premerged_output_mistake_is_caught():
+    assert not check_premerged_output(_premerged_output_blocks_swapped)
