@@ -201,14 +201,13 @@ def attention_workloads(device, peaks, iters: int = 20):
             o = torch.empty((B, shp.n_h, shp.d_c), dtype=torch.bfloat16, device=device)
             lse = torch.empty((B, shp.n_h), dtype=torch.float32, device=device)
             sl = torch.as_tensor(seqlens).to(device)
-            flush = torch.empty(256 << 20, dtype=torch.uint8, device=device) if B * max_len * shp.D * 2 < (256 << 20) \
-                else None
+            flush = L2Flush(device) if B * max_len * shp.D * 2 < (256 << 20) else None
             for _ in range(3):
                 M.mla_decode_attn(h, q, cache, B, max_len, sl, o, lse, ws, ws.numel())
             evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(iters)]
             for e0, e1 in evs:
                 if flush is not None:
-                    flush.fill_(1)   # the cache is smaller than two L2s: start each call cold
+                    flush()   # the cache is smaller than two L2s: start each call cold
                 e0.record()
                 M.mla_decode_attn(h, q, cache, B, max_len, sl, o, lse, ws, ws.numel())
                 e1.record()
@@ -223,7 +222,8 @@ def attention_workloads(device, peaks, iters: int = 20):
             r = roofline_of(nbytes, flops, us * 1e-6, peaks)
             r.update({"attn_us": round(us, 2), "GBps": round(nbytes / us / 1e3, 1), "cache_bytes": nbytes,
                       "tokens_per_s": round(B / (us * 1e-6), 1), "batch": B, "rows": rows,
-                      "l2": "flushed before each call" if flush is not None else "cache larger than L2",
+                      "l2": "flushed before each call (256 MB write, then 256 MB read)" if flush is not None
+                      else "cache larger than L2",
                       "decode_path": {M.MLA_DECODE_SIMT: "simt", M.MLA_DECODE_TCGEN05: "tcgen05"}[
                           M.mla_get_decode_path(h)]})
             if name == "v2_ragged":
@@ -237,6 +237,57 @@ def attention_workloads(device, peaks, iters: int = 20):
             del cache
             torch.cuda.empty_cache()
     return out
+
+
+def premerged_comparison(M, dec, shp, h_new, pos, device, iters: int = 15):
+    """S2 and S4/S5 two ways on the benchmark's batch: the two-step factors
+    (W_UQ then W_UK^T; W_UV then W_O) against the pre-merged maps W_QK and
+    W_OUV. L2 is flushed (L2Flush) before every timed call, as in the step,
+    where each weight byte is read once."""
+    import torch
+    B = shp.batch
+    dt = torch.bfloat16
+    W_QK = torch.empty((shp.n_h, shp.d_c, shp.d_cq), dtype=dt, device=device)
+    W_OUV = torch.empty((shp.d, shp.n_h * shp.d_c), dtype=dt, device=device)
+    M.mla_premerge_query_weights(dec.handle, dec.W["W_UQ"], dec.W["W_UK"], W_QK)
+    M.mla_premerge_output_weights(dec.handle, dec.W["W_UV"], dec.W["W_O"], W_OUV)
+    flush = L2Flush(device)
+    stream = torch.cuda.current_stream()
+
+    def timed(fn):
+        for _ in range(3):
+            fn()
+        ts = []
+        for _ in range(iters):
+            flush()
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+            fn()
+            e1.record(stream)
+            torch.cuda.synchronize()
+            ts.append(e0.elapsed_time(e1) * 1e3)
+        return round(statistics.median(ts), 2), M.mla_last_launch_count(dec.handle)
+
+    W = dec.W
+    a2, l_a2 = timed(lambda: M.mla_absorb_q(dec.handle, h_new, B, W["W_DQ"], W["W_UQ"], W["W_QR"], W["W_UK"], pos,
+                                            dec.q_abs, dec.ws, dec.ws.numel()))
+    a1, l_a1 = timed(lambda: M.mla_absorb_q_premerged(dec.handle, h_new, B, W["W_DQ"], W_QK, W["W_QR"], pos,
+                                                      dec.q_abs, dec.ws, dec.ws.numel()))
+    o2, l_o2 = timed(lambda: M.mla_out_proj(dec.handle, dec.o_lat, B, W["W_UV"], W["W_O"], dec.u, dec.ws,
+                                            dec.ws.numel()))
+    o1, l_o1 = timed(lambda: M.mla_out_proj_premerged(dec.handle, dec.o_lat, B, W_OUV, dec.u))
+    nb = lambda *ts: round(sum(t.numel() * 2 for t in ts) / 1e6, 1)
+    res = {
+        "batch": B,
+        "absorb_two_step": {"us": a2, "launches": l_a2, "weight_MB": nb(W["W_DQ"], W["W_UQ"], W["W_QR"], W["W_UK"])},
+        "absorb_premerged": {"us": a1, "launches": l_a1, "weight_MB": nb(W["W_DQ"], W_QK, W["W_QR"])},
+        "out_proj_two_step": {"us": o2, "launches": l_o2, "weight_MB": nb(W["W_UV"], W["W_O"])},
+        "out_proj_premerged": {"us": o1, "launches": l_o1, "weight_MB": nb(W_OUV)},
+        "l2": "flushed before every call (256 MB write, then 256 MB read)",
+    }
+    del W_QK, W_OUV, flush
+    torch.cuda.empty_cache()
+    return res
 
 
 def h_chunks(M, h, B, max_len, device):
@@ -527,6 +578,7 @@ def run_ours(args, rank, world, local_rank):
     }
     if world == 1 and not args.no_workloads:
         out["attention_workloads"] = attention_workloads(device, peaks)
+        out["premerged_comparison"] = premerged_comparison(M, dec, shp, h_new, pos, device)
     if world == 1 and not args.no_cpu_baseline:
         import mla_synth as S
 

@@ -92,6 +92,10 @@ _c = {
     "mla_set_wait_limit": _sig("mla_set_wait_limit", [_P, ctypes.c_int64]),
     "mla_set_kv_norm": _sig("mla_set_kv_norm", [_P, _P, ctypes.c_float]),
     "mla_set_fault_injection": _sig("mla_set_fault_injection", [_P, _I]),
+    "mla_premerge_query_weights": _sig("mla_premerge_query_weights", [_P, _P, _P, _P, _P]),
+    "mla_premerge_output_weights": _sig("mla_premerge_output_weights", [_P, _P, _P, _P, _P]),
+    "mla_absorb_q_premerged": _sig("mla_absorb_q_premerged", [_P, _P, _I, _P, _P, _P, _P, _P, _P, _S, _P]),
+    "mla_out_proj_premerged": _sig("mla_out_proj_premerged", [_P, _P, _I, _P, _P, _P]),
 }
 
 
@@ -186,6 +190,28 @@ def mla_out_proj_workspace_size(handle, batch) -> int:
 def mla_out_proj(handle, o_lat, batch, W_UV, W_O, u, ws, ws_bytes, stream=None):
     _check(_c["mla_out_proj"](handle, _ptr(o_lat), batch, _ptr(W_UV), _ptr(W_O), _ptr(u), _ptr(ws), ws_bytes,
                               _stream(stream)), "mla_out_proj")
+
+
+def mla_premerge_query_weights(handle, W_UQ, W_UK, W_QK, stream=None):
+    """W_QK [n_h, d_c, d_cq] = W_UK_i^T W_UQ_i per head (see include/mla.h)."""
+    _check(_c["mla_premerge_query_weights"](handle, _ptr(W_UQ), _ptr(W_UK), _ptr(W_QK), _stream(stream)),
+           "mla_premerge_query_weights")
+
+
+def mla_premerge_output_weights(handle, W_UV, W_O, W_OUV, stream=None):
+    """W_OUV [d, n_h * d_c], column block i = W_O_i W_UV_i (see include/mla.h)."""
+    _check(_c["mla_premerge_output_weights"](handle, _ptr(W_UV), _ptr(W_O), _ptr(W_OUV), _stream(stream)),
+           "mla_premerge_output_weights")
+
+
+def mla_absorb_q_premerged(handle, x, batch, W_DQ, W_QK, W_QR, pos, q_abs, ws, ws_bytes, stream=None):
+    _check(_c["mla_absorb_q_premerged"](handle, _ptr(x), batch, _ptr(W_DQ), _ptr(W_QK), _ptr(W_QR), _ptr(pos),
+                                        _ptr(q_abs), _ptr(ws), ws_bytes, _stream(stream)), "mla_absorb_q_premerged")
+
+
+def mla_out_proj_premerged(handle, o_lat, batch, W_OUV, u, stream=None):
+    _check(_c["mla_out_proj_premerged"](handle, _ptr(o_lat), batch, _ptr(W_OUV), _ptr(u), _stream(stream)),
+           "mla_out_proj_premerged")
 
 
 def mla_decode_step_workspace_size(handle, batch, max_len) -> int:

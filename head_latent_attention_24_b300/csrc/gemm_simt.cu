@@ -92,6 +92,8 @@ __global__ void __launch_bounds__(NT) gemm_simt_kernel(const GemmArgs a) {
     float v = Cs[n][m];
     if (a.epi == EPI_STORE) {
       out[gn * a.ldo + gm] = from_f32<T>(v);
+    } else if (a.epi == EPI_SEGS) {
+      out[gn * a.ldo + (gm / a.seg_len) * a.seg_stride + a.seg_off + gm % a.seg_len] = from_f32<T>(v);
     } else if (a.epi == EPI_ROPE_SEGS) {
       const int half = a.d_r / 2;
       const int seg = gm / a.d_r, j = gm % a.d_r;

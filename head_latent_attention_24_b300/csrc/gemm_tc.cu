@@ -59,7 +59,7 @@ struct Params {
   int n_tile, nstage, stage_bytes, splits, kstages;
   uint32_t tmem_cols, idesc;
   int epi[3]; void* out[3]; long long ldo[3], bo[3];
-  long long seg_stride[3]; int seg_off[3];
+  long long seg_stride[3]; int seg_off[3]; int seg_len[3];
   const float* rope_cos; const float* rope_sin; int d_r; int max_pos;
   const int32_t* pos;
   const int32_t* tok_seq; const int32_t* tok_pos; int cache_batch; int max_len; int d_c; int row_width;
@@ -305,6 +305,10 @@ __global__ void __launch_bounds__(NTHREADS, 2)
         __nv_bfloat16* dst;
         if (epi == EPI_STORE) {
           dst = out + z * bo + gn * ldo + p.col0[seg] + mb;
+        } else if (epi == EPI_SEGS) {
+          // 8 rows inside one segment (seg_len % 8 == 0)
+          const int sl = p.seg_len[seg];
+          dst = out + gn * ldo + (mb / sl) * p.seg_stride[seg] + p.seg_off[seg] + mb % sl;
         } else if (epi == EPI_ROPE_SEGS) {
           // 8 rows of one rotated segment, all in one half of it (d_r % 16 == 0)
           const int half = p.d_r / 2;
@@ -410,7 +414,8 @@ bool gemm_tc_shape_ok(const TcGemm& g) {
     if (e == EPI_ROPE_SEGS || e == EPI_APPEND) {
       if (g.d_r <= 0 || (BM % g.d_r) || (g.d_r % 16)) return false;
     }
-    if (e == EPI_ROPE_SEGS && ((g.seg_stride[s] % 8) || (g.seg_off[s] % 8))) return false;
+    if ((e == EPI_ROPE_SEGS || e == EPI_SEGS) && ((g.seg_stride[s] % 8) || (g.seg_off[s] % 8))) return false;
+    if (e == EPI_SEGS && (g.seg_len[s] <= 0 || (g.seg_len[s] % 8) || g.Z != 1)) return false;
     if (e == EPI_APPEND) {
       if ((g.row_width % 8) || (g.d_c % 8)) return false;
       // a cache segment is either inside the latent columns or exactly the rotated ones
@@ -418,7 +423,7 @@ bool gemm_tc_shape_ok(const TcGemm& g) {
       const bool rope = g.col0[s] == g.d_c && g.rows[s] == g.d_r;
       if (!latent && !rope) return false;
     }
-    if (e != EPI_STORE && e != EPI_ROPE_SEGS && e != EPI_APPEND) return false;
+    if (e != EPI_STORE && e != EPI_ROPE_SEGS && e != EPI_APPEND && e != EPI_SEGS) return false;
   }
   return true;
 }
@@ -437,6 +442,7 @@ cudaError_t launch_gemm_tc(const TcGemm& g, int num_sms, cudaStream_t s) {
     p.bo[sg] = on ? g.bo[sg] : 0;
     p.seg_stride[sg] = on ? g.seg_stride[sg] : 0;
     p.seg_off[sg] = on ? g.seg_off[sg] : 0;
+    p.seg_len[sg] = on ? g.seg_len[sg] : 0;
     p.mstart[sg + 1] = p.mstart[sg] + (on ? (g.rows[sg] + BM - 1) / BM : 0);
   }
   p.mtiles_total = p.mstart[3];
@@ -455,12 +461,15 @@ cudaError_t launch_gemm_tc(const TcGemm& g, int num_sms, cudaStream_t s) {
   num_sms *= per_sm;
 
   // Tiles per CTA: more than one only when the tiles outnumber the SMs and
-  // split-K is therefore off (one segment; the tiles' accumulators fit TMEM).
+  // split-K is therefore off (the tiles' accumulators fit TMEM, and no CTA's
+  // tiles straddle two segments).
   int mt = 1;
   const long long tiles1 = (long long)p.mtiles_total * n_tiles * g.Z;
-  if (tiles1 > num_sms && g.nseg == 1 && g.epi[0] == EPI_STORE) {
+  bool mt_ok = true;
+  for (int sg = 0; sg < g.nseg; ++sg) mt_ok = mt_ok && g.epi[sg] != EPI_APPEND;
+  if (tiles1 > num_sms && mt_ok) {
     for (int c = 2; c <= MAX_MT; c *= 2)
-      if (p.mtiles_total % c == 0 && c * p.n_tile <= 512) {
+      if (p.mtiles_total % c == 0 && p.mstart[1] % c == 0 && p.mstart[2] % c == 0 && c * p.n_tile <= 512) {
         mt = c;
         if (tiles1 / c <= num_sms) break;
       }

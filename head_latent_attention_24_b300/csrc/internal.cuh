@@ -88,6 +88,8 @@ enum Epilogue {
   EPI_ROPE_SEGS = 1,  // columns form segments of width d_r; RoPE at pos[n];
                       // out[n*ldo + (m/d_r)*seg_stride + seg_off + m%d_r]
   EPI_APPEND = 2,     // cache row (tok_seq[n], tok_pos[n]); columns >= d_c get RoPE
+  EPI_SEGS = 3,       // columns form segments of width seg_len, stored as they are:
+                      // out[n*ldo + (m/seg_len)*seg_stride + seg_off + m%seg_len]
 };
 
 struct GemmArgs {
@@ -100,6 +102,7 @@ struct GemmArgs {
   const float* rope_cos; const float* rope_sin; int d_r; int max_pos;
   const int32_t* pos;          // EPI_ROPE_SEGS: position of row n
   long long seg_stride; int seg_off;
+  int seg_len;                 // EPI_SEGS: segment width
   // append
   const int32_t* tok_seq; const int32_t* tok_pos; int cache_batch; int max_len; int d_c; int row_width;
   int32_t* status;
@@ -120,7 +123,8 @@ struct TcGemm {
   int col0[3];                 // first output column of each segment
   int epi[3];                  // epilogue of each segment
   void* out[3]; long long ldo[3], bo[3];
-  long long seg_stride[3]; int seg_off[3];   // EPI_ROPE_SEGS output layout
+  long long seg_stride[3]; int seg_off[3];   // EPI_ROPE_SEGS / EPI_SEGS output layout
+  int seg_len[3];                            // EPI_SEGS segment width
   long long ldw, bw;           // element stride between W rows; between batches
   int w_transposed;            // W'[m, k] = W[k*ldw + m] (stored [K rows][M cols])
   const void* x; long long ldx, bx;
@@ -171,6 +175,12 @@ cudaError_t launch_decode_simt(const DecodeArgs& a, int dtype, cudaStream_t s, i
 cudaError_t launch_decode_combine(const DecodeArgs& a, int dtype, cudaStream_t s);
 
 // RMSNorm of the latent part of appended cache rows (kv_norm variant).
+// Pre-merged weight forms (setup, once per set of weights): W_QK_i = W_UK_i^T W_UQ_i
+// into W_QK [n_h, d_c, d_cq]; W_OUV[:, i d_c:(i+1) d_c] = W_O_i W_UV_i into W_OUV [d, n_h d_c].
+cudaError_t launch_premerge_query(const void* W_UQ, const void* W_UK, void* W_QK, int n_h, int d_h, int d_c,
+                                  int d_cq, int dtype, cudaStream_t s);
+cudaError_t launch_premerge_output(const void* W_UV, const void* W_O, void* W_OUV, int n_h, int d_h, int d_c,
+                                   int d, int dtype, cudaStream_t s);
 cudaError_t launch_kv_norm_rows(void* cache, const void* weight, float eps, const int32_t* tok_seq,
                                 const int32_t* tok_pos, int n_tokens, int cache_batch, int max_len, int max_pos,
                                 int d_c, int row_width, int dtype, cudaStream_t s);

@@ -499,6 +499,115 @@ mla_status_t mla_out_proj(mla_handle_t h, const void* o_lat, int32_t batch, cons
   return MLA_OK;
 }
 
+// ------------------------------------------------------------------- pre-merged forms
+mla_status_t mla_premerge_query_weights(mla_handle_t h, const void* W_UQ, const void* W_UK, void* W_QK,
+                                        void* stream) {
+  if (!h || !W_UQ || !W_UK || !W_QK) return MLA_ERR_INVALID_ARG;
+  if (!aligned16(W_UQ) || !aligned16(W_UK) || !aligned16(W_QK)) return MLA_ERR_INVALID_ARG;
+  if (!on_handle_device(h)) return MLA_ERR_INVALID_ARG;
+  const mla_config_t& c = h->cfg;
+  if (launch_premerge_query(W_UQ, W_UK, W_QK, c.n_h, c.d_h, c.d_c, c.d_cq, c.dtype,
+                            static_cast<cudaStream_t>(stream)) != cudaSuccess)
+    return MLA_ERR_CUDA;
+  h->last_launches = 1;
+  return MLA_OK;
+}
+
+mla_status_t mla_premerge_output_weights(mla_handle_t h, const void* W_UV, const void* W_O, void* W_OUV,
+                                         void* stream) {
+  if (!h || !W_UV || !W_O || !W_OUV) return MLA_ERR_INVALID_ARG;
+  if (!aligned16(W_UV) || !aligned16(W_O) || !aligned16(W_OUV)) return MLA_ERR_INVALID_ARG;
+  if (!on_handle_device(h)) return MLA_ERR_INVALID_ARG;
+  const mla_config_t& c = h->cfg;
+  if (launch_premerge_output(W_UV, W_O, W_OUV, c.n_h, c.d_h, c.d_c, c.d, c.dtype,
+                             static_cast<cudaStream_t>(stream)) != cudaSuccess)
+    return MLA_ERR_CUDA;
+  h->last_launches = 1;
+  return MLA_OK;
+}
+
+mla_status_t mla_absorb_q_premerged(mla_handle_t h, const void* x, int32_t batch, const void* W_DQ,
+                                    const void* W_QK, const void* W_QR, const int32_t* pos, void* q_abs, void* ws,
+                                    size_t ws_bytes, void* stream) {
+  if (!h || batch <= 0 || !x || !W_DQ || !W_QK || !W_QR || !pos || !q_abs) return MLA_ERR_INVALID_ARG;
+  if (!aligned16(x) || !aligned16(W_DQ) || !aligned16(W_QK) || !aligned16(W_QR) || !aligned16(pos) ||
+      !aligned16(q_abs) || (ws && !aligned16(ws)))
+    return MLA_ERR_INVALID_ARG;
+  size_t need = 0;
+  mla_absorb_q_workspace_size(h, batch, &need);
+  if (!ws || ws_bytes < need) return MLA_ERR_WORKSPACE;
+  if (!on_handle_device(h)) return MLA_ERR_INVALID_ARG;
+  const mla_config_t& c = h->cfg;
+  if (64 % c.d_r != 0) return MLA_ERR_UNSUPPORTED;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  const int D = c.d_c + c.d_r;
+  void* c_q = ws;
+  {
+    TcGemm g1 = tc_base(h);  // c_Q = W_DQ x
+    tc_seg(g1, 0, W_DQ, c.d_cq, 0, EPI_STORE, c_q, c.d_cq);
+    g1.ldw = c.d; g1.x = x; g1.ldx = c.d; g1.N = batch; g1.K = c.d;
+    // [q~ | q_R] = [W_QK ; W_QR] c_Q in one launch: the W_QK rows go to
+    // q_abs[b, i, :d_c] in segments of d_c, the W_QR rows get RoPE and go to q_abs[b, i, d_c:]
+    TcGemm g2 = tc_base(h);
+    tc_seg(g2, 0, W_QK, c.n_h * c.d_c, 0, EPI_SEGS, q_abs, (long long)c.n_h * D, 0, D, 0);
+    g2.seg_len[0] = c.d_c;
+    tc_seg(g2, 1, W_QR, c.n_h * c.d_r, 0, EPI_ROPE_SEGS, q_abs, (long long)c.n_h * D, 0, D, c.d_c);
+    g2.ldw = c.d_cq; g2.x = c_q; g2.ldx = c.d_cq; g2.N = batch; g2.K = c.d_cq; g2.pos = pos;
+    const bool tc = use_tc_proj(h, g1) && use_tc_proj(h, g2);
+    if (h->proj_path == MLA_PROJ_TCGEN05 && !tc) return MLA_ERR_UNSUPPORTED;
+    if (tc) {
+      if (launch_gemm_tc(g1, h->num_sms, s) != cudaSuccess) return MLA_ERR_CUDA;
+      if (launch_gemm_tc(g2, h->num_sms, s) != cudaSuccess) return MLA_ERR_CUDA;
+      h->last_launches = 2;
+      return MLA_OK;
+    }
+  }
+  GemmArgs a{};
+  a.batch = 1; a.wlayout = W_NORMAL; a.status = h->status;
+  a.rope_cos = h->rope_cos; a.rope_sin = h->rope_sin; a.d_r = c.d_r; a.max_pos = c.max_pos;
+  // c_Q = W_DQ x
+  a.X = x; a.ldx = c.d; a.W = W_DQ; a.ldw = c.d; a.out = c_q; a.ldo = c.d_cq;
+  a.N = batch; a.M = c.d_cq; a.K = c.d; a.epi = EPI_STORE;
+  if (launch_gemm_simt(a, c.dtype, s) != cudaSuccess) return MLA_ERR_CUDA;
+  // q~ = W_QK c_Q into q_abs[b, i, :d_c]
+  a.X = c_q; a.ldx = c.d_cq; a.W = W_QK; a.ldw = c.d_cq; a.out = q_abs; a.ldo = (long long)c.n_h * D;
+  a.M = c.n_h * c.d_c; a.K = c.d_cq; a.epi = EPI_SEGS; a.seg_len = c.d_c; a.seg_stride = D; a.seg_off = 0;
+  if (launch_gemm_simt(a, c.dtype, s) != cudaSuccess) return MLA_ERR_CUDA;
+  // q_R = RoPE(W_QR c_Q) into q_abs[b, i, d_c:]
+  a.W = W_QR; a.M = c.n_h * c.d_r; a.epi = EPI_ROPE_SEGS; a.pos = pos; a.seg_stride = D; a.seg_off = c.d_c;
+  if (launch_gemm_simt(a, c.dtype, s) != cudaSuccess) return MLA_ERR_CUDA;
+  h->last_launches = 3;
+  return MLA_OK;
+}
+
+mla_status_t mla_out_proj_premerged(mla_handle_t h, const void* o_lat, int32_t batch, const void* W_OUV, void* u,
+                                    void* stream) {
+  if (!h || batch <= 0 || !o_lat || !W_OUV || !u) return MLA_ERR_INVALID_ARG;
+  if (!aligned16(o_lat) || !aligned16(W_OUV) || !aligned16(u)) return MLA_ERR_INVALID_ARG;
+  if (!on_handle_device(h)) return MLA_ERR_INVALID_ARG;
+  const mla_config_t& c = h->cfg;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  const int K = c.n_h * c.d_c;
+  {
+    TcGemm g = tc_base(h);  // u = W_OUV [o_lat_1; ...; o_lat_nh]
+    tc_seg(g, 0, W_OUV, c.d, 0, EPI_STORE, u, c.d);
+    g.ldw = K; g.x = o_lat; g.ldx = K; g.N = batch; g.K = K;
+    const bool tc = use_tc_proj(h, g);
+    if (h->proj_path == MLA_PROJ_TCGEN05 && !tc) return MLA_ERR_UNSUPPORTED;
+    if (tc) {
+      if (launch_gemm_tc(g, h->num_sms, s) != cudaSuccess) return MLA_ERR_CUDA;
+      h->last_launches = 1;
+      return MLA_OK;
+    }
+  }
+  GemmArgs a{};
+  a.X = o_lat; a.ldx = K; a.W = W_OUV; a.ldw = K; a.wlayout = W_NORMAL; a.out = u; a.ldo = c.d;
+  a.N = batch; a.M = c.d; a.K = K; a.batch = 1; a.epi = EPI_STORE; a.status = h->status;
+  if (launch_gemm_simt(a, c.dtype, s) != cudaSuccess) return MLA_ERR_CUDA;
+  h->last_launches = 1;
+  return MLA_OK;
+}
+
 // ------------------------------------------------------------------- S1..S5
 // Workspace of the whole step: q_abs, o_lat and lse, then one region the
 // stages use in turn (c_Q and q_C; the split plan and partials; o).

@@ -203,6 +203,41 @@ MLA_API mla_status_t mla_out_proj(mla_handle_t handle, const void* o_lat, int32_
                           const void* W_UV, const void* W_O, void* u,
                           void* ws, size_t ws_bytes, void* stream);
 
+/* Pre-merged weight forms ([MLA] §4: W^{UQ T} W^{UK} "can be merged ahead of
+   time", and the per-head u_t = sum_i W_O_i W_UV_i o_lat_i). Each merge runs
+   once per set of weights (a setup step, not part of the decode step); the
+   products are accumulated in fp32 and rounded once to the handle's dtype.
+   The caller owns every buffer; the calls are asynchronous on `stream`.
+
+   mla_premerge_query_weights: W_QK [n_h, d_c, d_cq] out, W_QK_i = W_UK_i^T W_UQ_i,
+     the map that takes c_Q straight to q~_i = W_QK_i c_Q.
+     W_UQ [n_h*d_h, d_cq], W_UK [n_h*d_h, d_c] as in mla_absorb_q.
+   mla_premerge_output_weights: W_OUV [d, n_h*d_c] out, column block i (columns
+     [i*d_c, (i+1)*d_c)) = W_O_i W_UV_i, so that u = W_OUV [o_lat_1; ...; o_lat_nh].
+     W_UV [n_h*d_h, d_c], W_O [d, n_h*d_h] as in mla_out_proj.
+   Sizes at the DeepSeek-V2 shape: W_QK 201 MB against 92 MB for W_UQ and W_UK,
+   W_OUV 671 MB against 185 MB for W_UV and W_O (bf16). */
+MLA_API mla_status_t mla_premerge_query_weights(mla_handle_t handle, const void* W_UQ, const void* W_UK,
+                                                void* W_QK, void* stream);
+MLA_API mla_status_t mla_premerge_output_weights(mla_handle_t handle, const void* W_UV, const void* W_O,
+                                                 void* W_OUV, void* stream);
+
+/* S2 with the pre-merged query map: c_Q = W_DQ x, q~_i = W_QK_i c_Q, q_R =
+   RoPE(W_QR c_Q), written to q_abs exactly as mla_absorb_q writes it (two
+   launches on the tensor-core path: c_Q, then [W_QK ; W_QR] together).
+     W_QK from mla_premerge_query_weights; other arguments as in mla_absorb_q;
+     ws at least mla_absorb_q_workspace_size bytes (c_Q is kept there). */
+MLA_API mla_status_t mla_absorb_q_premerged(mla_handle_t handle, const void* x, int32_t batch,
+                                            const void* W_DQ, const void* W_QK, const void* W_QR,
+                                            const int32_t* pos, void* q_abs, void* ws, size_t ws_bytes,
+                                            void* stream);
+
+/* S4/S5 with the pre-merged output map: u = W_OUV [o_lat_1; ...; o_lat_nh]
+   in one launch, without the expanded per-head outputs o (no workspace).
+     o_lat [batch, n_h, d_c], W_OUV [d, n_h*d_c], u [batch, d] out. */
+MLA_API mla_status_t mla_out_proj_premerged(mla_handle_t handle, const void* o_lat, int32_t batch,
+                                            const void* W_OUV, void* u, void* stream);
+
 /* S1..S5 in one call ([MLA] §3-§7; [MiniMind] §9-§12): the new token of
    sequence b (x[b], position pos[b]) is written to cache[b, pos[b], :], the
    absorbed queries are formed, attention covers seqlens[b] rows of sequence b

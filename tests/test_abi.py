@@ -75,6 +75,11 @@ def test_null_handle_is_rejected():
     assert m._c["mla_set_wait_limit"](None, 1000) == m.MLA_ERR_INVALID_ARG
     assert m._c["mla_set_fault_injection"](None, 0) == m.MLA_ERR_INVALID_ARG
     assert m._c["mla_set_kv_norm"](None, None, 1e-5) == m.MLA_ERR_INVALID_ARG
+    assert m._c["mla_premerge_query_weights"](None, None, None, None, None) == m.MLA_ERR_INVALID_ARG
+    assert m._c["mla_premerge_output_weights"](None, None, None, None, None) == m.MLA_ERR_INVALID_ARG
+    assert m._c["mla_absorb_q_premerged"](None, None, 1, None, None, None, None, None, None, 0,
+                                          None) == m.MLA_ERR_INVALID_ARG
+    assert m._c["mla_out_proj_premerged"](None, None, 1, None, None, None) == m.MLA_ERR_INVALID_ARG
 
 
 def test_binding_has_every_declared_function():

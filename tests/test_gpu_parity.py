@@ -387,6 +387,81 @@ def test_projections_full_size(name):
     assert_close(host(dec.u), ref_u, shp.dtype, what="u")
 
 
+# --------------------------------------------------------------------- pre-merged forms
+def premerged_dev(shp, dec):
+    """The library's merged weights for the decoder's weights (setup calls)."""
+    dt = torch_dtype(shp)
+    W_QK = torch.empty((shp.n_h, shp.d_c, shp.d_cq), dtype=dt, device="cuda")
+    W_OUV = torch.empty((shp.d, shp.n_h * shp.d_c), dtype=dt, device="cuda")
+    M.mla_premerge_query_weights(dec.handle, dec.W["W_UQ"], dec.W["W_UK"], W_QK)
+    M.mla_premerge_output_weights(dec.handle, dec.W["W_UV"], dec.W["W_O"], W_OUV)
+    return W_QK, W_OUV
+
+
+@pytest.mark.parametrize("name", SMALL)
+def test_premerged_weights_match_oracle(name):
+    shp = small_shape(name)
+    W = S.draw_weights(shp)
+    dec = decoder(shp, make_weights_dev(shp, W), 2, 16)
+    W_QK, W_OUV = premerged_dev(shp, dec)
+    ref_qk = O.premerged_query_weights(W["W_UQ"], W["W_UK"], shp.n_h, shp.d_h)
+    ref_ouv = O.premerged_output_weights(W["W_UV"], W["W_O"], shp.n_h, shp.d_h)
+    assert_close(host(W_QK), ref_qk, shp.dtype, what="W_QK")
+    assert_close(host(W_OUV), ref_ouv, shp.dtype, what="W_OUV")
+
+
+@pytest.mark.parametrize("name", SMALL)
+@pytest.mark.parametrize("proj", PROJ)
+def test_premerged_calls_match_oracle(name, proj):
+    """The absorbed query through W_QK and the output through W_OUV reach the
+    oracle's two-step forms (the merge is exact up to rounding)."""
+    shp = small_shape(name)
+    W = S.draw_weights(shp)
+    B = 37 if name != "tiny" else 2
+    h = S.draw_new_tokens(shp, B)
+    max_pos = 5000
+    pos = np.random.default_rng(7).integers(0, max_pos, size=B)
+    pos[0], pos[-1] = 0, max_pos - 1
+    dec = decoder(shp, make_weights_dev(shp, W), B, 16, max_pos=max_pos)
+    set_proj(dec, proj)
+    W_QK, W_OUV = premerged_dev(shp, dec)
+    M.mla_absorb_q_premerged(dec.handle, dev(h, shp), B, dec.W["W_DQ"], W_QK, dec.W["W_QR"], dev_i32(pos),
+                             dec.q_abs, dec.ws, dec.ws.numel())
+    ref_q = O.absorbed_query(h, W["W_DQ"], W["W_UQ"], W["W_QR"], W["W_UK"], pos, shp.n_h, shp.d_h, shp.d_r,
+                             shp.rope_base)
+    assert_close(host(dec.q_abs), ref_q, shp.dtype, what="q_abs (pre-merged)")
+    o_lat = S.to_dtype(S.draw_latent_rows(shp, B * shp.n_h, sub=13)[:, :shp.d_c].reshape(B, shp.n_h, shp.d_c)
+                       / 8.0, shp.dtype)
+    M.mla_out_proj_premerged(dec.handle, dev(o_lat, shp), B, W_OUV, dec.u)
+    ref_u = O.output_projection(o_lat, W["W_UV"], W["W_O"], shp.n_h, shp.d_h)
+    assert_close(host(dec.u), ref_u, shp.dtype, what="u (pre-merged)")
+    assert M.mla_get_device_status(dec.handle) == (M.MLA_OK, 0)
+
+
+def test_premerged_full_size_v2():
+    """The benchmark's V2 projection shapes (batch 64) through the pre-merged maps."""
+    shp = S.workload("v2")
+    W = S.draw_weights(shp)
+    B = shp.batch
+    h = S.draw_new_tokens(shp, B)
+    pos = np.random.default_rng(9).integers(0, 4097, size=B)
+    dec = decoder(shp, make_weights_dev(shp, W), B, 4097, max_pos=4097)
+    W_QK, W_OUV = premerged_dev(shp, dec)
+    M.mla_absorb_q_premerged(dec.handle, dev(h, shp), B, dec.W["W_DQ"], W_QK, dec.W["W_QR"], dev_i32(pos),
+                             dec.q_abs, dec.ws, dec.ws.numel())
+    assert M.mla_last_launch_count(dec.handle) == 2
+    o_lat = S.to_dtype(S.draw_latent_rows(shp, B * shp.n_h, sub=14)[:, :shp.d_c].reshape(B, shp.n_h, shp.d_c)
+                       / 8.0, shp.dtype)
+    M.mla_out_proj_premerged(dec.handle, dev(o_lat, shp), B, W_OUV, dec.u)
+    assert M.mla_last_launch_count(dec.handle) == 1
+    assert M.mla_get_device_status(dec.handle) == (M.MLA_OK, 0)
+    ref_q = O.absorbed_query(h, W["W_DQ"], W["W_UQ"], W["W_QR"], W["W_UK"], pos, shp.n_h, shp.d_h, shp.d_r,
+                             shp.rope_base)
+    assert_close(host(dec.q_abs), ref_q, shp.dtype, what="q_abs (pre-merged)")
+    ref_u = O.output_projection(o_lat, W["W_UV"], W["W_O"], shp.n_h, shp.d_h)
+    assert_close(host(dec.u), ref_u, shp.dtype, what="u (pre-merged)")
+
+
 # --------------------------------------------------------------------- whole step
 def end_to_end(shp, ctx_lens):
     B = len(ctx_lens)
