@@ -179,6 +179,22 @@ def plan_balance(seqlens, chunks: int, granule: int):
     return round(max(rows) / (sum(rows) / len(rows)), 4), len(rows)
 
 
+class L2Flush:
+    """Empties L2 before a timed call: writes a 256 MB buffer (twice L2), then
+    reads another 256 MB one, so that L2 ends up holding clean lines. Without
+    the read the timed kernel would pay for writing back up to 126 MB of the
+    flush's dirty lines."""
+
+    def __init__(self, device):
+        import torch
+        self.w = torch.empty(256 << 20, dtype=torch.uint8, device=device)
+        self.r = torch.ones(64 << 20, dtype=torch.float32, device=device)
+
+    def __call__(self):
+        self.w.fill_(1)
+        self.r.sum()
+
+
 def attention_workloads(device, peaks, iters: int = 20):
     """mla_decode_attn alone on the other decode workloads (random caches of
     the workload's shape; CUDA events, median of `iters` calls)."""
