@@ -46,21 +46,21 @@ def load_peaks():
     return dict(FALLBACK_PEAKS), "fallback"
 
 
-def kernel_source_hash() -> str:
-    """Hash of the attention kernel's sources (the kernel the committed
-    traffic figure was measured on, and the headers it includes)."""
+def kernel_source_hash(kernel: str = "decode_pair") -> str:
+    """Hash of an attention kernel's sources (the kernel a committed traffic
+    figure was measured on, and the headers it includes)."""
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "head_latent_attention_24_b300", "csrc")
-    for n in ("decode_pair.cu", "decode_pair.cuh", "tc_ptx.cuh", "tmap.cuh", "internal.cuh"):
+    for n in (f"{kernel}.cu", f"{kernel}.cuh", "tc_ptx.cuh", "tmap.cuh", "internal.cuh"):
         with open(os.path.join(csrc, n), "rb") as f:
             h.update(n.encode() + f.read())
     return h.hexdigest()[:16]
 
 
-def committed_traffic(kernel_hash: str):
-    """DRAM bytes per launch of the attention kernel from the committed ncu
-    summary, if it was taken on the current kernel sources."""
-    p = os.path.join(ROOT, "profiles", "decode_attn_v2_traffic.json")
+def committed_traffic(kernel_hash: str, record: str = "decode_attn_v2_traffic.json"):
+    """DRAM bytes per launch of a kernel from its committed ncu summary, if it
+    was taken on the current kernel sources."""
+    p = os.path.join(ROOT, "profiles", record)
     if not os.path.exists(p):
         return None
     with open(p) as f:
@@ -242,6 +242,9 @@ def attention_workloads(device, peaks, iters: int = 20):
                       else "cache larger than L2",
                       "decode_path": {M.MLA_DECODE_SIMT: "simt", M.MLA_DECODE_TCGEN05: "tcgen05"}[
                           M.mla_get_decode_path(h)]})
+            if name == "minimind":
+                r["traffic"] = committed_traffic(kernel_source_hash("decode_narrow"),
+                                                 "decode_narrow_minimind_traffic.json")
             if name == "v2_ragged":
                 bal, busy = plan_balance(seqlens, h_chunks(M, h, B, max_len, device), 64)
                 r["split_rows_max_over_mean"] = bal
