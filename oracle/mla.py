@@ -290,3 +290,85 @@ def decode_materialised(h_ctx_list, h_new, W, n_h, d_h, d_r, base, pos=None, ret
     if return_parts:
         return u, o_all, lse_all
     return u
+
+
+# --------------------------------------------------------------------------
+# The materialised (MHA) path for several query tokens per sequence
+# --------------------------------------------------------------------------
+def materialised_kv(rows, W_UK, W_UV, n_h: int, d_h: int):
+    """k_C [N, n_h, d_h] = W_UK_i c_KV and v_C [N, n_h, d_h] = W_UV_i c_KV for
+    cache rows [N, d_c + d_r] ([MLA] §3 low-rank K/V; [MiniMind] §10 naive
+    version: K_nope and V restored from the latent)."""
+    rows = _f64(rows)
+    d_c = _f64(W_UK).shape[1]
+    c_kv = rows[:, :d_c]
+    N = rows.shape[0]
+    k_c = (c_kv @ _f64(W_UK).T).reshape(N, n_h, d_h)
+    v_c = (c_kv @ _f64(W_UV).T).reshape(N, n_h, d_h)
+    return k_c, v_c
+
+
+def materialised_query(h, W_DQ, W_UQ, W_QR, pos, n_h: int, d_h: int, d_r: int, base: float):
+    """q [N, n_h, d_h + d_r] = [W_UQ_i c_Q ; RoPE(W_QR_i c_Q)], c_Q = W_DQ h
+    ([MLA] §3 and §6), for tokens h [N, d] at positions pos [N]."""
+    h = _f64(h)
+    N = h.shape[0]
+    c_q = h @ _f64(W_DQ).T
+    q_c = (c_q @ _f64(W_UQ).T).reshape(N, n_h, d_h)
+    q_r = rope((c_q @ _f64(W_QR).T).reshape(N, n_h, d_r), _f64(pos)[:, None], base)
+    return np.concatenate([q_c, q_r], axis=-1)
+
+
+def mha_attention(q, k_c, k_r, v_c, q_pos, scale: float):
+    """Causal multi-head attention of one sequence over materialised keys.
+
+    q [T, n_h, d_h + d_r] at positions q_pos [T]; k_c [L, n_h, d_h], the shared
+    RoPE key k_r [L, d_r] and v_c [L, n_h, d_h] of rows 0..L-1. Query t sees
+    rows 0..q_pos[t] ([MiniMind] §12: with a cache the query sees every earlier
+    row and itself); k = [k_C ; k_R] per head ([MLA] §6), scale 1/sqrt(d_h+d_r)
+    ([MLA] §7). Two-pass softmax. Returns o [T, n_h, d_h] and the natural-log
+    LSE [T, n_h].
+    """
+    q, k_c, k_r, v_c = _f64(q), _f64(k_c), _f64(k_r), _f64(v_c)
+    T, n_h, _ = q.shape
+    L = k_c.shape[0]
+    k = np.concatenate([k_c, np.broadcast_to(k_r[:, None, :], (L, n_h, k_r.shape[1]))], axis=-1)
+    s = np.einsum("thc,lhc->htl", q, k) * scale                          # [n_h, T, L]
+    visible = np.arange(L)[None, :] <= _f64(q_pos)[:, None]               # [T, L]
+    s = np.where(visible[None], s, -np.inf)
+    m = s.max(axis=2, keepdims=True)
+    e = np.exp(s - m)
+    l = e.sum(axis=2, keepdims=True)
+    o = np.einsum("htl,lhc->thc", e / l, v_c)
+    lse = (m + np.log(l))[:, :, 0].T
+    return o, lse
+
+
+def prefill_materialised(h_ctx_list, h_new_list, W, n_h, d_h, d_r, base, return_parts=False):
+    """Several new tokens per sequence through the materialised (MHA) path.
+
+    [Latent]: at prefill MLA takes the MHA path (K and V restored from the
+    latent); [MiniMind] §10 naive version. Sequence b holds L_b cached tokens
+    h_ctx_list[b] at positions 0..L_b-1 and T_b new tokens h_new_list[b] at
+    positions L_b..L_b+T_b-1; every new token is appended to the cache and
+    then attends causally. Returns u per sequence [T_b, d] (and o [T_b, n_h*d_h],
+    lse [T_b, n_h] per sequence if asked).
+    """
+    W = {k: _f64(v) for k, v in W.items()}
+    scale = scale_of(d_h, d_r)
+    us, os_, lses = [], [], []
+    for h_ctx, h_new in zip(h_ctx_list, h_new_list):
+        h_ctx, h_new = _f64(h_ctx), _f64(h_new)
+        L, T = h_ctx.shape[0], h_new.shape[0]
+        toks = np.concatenate([h_ctx, h_new], axis=0)
+        rows = cache_rows(toks, W["W_DKV"], W["W_KR"], np.arange(L + T), base)
+        k_c, v_c = materialised_kv(rows, W["W_UK"], W["W_UV"], n_h, d_h)
+        q_pos = L + np.arange(T)
+        q = materialised_query(h_new, W["W_DQ"], W["W_UQ"], W["W_QR"], q_pos, n_h, d_h, d_r, base)
+        d_c = W["W_DKV"].shape[0]
+        o, lse = mha_attention(q, k_c, rows[:, d_c:], v_c, q_pos, scale)
+        o = o.reshape(T, n_h * d_h)
+        us.append(o @ W["W_O"].T)
+        os_.append(o)
+        lses.append(lse)
+    return (us, os_, lses) if return_parts else us

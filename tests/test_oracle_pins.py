@@ -667,3 +667,113 @@ def test_planted_premerged_query_mistakes_are_caught(mutant):
 
 def test_planted_premerged_output_mistake_is_caught():
     assert not check_premerged_output(_premerged_output_blocks_swapped)
+
+
+# ---------------------------------------------------------------------------
+# pins: the materialised (MHA) path for several new tokens (Latent page: prefill
+# takes the MHA path; MiniMind page §10 naive version, §12 causal visibility)
+# ---------------------------------------------------------------------------
+def check_mha_brute(fn):
+    """Pure-Python loops on tiny shapes, including rows that a query must not see."""
+    rng = np.random.default_rng(41)
+    T, L, n_h, d_h, d_r = 3, 6, 2, 3, 2
+    q = rng.standard_normal((T, n_h, d_h + d_r))
+    k_c = rng.standard_normal((L, n_h, d_h))
+    k_r = rng.standard_normal((L, d_r))
+    v_c = rng.standard_normal((L, n_h, d_h))
+    q_pos = np.array([2, 3, 5])
+    sc = 0.6
+    o, lse = fn(q, k_c, k_r, v_c, q_pos, sc)
+    ok = True
+    for t in range(T):
+        for i in range(n_h):
+            s = [sc * (sum(q[t, i, c] * k_c[r, i, c] for c in range(d_h)) +
+                       sum(q[t, i, d_h + c] * k_r[r, c] for c in range(d_r))) for r in range(q_pos[t] + 1)]
+            ref_lse = logsumexp(s)
+            w = [math.exp(v - ref_lse) for v in s]
+            ref_o = [sum(w[r] * v_c[r, i, c] for r in range(len(s))) for c in range(d_h)]
+            ok &= abs(lse[t, i] - ref_lse) < 1e-12 and np.allclose(o[t, i], ref_o, rtol=1e-12, atol=1e-14)
+    return bool(ok)
+
+
+def check_prefill_rows_are_decode_steps(prefill):
+    """Row t of a T-token prefill equals the decode step of new token t with the
+    context and new tokens 0..t-1 cached (the decode definition is pinned above)."""
+    m = MICRO
+    W, h_ctx, _ = micro_inputs(42, L=4)
+    rng = np.random.default_rng(43)
+    h_new = rng.standard_normal((3, m["d"]))
+    us, os_, lses = prefill([h_ctx[0]], [h_new], W, m["n_h"], m["d_h"], m["d_r"], 10000.0, return_parts=True)
+    ok = True
+    for t in range(3):
+        ctx = np.concatenate([h_ctx[0], h_new[:t]])
+        u, o, lse = O.decode_materialised([ctx], h_new[t:t + 1], W, m["n_h"], m["d_h"], m["d_r"], 10000.0,
+                                          return_parts=True)
+        ok &= np.allclose(us[0][t], u[0], rtol=1e-10, atol=1e-12) and np.allclose(os_[0][t], o[0], rtol=1e-10,
+                                                                                   atol=1e-12)
+        ok &= np.allclose(lses[0][t], lse[0], rtol=1e-12, atol=1e-12)
+    return bool(ok)
+
+
+def check_prefill_causal(prefill):
+    """Changing the last new token leaves every earlier row unchanged."""
+    m = MICRO
+    W, h_ctx, _ = micro_inputs(44, L=2)
+    rng = np.random.default_rng(45)
+    h_new = rng.standard_normal((4, m["d"]))
+    h_alt = h_new.copy()
+    h_alt[-1] += 3.0
+    a = prefill([h_ctx[0]], [h_new], W, m["n_h"], m["d_h"], m["d_r"], 10000.0)[0]
+    b = prefill([h_ctx[0]], [h_alt], W, m["n_h"], m["d_h"], m["d_r"], 10000.0)[0]
+    return bool(np.allclose(a[:-1], b[:-1], rtol=1e-13, atol=1e-13) and not np.allclose(a[-1], b[-1]))
+
+
+def test_mha_attention_brute_force():
+    assert check_mha_brute(O.mha_attention)
+
+
+def test_prefill_rows_are_decode_steps():
+    assert check_prefill_rows_are_decode_steps(O.prefill_materialised)
+
+
+def test_prefill_is_causal():
+    assert check_prefill_causal(O.prefill_materialised)
+
+
+def test_materialised_query_is_absorbed_query_parts():
+    m = MICRO
+    W, _, h_new = micro_inputs(46, L=2)
+    pos = np.array([7])
+    q = O.materialised_query(h_new, W["W_DQ"], W["W_UQ"], W["W_QR"], pos, m["n_h"], m["d_h"], m["d_r"], 10000.0)
+    _, parts = O.absorbed_query(h_new, W["W_DQ"], W["W_UQ"], W["W_QR"], W["W_UK"], pos, m["n_h"], m["d_h"], m["d_r"],
+                                10000.0, return_parts=True)
+    assert np.allclose(q, np.concatenate([parts["q_C"], parts["q_R"]], axis=-1), rtol=1e-13, atol=1e-13)
+
+
+_MHA = O.mha_attention
+
+
+def _mha_no_mask(q, k_c, k_r, v_c, q_pos, scale):
+    return _MHA(q, k_c, k_r, v_c, np.full(len(q_pos), np.asarray(k_c).shape[0] - 1), scale)
+
+
+def _mha_excludes_self(q, k_c, k_r, v_c, q_pos, scale):
+    return _MHA(q, k_c, k_r, v_c, np.asarray(q_pos) - 1, scale)
+
+
+def _prefill_with(mha):
+    def run(h_ctx_list, h_new_list, W, n_h, d_h, d_r, base, return_parts=False):
+        orig = O.mha_attention
+        O.mha_attention = mha
+        try:
+            return O.prefill_materialised(h_ctx_list, h_new_list, W, n_h, d_h, d_r, base, return_parts)
+        finally:
+            O.mha_attention = orig
+    return run
+
+
+@pytest.mark.parametrize("mutant", [_mha_no_mask, _mha_excludes_self])
+def test_planted_mha_mistakes_are_caught(mutant):
+    assert not check_mha_brute(mutant)
+    assert not (check_prefill_rows_are_decode_steps(_prefill_with(mutant))
+                and check_prefill_causal(_prefill_with(mutant)))
