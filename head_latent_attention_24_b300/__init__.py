@@ -96,6 +96,10 @@ _c = {
     "mla_premerge_output_weights": _sig("mla_premerge_output_weights", [_P, _P, _P, _P, _P]),
     "mla_absorb_q_premerged": _sig("mla_absorb_q_premerged", [_P, _P, _I, _P, _P, _P, _P, _P, _P, _S, _P]),
     "mla_out_proj_premerged": _sig("mla_out_proj_premerged", [_P, _P, _I, _P, _P, _P]),
+    "mla_project_q": _sig("mla_project_q", [_P, _P, _I, _P, _P, _P, _P, _P, _P, _S, _P]),
+    "mla_materialise_kv": _sig("mla_materialise_kv", [_P, _P, _I, _P, _P, _P, _P, _P]),
+    "mla_mha_attn": _sig("mla_mha_attn", [_P, _P, _I, _I, _P, _P, _P, _I, _P, _P, _P, _P]),
+    "mla_project_out": _sig("mla_project_out", [_P, _P, _I, _P, _P, _P]),
 }
 
 
@@ -212,6 +216,25 @@ def mla_absorb_q_premerged(handle, x, batch, W_DQ, W_QK, W_QR, pos, q_abs, ws, w
 def mla_out_proj_premerged(handle, o_lat, batch, W_OUV, u, stream=None):
     _check(_c["mla_out_proj_premerged"](handle, _ptr(o_lat), batch, _ptr(W_OUV), _ptr(u), _stream(stream)),
            "mla_out_proj_premerged")
+
+
+def mla_project_q(handle, x, n_tokens, W_DQ, W_UQ, W_QR, pos, q, ws, ws_bytes, stream=None):
+    _check(_c["mla_project_q"](handle, _ptr(x), n_tokens, _ptr(W_DQ), _ptr(W_UQ), _ptr(W_QR), _ptr(pos), _ptr(q),
+                               _ptr(ws), ws_bytes, _stream(stream)), "mla_project_q")
+
+
+def mla_materialise_kv(handle, rows, n_rows, W_UK, W_UV, k_c, v_c, stream=None):
+    _check(_c["mla_materialise_kv"](handle, _ptr(rows), n_rows, _ptr(W_UK), _ptr(W_UV), _ptr(k_c), _ptr(v_c),
+                                    _stream(stream)), "mla_materialise_kv")
+
+
+def mla_mha_attn(handle, q, batch, n_q, k_c, v_c, cache, max_len, q_pos0, o, lse, stream=None):
+    _check(_c["mla_mha_attn"](handle, _ptr(q), batch, n_q, _ptr(k_c), _ptr(v_c), _ptr(cache), max_len, _ptr(q_pos0),
+                              _ptr(o), _ptr(lse), _stream(stream)), "mla_mha_attn")
+
+
+def mla_project_out(handle, o, n_tokens, W_O, u, stream=None):
+    _check(_c["mla_project_out"](handle, _ptr(o), n_tokens, _ptr(W_O), _ptr(u), _stream(stream)), "mla_project_out")
 
 
 def mla_decode_step_workspace_size(handle, batch, max_len) -> int:

@@ -455,8 +455,10 @@ cudaError_t launch_gemm_tc(const TcGemm& g, int num_sms, cudaStream_t s) {
   // When the tiles outnumber the SMs, two CTAs share an SM (half the stage
   // budget each) so that every tile is resident at once; otherwise one CTA
   // per SM keeps the most bytes in flight per tile.
+  // The epilogue's fp32 partial tile (n_tile x 128) reuses the stage buffers:
+  // two CTAs share an SM only when it fits their half of shared memory.
   const long long tiles_all = (long long)p.mtiles_total * n_tiles * g.Z;
-  const int per_sm = tiles_all > num_sms ? 2 : 1;
+  const int per_sm = (tiles_all > num_sms && (size_t)p.n_tile * BM * 4 <= (size_t)SMEM_TWO) ? 2 : 1;
   const int budget = per_sm == 2 ? SMEM_TWO : SMEM_ONE;
   num_sms *= per_sm;
 
@@ -469,7 +471,8 @@ cudaError_t launch_gemm_tc(const TcGemm& g, int num_sms, cudaStream_t s) {
   for (int sg = 0; sg < g.nseg; ++sg) mt_ok = mt_ok && g.epi[sg] != EPI_APPEND;
   if (tiles1 > num_sms && mt_ok) {
     for (int c = 2; c <= MAX_MT; c *= 2)
-      if (p.mtiles_total % c == 0 && p.mstart[1] % c == 0 && p.mstart[2] % c == 0 && c * p.n_tile <= 512) {
+      if (p.mtiles_total % c == 0 && p.mstart[1] % c == 0 && p.mstart[2] % c == 0 && c * p.n_tile <= 512 &&
+          (size_t)c * p.n_tile * BM * 4 <= (size_t)budget) {
         mt = c;
         if (tiles1 / c <= num_sms) break;
       }

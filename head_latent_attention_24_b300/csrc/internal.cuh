@@ -175,6 +175,23 @@ cudaError_t launch_decode_simt(const DecodeArgs& a, int dtype, cudaStream_t s, i
 cudaError_t launch_decode_combine(const DecodeArgs& a, int dtype, cudaStream_t s);
 
 // RMSNorm of the latent part of appended cache rows (kv_norm variant).
+// Causal multi-head attention over materialised K and V (the MHA path of
+// several new tokens per sequence). q [B, T, n_h, d_h + d_r]; k_c, v_c
+// [B, max_len, n_h, d_h]; k_R from the cache rows [B, max_len, d_c + d_r];
+// query t of sequence b is at position q_pos0[b] + t and sees rows 0..that.
+struct MhaArgs {
+  const void* q; const void* k_c; const void* v_c; const void* cache;
+  const int32_t* q_pos0;
+  void* o; float* lse;         // o [B, T, n_h, d_h], lse [B, T, n_h] (natural log)
+  int B, T, max_len, n_h, d_h, d_c, d_r;
+  float scale_log2;            // scale * log2(e)
+  long long wait_cycles;       // tensor-core kernel: bound of every mbarrier wait (0 = default)
+  int32_t* status;
+};
+cudaError_t launch_mha_simt(const MhaArgs& a, int dtype, cudaStream_t s);
+bool mha_tc_supported(const mla_handle_s* h);
+cudaError_t launch_mha_tc(const MhaArgs& a, cudaStream_t s);
+
 // Pre-merged weight forms (setup, once per set of weights): W_QK_i = W_UK_i^T W_UQ_i
 // into W_QK [n_h, d_c, d_cq]; W_OUV[:, i d_c:(i+1) d_c] = W_O_i W_UV_i into W_OUV [d, n_h d_c].
 cudaError_t launch_premerge_query(const void* W_UQ, const void* W_UK, void* W_QK, int n_h, int d_h, int d_c,

@@ -608,6 +608,146 @@ mla_status_t mla_out_proj_premerged(mla_handle_t h, const void* o_lat, int32_t b
   return MLA_OK;
 }
 
+// ------------------------------------------------------------------- the MHA path (several new tokens)
+mla_status_t mla_project_q(mla_handle_t h, const void* x, int32_t n_tokens, const void* W_DQ, const void* W_UQ,
+                           const void* W_QR, const int32_t* pos, void* q, void* ws, size_t ws_bytes, void* stream) {
+  if (!h || n_tokens <= 0 || !x || !W_DQ || !W_UQ || !W_QR || !pos || !q) return MLA_ERR_INVALID_ARG;
+  if (!aligned16(x) || !aligned16(W_DQ) || !aligned16(W_UQ) || !aligned16(W_QR) || !aligned16(pos) ||
+      !aligned16(q) || (ws && !aligned16(ws)))
+    return MLA_ERR_INVALID_ARG;
+  size_t need = 0;
+  mla_absorb_q_workspace_size(h, n_tokens, &need);
+  if (!ws || ws_bytes < need) return MLA_ERR_WORKSPACE;
+  if (!on_handle_device(h)) return MLA_ERR_INVALID_ARG;
+  const mla_config_t& c = h->cfg;
+  if (64 % c.d_r != 0) return MLA_ERR_UNSUPPORTED;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  const int DQ = c.d_h + c.d_r;
+  void* c_q = ws;
+  {
+    TcGemm g1 = tc_base(h);  // c_Q = W_DQ x
+    tc_seg(g1, 0, W_DQ, c.d_cq, 0, EPI_STORE, c_q, c.d_cq);
+    g1.ldw = c.d; g1.x = x; g1.ldx = c.d; g1.N = n_tokens; g1.K = c.d;
+    // q = [W_UQ_i c_Q ; RoPE(W_QR_i c_Q)]: segments of d_h and of d_r, one launch
+    TcGemm g2 = tc_base(h);
+    tc_seg(g2, 0, W_UQ, c.n_h * c.d_h, 0, EPI_SEGS, q, (long long)c.n_h * DQ, 0, DQ, 0);
+    g2.seg_len[0] = c.d_h;
+    tc_seg(g2, 1, W_QR, c.n_h * c.d_r, 0, EPI_ROPE_SEGS, q, (long long)c.n_h * DQ, 0, DQ, c.d_h);
+    g2.ldw = c.d_cq; g2.x = c_q; g2.ldx = c.d_cq; g2.N = n_tokens; g2.K = c.d_cq; g2.pos = pos;
+    const bool tc = use_tc_proj(h, g1) && use_tc_proj(h, g2);
+    if (h->proj_path == MLA_PROJ_TCGEN05 && !tc) return MLA_ERR_UNSUPPORTED;
+    if (tc) {
+      if (launch_gemm_tc(g1, h->num_sms, s) != cudaSuccess) return MLA_ERR_CUDA;
+      if (launch_gemm_tc(g2, h->num_sms, s) != cudaSuccess) return MLA_ERR_CUDA;
+      h->last_launches = 2;
+      return MLA_OK;
+    }
+  }
+  GemmArgs a{};
+  a.batch = 1; a.wlayout = W_NORMAL; a.status = h->status;
+  a.rope_cos = h->rope_cos; a.rope_sin = h->rope_sin; a.d_r = c.d_r; a.max_pos = c.max_pos;
+  a.X = x; a.ldx = c.d; a.W = W_DQ; a.ldw = c.d; a.out = c_q; a.ldo = c.d_cq;
+  a.N = n_tokens; a.M = c.d_cq; a.K = c.d; a.epi = EPI_STORE;
+  if (launch_gemm_simt(a, c.dtype, s) != cudaSuccess) return MLA_ERR_CUDA;
+  a.X = c_q; a.ldx = c.d_cq; a.W = W_UQ; a.ldw = c.d_cq; a.out = q; a.ldo = (long long)c.n_h * DQ;
+  a.M = c.n_h * c.d_h; a.K = c.d_cq; a.epi = EPI_SEGS; a.seg_len = c.d_h; a.seg_stride = DQ; a.seg_off = 0;
+  if (launch_gemm_simt(a, c.dtype, s) != cudaSuccess) return MLA_ERR_CUDA;
+  a.W = W_QR; a.M = c.n_h * c.d_r; a.epi = EPI_ROPE_SEGS; a.pos = pos; a.seg_stride = DQ; a.seg_off = c.d_h;
+  if (launch_gemm_simt(a, c.dtype, s) != cudaSuccess) return MLA_ERR_CUDA;
+  h->last_launches = 3;
+  return MLA_OK;
+}
+
+mla_status_t mla_materialise_kv(mla_handle_t h, const void* rows, int32_t n_rows, const void* W_UK, const void* W_UV,
+                                void* k_c, void* v_c, void* stream) {
+  if (!h || n_rows <= 0 || !rows || !W_UK || !W_UV || !k_c || !v_c) return MLA_ERR_INVALID_ARG;
+  if (!aligned16(rows) || !aligned16(W_UK) || !aligned16(W_UV) || !aligned16(k_c) || !aligned16(v_c))
+    return MLA_ERR_INVALID_ARG;
+  if (!on_handle_device(h)) return MLA_ERR_INVALID_ARG;
+  const mla_config_t& c = h->cfg;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  const int D = c.d_c + c.d_r;
+  {
+    // [k_C | v_C] = [W_UK ; W_UV] c_KV over the rows' latent columns, one launch
+    TcGemm g = tc_base(h);
+    tc_seg(g, 0, W_UK, c.n_h * c.d_h, 0, EPI_STORE, k_c, (long long)c.n_h * c.d_h);
+    tc_seg(g, 1, W_UV, c.n_h * c.d_h, 0, EPI_STORE, v_c, (long long)c.n_h * c.d_h);
+    g.ldw = c.d_c; g.x = rows; g.ldx = D; g.N = n_rows; g.K = c.d_c;
+    const bool tc = use_tc_proj(h, g);
+    if (h->proj_path == MLA_PROJ_TCGEN05 && !tc) return MLA_ERR_UNSUPPORTED;
+    if (tc) {
+      if (launch_gemm_tc(g, h->num_sms, s) != cudaSuccess) return MLA_ERR_CUDA;
+      h->last_launches = 1;
+      return MLA_OK;
+    }
+  }
+  GemmArgs a{};
+  a.batch = 1; a.wlayout = W_NORMAL; a.status = h->status; a.epi = EPI_STORE;
+  a.X = rows; a.ldx = D; a.W = W_UK; a.ldw = c.d_c; a.out = k_c; a.ldo = (long long)c.n_h * c.d_h;
+  a.N = n_rows; a.M = c.n_h * c.d_h; a.K = c.d_c;
+  if (launch_gemm_simt(a, c.dtype, s) != cudaSuccess) return MLA_ERR_CUDA;
+  a.W = W_UV; a.out = v_c;
+  if (launch_gemm_simt(a, c.dtype, s) != cudaSuccess) return MLA_ERR_CUDA;
+  h->last_launches = 2;
+  return MLA_OK;
+}
+
+mla_status_t mla_mha_attn(mla_handle_t h, const void* q, int32_t batch, int32_t n_q, const void* k_c,
+                          const void* v_c, const void* cache, int32_t max_len, const int32_t* q_pos0, void* o,
+                          float* lse, void* stream) {
+  if (!h || batch <= 0 || n_q <= 0 || max_len <= 0 || n_q > max_len || !q || !k_c || !v_c || !cache || !q_pos0 ||
+      !o || !lse)
+    return MLA_ERR_INVALID_ARG;
+  if (!aligned16(q) || !aligned16(k_c) || !aligned16(v_c) || !aligned16(cache) || !aligned16(q_pos0) ||
+      !aligned16(o) || !aligned16(lse))
+    return MLA_ERR_INVALID_ARG;
+  if ((long long)batch * max_len >= (1LL << 31)) return MLA_ERR_INVALID_ARG;
+  if (!on_handle_device(h)) return MLA_ERR_INVALID_ARG;
+  const mla_config_t& c = h->cfg;
+  if (c.d_h > 128) return MLA_ERR_UNSUPPORTED;
+  MhaArgs a{};
+  a.q = q; a.k_c = k_c; a.v_c = v_c; a.cache = cache; a.q_pos0 = q_pos0; a.o = o; a.lse = lse;
+  a.B = batch; a.T = n_q; a.max_len = max_len; a.n_h = c.n_h; a.d_h = c.d_h; a.d_c = c.d_c; a.d_r = c.d_r;
+  a.scale_log2 = h->scale * 1.4426950408889634f;
+  a.wait_cycles = h->wait_cycles;
+  a.status = h->status;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  const bool tc = h->decode_path != MLA_DECODE_SIMT && mha_tc_supported(h);
+  if (h->decode_path == MLA_DECODE_TCGEN05 && !tc) return MLA_ERR_UNSUPPORTED;
+  const cudaError_t e = tc ? launch_mha_tc(a, s) : launch_mha_simt(a, c.dtype, s);
+  if (e != cudaSuccess) return MLA_ERR_CUDA;
+  h->last_launches = 1;
+  return MLA_OK;
+}
+
+mla_status_t mla_project_out(mla_handle_t h, const void* o, int32_t n_tokens, const void* W_O, void* u,
+                             void* stream) {
+  if (!h || n_tokens <= 0 || !o || !W_O || !u) return MLA_ERR_INVALID_ARG;
+  if (!aligned16(o) || !aligned16(W_O) || !aligned16(u)) return MLA_ERR_INVALID_ARG;
+  if (!on_handle_device(h)) return MLA_ERR_INVALID_ARG;
+  const mla_config_t& c = h->cfg;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  const int K = c.n_h * c.d_h;
+  {
+    TcGemm g = tc_base(h);  // u = W_O o
+    tc_seg(g, 0, W_O, c.d, 0, EPI_STORE, u, c.d);
+    g.ldw = K; g.x = o; g.ldx = K; g.N = n_tokens; g.K = K;
+    const bool tc = use_tc_proj(h, g);
+    if (h->proj_path == MLA_PROJ_TCGEN05 && !tc) return MLA_ERR_UNSUPPORTED;
+    if (tc) {
+      if (launch_gemm_tc(g, h->num_sms, s) != cudaSuccess) return MLA_ERR_CUDA;
+      h->last_launches = 1;
+      return MLA_OK;
+    }
+  }
+  GemmArgs a{};
+  a.X = o; a.ldx = K; a.W = W_O; a.ldw = K; a.wlayout = W_NORMAL; a.out = u; a.ldo = c.d;
+  a.N = n_tokens; a.M = c.d; a.K = K; a.batch = 1; a.epi = EPI_STORE; a.status = h->status;
+  if (launch_gemm_simt(a, c.dtype, s) != cudaSuccess) return MLA_ERR_CUDA;
+  h->last_launches = 1;
+  return MLA_OK;
+}
+
 // ------------------------------------------------------------------- S1..S5
 // Workspace of the whole step: q_abs, o_lat and lse, then one region the
 // stages use in turn (c_Q and q_C; the split plan and partials; o).

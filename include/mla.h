@@ -238,6 +238,40 @@ MLA_API mla_status_t mla_absorb_q_premerged(mla_handle_t handle, const void* x, 
 MLA_API mla_status_t mla_out_proj_premerged(mla_handle_t handle, const void* o_lat, int32_t batch,
                                             const void* W_OUV, void* u, void* stream);
 
+/* The MHA path for several new tokens per sequence ([Latent]: at prefill MLA
+   takes the MHA path, K and V restored from the latent; [MiniMind] §10 naive
+   version; §12 causal visibility with a cache). Append the new tokens with
+   mla_append_cache first; then:
+
+   mla_project_q: q [n_tokens, n_h, d_h + d_r] = [W_UQ_i c_Q ; RoPE(W_QR_i c_Q)],
+     c_Q = W_DQ x, RoPE at pos[n] (device int32 [n_tokens], < max_pos).
+     ws: at least mla_absorb_q_workspace_size(handle, n_tokens) bytes.
+   mla_materialise_kv: k_c and v_c [n_rows, n_h, d_h] = W_UK_i c_KV and
+     W_UV_i c_KV for n_rows cache rows `rows` [n_rows, d_c + d_r] (e.g. the
+     whole cache [batch * max_len] rows; rows past a sequence's end produce
+     values that no query reads).
+   mla_mha_attn: for sequence b and query t < n_q at position q_pos0[b] + t
+     (device int32 [batch]; q_pos0[b] + n_q <= max_len, else clamped and
+     flagged MLA_DEV_QPOS_RANGE), causal attention over rows 0..q_pos0[b] + t
+     with k = [k_c[b, r, i] ; k_R of cache row (b, r)], v = v_c[b, r, i],
+     scale 1/sqrt(d_h + d_r).
+       q [batch, n_q, n_h, d_h + d_r], k_c / v_c [batch, max_len, n_h, d_h],
+       cache [batch, max_len, d_c + d_r] (k_R read from its last d_r columns),
+       o [batch, n_q, n_h, d_h] out (normalised), lse [batch, n_q, n_h] fp32 out
+       (natural log). d_h <= 128, else MLA_ERR_UNSUPPORTED.
+   mla_project_out: u [n_tokens, d] = W_O o for o [n_tokens, n_h * d_h].
+   All asynchronous on `stream`; the caller owns every buffer. */
+MLA_API mla_status_t mla_project_q(mla_handle_t handle, const void* x, int32_t n_tokens, const void* W_DQ,
+                                   const void* W_UQ, const void* W_QR, const int32_t* pos, void* q, void* ws,
+                                   size_t ws_bytes, void* stream);
+MLA_API mla_status_t mla_materialise_kv(mla_handle_t handle, const void* rows, int32_t n_rows, const void* W_UK,
+                                        const void* W_UV, void* k_c, void* v_c, void* stream);
+MLA_API mla_status_t mla_mha_attn(mla_handle_t handle, const void* q, int32_t batch, int32_t n_q, const void* k_c,
+                                  const void* v_c, const void* cache, int32_t max_len, const int32_t* q_pos0,
+                                  void* o, float* lse, void* stream);
+MLA_API mla_status_t mla_project_out(mla_handle_t handle, const void* o, int32_t n_tokens, const void* W_O,
+                                     void* u, void* stream);
+
 /* S1..S5 in one call ([MLA] §3-§7; [MiniMind] §9-§12): the new token of
    sequence b (x[b], position pos[b]) is written to cache[b, pos[b], :], the
    absorbed queries are formed, attention covers seqlens[b] rows of sequence b

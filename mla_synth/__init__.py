@@ -212,6 +212,13 @@ def context_h_device(shape: MLAShape, b: int, n_tokens: int, device, start: int 
     return torch.cat(outs, 0) if outs else torch.empty((0, shape.d), device=device)
 
 
+def draw_gaussian(shape: MLAShape, tag: str, dims, sub: int = 0, std: float = 1.0) -> np.ndarray:
+    """A stand-alone tensor of the workload dtype, every element ~ N(0, std^2),
+    from its own seeded stream (tag, sub)."""
+    g = _stream(shape, tag, sub=sub)
+    return to_dtype(g.standard_normal(tuple(dims)) * std, shape.dtype)
+
+
 def draw_latent_rows(shape: MLAShape, n_rows: int, sub: int = 0) -> np.ndarray:
     """Stand-alone cache rows [n, d_c + d_r] with the statistics the append path
     produces under this recipe (every element ~ N(0, 1))."""

@@ -80,6 +80,11 @@ def test_null_handle_is_rejected():
     assert m._c["mla_absorb_q_premerged"](None, None, 1, None, None, None, None, None, None, 0,
                                           None) == m.MLA_ERR_INVALID_ARG
     assert m._c["mla_out_proj_premerged"](None, None, 1, None, None, None) == m.MLA_ERR_INVALID_ARG
+    assert m._c["mla_project_q"](None, None, 1, None, None, None, None, None, None, 0, None) == m.MLA_ERR_INVALID_ARG
+    assert m._c["mla_materialise_kv"](None, None, 1, None, None, None, None, None) == m.MLA_ERR_INVALID_ARG
+    assert m._c["mla_mha_attn"](None, None, 1, 1, None, None, None, 1, None, None, None,
+                                None) == m.MLA_ERR_INVALID_ARG
+    assert m._c["mla_project_out"](None, None, 1, None, None, None) == m.MLA_ERR_INVALID_ARG
 
 
 def test_binding_has_every_declared_function():

@@ -462,6 +462,106 @@ def test_premerged_full_size_v2():
     assert_close(host(dec.u), ref_u, shp.dtype, what="u (pre-merged)")
 
 
+# --------------------------------------------------------------------- the MHA path (several new tokens)
+MHA_CASES = [("tiny", [5, 0], 3), ("minimind", [40, 7, 0], 6), ("v2", [150, 3], 140)]
+
+
+@pytest.mark.parametrize("name", SMALL)
+@pytest.mark.parametrize("proj", PROJ)
+def test_project_q_and_materialise_kv_match_oracle(name, proj):
+    shp = small_shape(name)
+    W = S.draw_weights(shp)
+    N = 37 if name != "tiny" else 5
+    h = S.draw_new_tokens(shp, N)
+    max_pos = 3000
+    pos = np.random.default_rng(17).integers(0, max_pos, size=N)
+    pos[0], pos[-1] = 0, max_pos - 1
+    dec = decoder(shp, make_weights_dev(shp, W), N, 16, max_pos=max_pos)
+    set_proj(dec, proj)
+    q = torch.empty((N, shp.n_h, shp.d_h + shp.d_r), dtype=torch_dtype(shp), device="cuda")
+    M.mla_project_q(dec.handle, dev(h, shp), N, dec.W["W_DQ"], dec.W["W_UQ"], dec.W["W_QR"], dev_i32(pos), q,
+                    dec.ws, dec.ws.numel())
+    ref_q = O.materialised_query(h, W["W_DQ"], W["W_UQ"], W["W_QR"], pos, shp.n_h, shp.d_h, shp.d_r,
+                                 shp.rope_base)
+    assert_close(host(q), ref_q, shp.dtype, what="q")
+    rows = S.draw_latent_rows(shp, 300, sub=21)
+    k_c = torch.empty((300, shp.n_h, shp.d_h), dtype=torch_dtype(shp), device="cuda")
+    v_c = torch.empty_like(k_c)
+    M.mla_materialise_kv(dec.handle, dev(rows, shp), 300, dec.W["W_UK"], dec.W["W_UV"], k_c, v_c)
+    ref_k, ref_v = O.materialised_kv(rows, W["W_UK"], W["W_UV"], shp.n_h, shp.d_h)
+    assert_close(host(k_c), ref_k, shp.dtype, what="k_C")
+    assert_close(host(v_c), ref_v, shp.dtype, what="v_C")
+    assert M.mla_get_device_status(dec.handle) == (M.MLA_OK, 0)
+
+
+@pytest.mark.parametrize("name,ctx,n_q", MHA_CASES)
+@pytest.mark.parametrize("path", ["auto", "simt"])
+def test_mha_attn_matches_oracle(name, ctx, n_q, path):
+    """Causal attention over stand-alone materialised inputs (unit-variance scores)."""
+    shp = small_shape(name)
+    B = len(ctx)
+    max_len = max(ctx) + n_q + 3
+    DQ = shp.d_h + shp.d_r
+    q = S.draw_gaussian(shp, "spare0", (B, n_q, shp.n_h, DQ), sub=1)
+    k_c = S.draw_gaussian(shp, "spare0", (B, max_len, shp.n_h, shp.d_h), sub=2)
+    v_c = S.draw_gaussian(shp, "spare0", (B, max_len, shp.n_h, shp.d_h), sub=3)
+    cache = S.draw_gaussian(shp, "spare0", (B, max_len, shp.D), sub=4)
+    q_pos0 = np.array(ctx)
+    W = {k: np.zeros(shp.weight_shape(k)) for k in S.WEIGHT_NAMES}
+    dec = decoder(shp, {k: torch.zeros(1, device="cuda") for k in W}, B, max_len)
+    if path == "simt":
+        M.mla_set_decode_path(dec.handle, M.MLA_DECODE_SIMT)
+    o = torch.empty((B, n_q, shp.n_h, shp.d_h), dtype=torch_dtype(shp), device="cuda")
+    lse = torch.empty((B, n_q, shp.n_h), dtype=torch.float32, device="cuda")
+    M.mla_mha_attn(dec.handle, dev(q, shp), B, n_q, dev(k_c, shp), dev(v_c, shp), dev(cache, shp), max_len,
+                   dev_i32(q_pos0), o, lse)
+    assert M.mla_get_device_status(dec.handle) == (M.MLA_OK, 0)
+    sc = O.scale_of(shp.d_h, shp.d_r)
+    got_o, got_l = host(o), lse.cpu().numpy().astype(np.float64)
+    for b in range(B):
+        ref_o, ref_l = O.mha_attention(q[b], k_c[b], cache[b][:, shp.d_c:], v_c[b], q_pos0[b] + np.arange(n_q), sc)
+        assert_close(got_o[b], ref_o, shp.dtype, what=f"o seq {b}")
+        assert np.abs(got_l[b] - ref_l).max() <= 2e-4 * max(1.0, np.abs(ref_l).max()), "lse"
+
+
+@pytest.mark.parametrize("name,ctx,n_q", MHA_CASES)
+def test_mha_path_end_to_end(name, ctx, n_q):
+    """New tokens appended, K/V materialised, queries projected, causal MHA and
+    W_O, chained on the GPU, against the oracle's prefill definition."""
+    shp = small_shape(name)
+    B = len(ctx)
+    max_len = max(ctx) + n_q
+    W = S.draw_weights(shp)
+    h_ctx = [S.draw_context_h(shp, b, n) for b, n in enumerate(ctx)]
+    h_new = [S.draw_gaussian(shp, "spare1", (n_q, shp.d), sub=b) for b in range(B)]
+    dec = decoder(shp, make_weights_dev(shp, W), B * n_q, max_len, max_pos=max_len)
+    cache = torch.zeros((B, max_len, shp.D), dtype=torch_dtype(shp), device="cuda")
+    toks = np.concatenate([np.concatenate([h_ctx[b], h_new[b]]) for b in range(B)])
+    seq = np.concatenate([np.full(ctx[b] + n_q, b) for b in range(B)])
+    pos = np.concatenate([np.arange(ctx[b] + n_q) for b in range(B)])
+    dec.append(dev(toks, shp), dev_i32(seq), dev_i32(pos), cache)
+    k_c = torch.empty((B, max_len, shp.n_h, shp.d_h), dtype=torch_dtype(shp), device="cuda")
+    v_c = torch.empty_like(k_c)
+    M.mla_materialise_kv(dec.handle, cache, B * max_len, dec.W["W_UK"], dec.W["W_UV"], k_c, v_c)
+    q = torch.empty((B, n_q, shp.n_h, shp.d_h + shp.d_r), dtype=torch_dtype(shp), device="cuda")
+    qpos = np.concatenate([ctx[b] + np.arange(n_q) for b in range(B)])
+    M.mla_project_q(dec.handle, dev(np.concatenate(h_new), shp), B * n_q, dec.W["W_DQ"], dec.W["W_UQ"],
+                    dec.W["W_QR"], dev_i32(qpos), q, dec.ws, dec.ws.numel())
+    o = torch.empty((B, n_q, shp.n_h, shp.d_h), dtype=torch_dtype(shp), device="cuda")
+    lse = torch.empty((B, n_q, shp.n_h), dtype=torch.float32, device="cuda")
+    M.mla_mha_attn(dec.handle, q, B, n_q, k_c, v_c, cache, max_len, dev_i32(np.array(ctx)), o, lse)
+    u = torch.empty((B * n_q, shp.d), dtype=torch_dtype(shp), device="cuda")
+    M.mla_project_out(dec.handle, o, B * n_q, dec.W["W_O"], u)
+    assert M.mla_get_device_status(dec.handle) == (M.MLA_OK, 0)
+    ref_u, ref_o, ref_l = O.prefill_materialised(h_ctx, h_new, W, shp.n_h, shp.d_h, shp.d_r, shp.rope_base,
+                                                 return_parts=True)
+    got_u = host(u).reshape(B, n_q, shp.d)
+    got_l = lse.cpu().numpy().astype(np.float64)
+    for b in range(B):
+        assert_close(got_u[b], ref_u[b], shp.dtype, tol=TOL_E2E, what=f"u seq {b}")
+        assert np.abs(got_l[b] - ref_l[b]).max() <= TOL_LSE_E2E[shp.dtype], "lse"
+
+
 # --------------------------------------------------------------------- whole step
 def end_to_end(shp, ctx_lens):
     B = len(ctx_lens)
