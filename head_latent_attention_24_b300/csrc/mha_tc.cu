@@ -1,12 +1,362 @@
-// Tensor-core causal multi-head attention over materialised keys and values
-// (the MHA path of several new tokens per sequence): not available yet for
-// any shape; mla_mha_attn uses the CUDA-core kernel.
+// Tensor-core causal multi-head attention over materialised keys and values,
+// for the DeepSeek-V2 head shape (d_h = 128, d_r = 64, bf16): the MHA path of
+// several new tokens per sequence (page "Latent 压缩": at prefill MLA takes the
+// MHA path; page "MiniMind 学习笔记 10", §10 naive version, §12 causal
+// visibility with a cache; page "MLA：潜在表示压缩与解耦 RoPE", §6 k = [k_C ; k_R]
+// with the RoPE key shared by the heads, §7 scale 1/sqrt(d_h + d_r)).
+//
+// One CTA per (128 queries, head, sequence). The query tile (128 x 192, K-major)
+// stays in shared memory; key tiles of 128 rows stream through a two-stage TMA
+// ring, each stage holding k_C (128 x 128), the shared k_R (128 x 64, read
+// straight from the cache rows) and v_C (128 x 128). Per key tile:
+//   S = Q . K^T      M = 128 queries, N = 128 keys, K = 192   (TMEM, double buffer)
+//   P = 2^(S*scale*log2e - m)  in bf16, written by the softmax threads into TMEM
+//   O += P . V       M = 128 queries, N = 128 (d_h), K = 128 keys, A from TMEM
+// Each softmax thread owns one query row (its TMEM lane): the row maximum is
+// its own, the reference maximum moves lazily (only when a tile's maximum rises
+// more than 8 above it, when the thread rescales its row of O in TMEM), and
+// rows a query may not see (later positions) get P = 0; v_C rows past the last
+// query's position are zeroed in shared memory before PV reads them. The QK of
+// tile j+1 runs on the tensor core while the softmax works on tile j.
+//
+// Warp 0 issues TMA, warp 1 owns TMEM and issues the MMAs from one thread,
+// warps 2-5 run the softmax and the epilogue. Every mbarrier wait is bounded;
+// on expiry the CTA records MLA_DEV_TIMEOUT, stops issuing work, waits
+// (bounded) for its own copies in flight and frees its TMEM.
 #include "internal.cuh"
+#include "tc_ptx.cuh"
+#include "tmap.cuh"
 
 namespace mla {
 
-bool mha_tc_supported(const mla_handle_s*) { return false; }
+namespace {
 
-cudaError_t launch_mha_tc(const MhaArgs&, cudaStream_t) { return cudaErrorNotSupported; }
+using namespace tc;
+
+constexpr int DH = 128, DR = 64, DQ = DH + DR;   // the head shape this kernel serves
+constexpr int TQ = 128;                           // queries per CTA (MMA M)
+constexpr int TK = 128;                           // keys per tile (MMA N of QK, K of PV)
+constexpr int NTHREADS = 192;
+constexpr long long WAIT_CYCLES = 4000000000LL;   // ~2 s
+constexpr float kLn2 = 0.693147180559945309f;
+constexpr float RESCALE_THRESHOLD = 8.0f;
+
+constexpr int CHUNK = TK * 128;                   // 16 KB: 128 rows x 64 bf16 (128 B, swizzled)
+constexpr int Q_OFF = 0;                          // 3 chunks: q_C (2), q_R (1)
+constexpr int STAGE = 5 * CHUNK;                  // k_C (2 chunks), k_R (1), v_C (2)
+constexpr int NSTAGE = 2;
+constexpr int RING_OFF = Q_OFF + 3 * CHUNK;
+constexpr int SMEM_DYN = RING_OFF + NSTAGE * STAGE + 1024;
+// TMEM columns
+constexpr uint32_t S_COL = 0;                     // 2 x 128 fp32
+constexpr uint32_t O_COL = 256;                   // 128 fp32
+constexpr uint32_t P_COL = 384;                   // 64: 128 bf16 packed two per column
+constexpr uint32_t TMEM_COLS = 512;
+
+struct Ctl {
+  uint64_t q_full, full[NSTAGE], empty[NSTAGE];
+  uint64_t s_full[2], s_free[2], p_full, pv_done, mma_done;
+  uint32_t tmem_base;
+  int abort;
+  long long wait_limit;
+};
+
+__device__ __forceinline__ bool wait_or_abort(uint64_t* bar, uint32_t parity, Ctl& ctl, int32_t* status) {
+  volatile int* ab = reinterpret_cast<volatile int*>(&ctl.abort);
+  if (*ab) return false;
+  if (mbar_wait_abortable(bar, parity, ctl.wait_limit, ab)) return true;
+  if (!*ab) atomicOr(status, MLA_DEV_TIMEOUT);
+  *ab = 1;
+  return false;
+}
+
+__device__ __forceinline__ void drain_ring(uint64_t* full, int ring, int issued) {
+  for (int s = 0; s < ring; ++s) {
+    if (issued <= s) break;
+    const int last = s + ring * ((issued - 1 - s) / ring);
+    mbar_wait(&full[s], (uint32_t)((last / ring) & 1), WAIT_CYCLES / 8);
+  }
+}
+
+__device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
+  __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
+  return *reinterpret_cast<uint32_t*>(&v);
+}
+
+__global__ void __launch_bounds__(NTHREADS, 1)
+    mha_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ CUtensorMap map_k,
+                  const __grid_constant__ CUtensorMap map_v, const __grid_constant__ CUtensorMap map_kr,
+                  const MhaArgs a) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  __shared__ Ctl ctl;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int q0 = blockIdx.x * TQ, head = blockIdx.y, b = blockIdx.z;
+
+  if (threadIdx.x == 0) {
+    mbar_init(&ctl.q_full, 1);
+    for (int i = 0; i < NSTAGE; ++i) { mbar_init(&ctl.full[i], 1); mbar_init(&ctl.empty[i], 1); }
+    for (int i = 0; i < 2; ++i) { mbar_init(&ctl.s_full[i], 1); mbar_init(&ctl.s_free[i], 4); }
+    mbar_init(&ctl.p_full, 4);
+    mbar_init(&ctl.pv_done, 1);
+    mbar_init(&ctl.mma_done, 1);
+    ctl.abort = 0;
+    ctl.wait_limit = a.wait_cycles > 0 ? a.wait_cycles : WAIT_CYCLES;
+    fence_mbar_init();
+  }
+  if (warp == 1) {
+    tmem_alloc(&ctl.tmem_base, TMEM_COLS);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tbase = ctl.tmem_base;
+  pdl_trigger();
+  pdl_wait();   // q, k_c and v_c come from earlier kernels
+
+  // The queries of this tile sit at positions qp0 .. qp0 + nq - 1 and see keys
+  // 0 .. qp_last; key tiles 0 .. nk - 1 cover them.
+  int pos0 = a.q_pos0[b];
+  if (pos0 < 0 || pos0 > a.max_len - a.T) {
+    if (threadIdx.x == 0 && blockIdx.x == 0 && head == 0) atomicOr(a.status, MLA_DEV_QPOS_RANGE);
+    pos0 = pos0 < 0 ? 0 : a.max_len - a.T;
+  }
+  const int nq = min(TQ, a.T - q0);
+  const int qp0 = pos0 + q0, qp_last = qp0 + nq - 1;
+  const int nk = qp_last / TK + 1;
+  const uint32_t sbase = smem_u32(smem);
+
+  if (warp == 0) {
+    // ------------------------------------------------------------ TMA producer
+    if (lane == 0) {
+      prefetch_tensormap(&map_q);
+      prefetch_tensormap(&map_k);
+      prefetch_tensormap(&map_v);
+      prefetch_tensormap(&map_kr);
+      const int qrow = b * a.T + q0;
+      mbar_arrive_expect_tx(&ctl.q_full, 3 * CHUNK);
+      for (int c = 0; c < 3; ++c) tma_load_2d(smem + Q_OFF + c * CHUNK, &map_q, &ctl.q_full, head * DQ + c * 64, qrow);
+      int i = 0;
+      bool ok = true;
+      for (; i < nk; ++i) {
+        const int st = i % NSTAGE;
+        if (i >= NSTAGE) ok = wait_or_abort(&ctl.empty[st], ((i / NSTAGE) - 1) & 1, ctl, a.status);
+        if (!ok) break;
+        uint8_t* dst = smem + RING_OFF + st * STAGE;
+        const int krow = b * a.max_len + i * TK;
+        mbar_arrive_expect_tx(&ctl.full[st], STAGE);
+        tma_load_2d(dst, &map_k, &ctl.full[st], head * DH, krow);
+        tma_load_2d(dst + CHUNK, &map_k, &ctl.full[st], head * DH + 64, krow);
+        tma_load_2d(dst + 2 * CHUNK, &map_kr, &ctl.full[st], 0, krow);
+        tma_load_2d(dst + 3 * CHUNK, &map_v, &ctl.full[st], head * DH, krow);
+        tma_load_2d(dst + 4 * CHUNK, &map_v, &ctl.full[st], head * DH + 64, krow);
+      }
+      if (!ok) {   // no copy lands after the CTA moves on
+        drain_ring(ctl.full, NSTAGE, i);
+        mbar_wait(&ctl.q_full, 0, WAIT_CYCLES / 8);
+      }
+    }
+  } else if (warp == 1) {
+    // ------------------------------------------------------------ MMA issuer
+    if (lane == 0) {
+      constexpr uint32_t IDESC_QK = idesc_bf16(TQ, TK, false, false);
+      constexpr uint32_t IDESC_PV = idesc_bf16(TQ, DH, false, true);
+      const uint64_t q_desc = sdesc_sw128(sbase + Q_OFF, 16, 1024);
+      const uint64_t k_desc = sdesc_sw128(sbase + RING_OFF, 16, 1024);
+      const uint64_t v_desc = sdesc_sw128(sbase + RING_OFF + 3 * CHUNK, CHUNK, 1024);
+      bool ok = wait_or_abort(&ctl.q_full, 0, ctl, a.status);
+      // S(j) = Q . K(j)^T into buffer j % 2 once stage j has landed and the
+      // softmax has read the buffer's previous tile
+      auto issue_qk = [&](int j) -> bool {
+        const int st = j % NSTAGE, sb = j & 1;
+        if (!wait_or_abort(&ctl.full[st], (j / NSTAGE) & 1, ctl, a.status)) return false;
+        if (j >= 2 && !wait_or_abort(&ctl.s_free[sb], ((j >> 1) - 1) & 1, ctl, a.status)) return false;
+        tc_fence_after();
+        const uint64_t kd = k_desc + (uint64_t)((st * STAGE) >> 4);
+#pragma unroll
+        for (int c = 0; c < 3; ++c)
+#pragma unroll
+          for (int k = 0; k < 4; ++k)
+            mma_bf16(tbase + S_COL + sb * TK, q_desc + (uint64_t)((c * CHUNK + k * 32) >> 4),
+                     kd + (uint64_t)((c * CHUNK + k * 32) >> 4), IDESC_QK, (c > 0 || k > 0) ? 1u : 0u);
+        mma_commit(&ctl.s_full[sb]);
+        return true;
+      };
+      if (ok) ok = issue_qk(0);
+      for (int j = 0; j < nk && ok; ++j) {
+        if (j + 1 < nk) ok = issue_qk(j + 1);
+        // O += P(j) . V(j) once the softmax has written P(j)
+        if (ok) ok = wait_or_abort(&ctl.p_full, j & 1, ctl, a.status);
+        if (!ok) break;
+        tc_fence_after();
+        const int st = j % NSTAGE;
+        const uint64_t vd = v_desc + (uint64_t)((st * STAGE) >> 4);
+#pragma unroll
+        for (int k = 0; k < TK / 16; ++k)
+          mma_bf16_ta(tbase + O_COL, tbase + P_COL + k * 8, vd + (uint64_t)((k * 2048) >> 4), IDESC_PV,
+                      (j > 0 || k > 0) ? 1u : 0u);
+        mma_commit(&ctl.pv_done);
+        mma_commit(&ctl.empty[st]);   // the stage's QK and PV are done
+      }
+      // nothing of this CTA's reaches the tensor cores after it moves on
+      mma_commit(&ctl.mma_done);
+      mbar_wait(&ctl.mma_done, 0, WAIT_CYCLES / 8);
+    }
+  } else {
+    // ------------------------------------------------------------ softmax warps 2..5: one query row each
+    const int quarter = warp & 3;
+    const int r = quarter * 32 + lane;                 // TMEM lane = query row of the tile
+    const uint32_t lane_base = static_cast<uint32_t>(quarter * 32) << 16;
+    const int qp = qp0 + r;                            // this row's position (rows past nq: not stored)
+    const float sl2 = a.scale_log2;
+    float m_ref = -INFINITY, l = 0.f;
+    bool ok = true;
+    for (int j = 0; j < nk && ok; ++j) {
+      const int sb = j & 1, k0 = j * TK;
+      ok = __all_sync(0xffffffffu, wait_or_abort(&ctl.s_full[sb], (j >> 1) & 1, ctl, a.status));
+      if (!ok) break;
+      tc_fence_after();
+      float s[TK];
+#pragma unroll
+      for (int c = 0; c < TK; c += 32) tmem_ld32(tbase + lane_base + S_COL + sb * TK + c, s + c);
+      tmem_ld_wait();
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&ctl.s_free[sb]);
+      // causal mask: key k0 + c is visible to this row when k0 + c <= qp
+      const int nvis = max(0, min(TK, qp - k0 + 1));
+      float mx = -INFINITY;
+#pragma unroll
+      for (int c = 0; c < TK; ++c) {
+        s[c] = c < nvis ? s[c] * sl2 : -INFINITY;
+        mx = fmaxf(mx, s[c]);
+      }
+      float alpha = 1.f;
+      if (mx > m_ref + RESCALE_THRESHOLD) {   // also the first tile a row sees anything (m_ref = -inf)
+        alpha = exp2f(m_ref - mx);
+        m_ref = mx;
+      }
+      uint32_t pk[TK / 2];
+      float lsum = 0.f;
+#pragma unroll
+      for (int c = 0; c < TK; c += 2) {
+        const float p0 = c < nvis ? exp2f(s[c] - m_ref) : 0.f, p1 = c + 1 < nvis ? exp2f(s[c + 1] - m_ref) : 0.f;
+        lsum += p0 + p1;   // the softmax sum from the unrounded weights
+        pk[c / 2] = pack_bf16(p0, p1);
+      }
+      l = l * alpha + lsum;
+      // P(j) replaces P(j-1) in TMEM and O is rescaled: both only after PV(j-1)
+      if (j > 0) {
+        ok = __all_sync(0xffffffffu, wait_or_abort(&ctl.pv_done, (j - 1) & 1, ctl, a.status));
+        if (!ok) break;
+        tc_fence_after();
+        if (__any_sync(0xffffffffu, alpha != 1.f)) {
+#pragma unroll 1
+          for (int c = 0; c < DH; c += 32) {
+            float v[32];
+            tmem_ld32(tbase + lane_base + O_COL + c, v);
+            tmem_ld_wait();
+            uint32_t w[32];
+#pragma unroll
+            for (int e = 0; e < 32; ++e) w[e] = __float_as_uint(v[e] * alpha);
+            tmem_st32(tbase + lane_base + O_COL + c, w);
+          }
+        }
+      }
+      tmem_st32(tbase + lane_base + P_COL, *reinterpret_cast<const uint32_t(*)[32]>(pk));
+      tmem_st32(tbase + lane_base + P_COL + 32, *reinterpret_cast<const uint32_t(*)[32]>(pk + 32));
+      asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
+      // the last tile's v_C rows past the last query's position may hold
+      // anything (rows no query of this tile may see): zero them in the stage
+      // before PV reads it (each warp a share of the rows; its p_full arrival
+      // below publishes them)
+      if (j == nk - 1 && qp_last - k0 + 1 < TK) {
+        const int st = j % NSTAGE;
+        ok = __all_sync(0xffffffffu, wait_or_abort(&ctl.full[st], (j / NSTAGE) & 1, ctl, a.status));
+        if (!ok) break;
+        const int first = qp_last - k0 + 1;   // rows first .. TK-1 of both v_C chunks
+        uint8_t* vbase = smem + RING_OFF + st * STAGE + 3 * CHUNK;
+        const int tid = threadIdx.x - 64;
+        for (int w = tid; w < (TK - first) * 16; w += 128) {
+          const int row = first + w / 16, part = w % 16;   // 8 x 16 B per row and chunk
+          *reinterpret_cast<uint4*>(vbase + (part >> 3) * CHUNK + row * 128 + (part & 7) * 16) =
+              make_uint4(0, 0, 0, 0);
+        }
+        fence_proxy_async_smem();
+      }
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&ctl.p_full);
+    }
+    // ---------------------------------------------------------------- epilogue
+    if (ok) ok = __all_sync(0xffffffffu, wait_or_abort(&ctl.pv_done, (nk - 1) & 1, ctl, a.status));
+    if (ok) {
+      tc_fence_after();
+      const float inv_l = l > 0.f ? 1.f / l : 0.f;
+      const bool store = r < nq;
+      __nv_bfloat16* orow = static_cast<__nv_bfloat16*>(a.o) + (((size_t)b * a.T + q0 + r) * a.n_h + head) * DH;
+#pragma unroll 1
+      for (int c = 0; c < DH; c += 32) {
+        float v[32];
+        tmem_ld32(tbase + lane_base + O_COL + c, v);
+        tmem_ld_wait();
+        if (store) {
+#pragma unroll
+          for (int e = 0; e < 32; e += 8)
+            *reinterpret_cast<uint4*>(orow + c + e) =
+                make_uint4(pack_bf16(v[e] * inv_l, v[e + 1] * inv_l), pack_bf16(v[e + 2] * inv_l, v[e + 3] * inv_l),
+                           pack_bf16(v[e + 4] * inv_l, v[e + 5] * inv_l), pack_bf16(v[e + 6] * inv_l, v[e + 7] * inv_l));
+        }
+      }
+      if (store) a.lse[((size_t)b * a.T + q0 + r) * a.n_h + head] = (m_ref + log2f(l)) * kLn2;
+    }
+  }
+
+  // ------------------------------------------------------------------ teardown
+  __syncwarp();
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  if (warp == 1) tmem_dealloc(tbase, TMEM_COLS);
+}
+
+}  // namespace
+
+bool mha_tc_supported(const mla_handle_s* h) {
+  const mla_config_t& c = h->cfg;
+  return c.dtype == MLA_BF16 && c.d_h == DH && c.d_r == DR && c.d_c % 8 == 0;
+}
+
+cudaError_t launch_mha_tc(const MhaArgs& a, cudaStream_t s) {
+  if (a.d_h != DH || a.d_r != DR || a.T <= 0 || a.B <= 0 || a.n_h <= 0) return cudaErrorInvalidValue;
+  if (a.n_h > 65535 || a.B > 65535) return cudaErrorInvalidValue;
+  const int D = a.d_c + a.d_r;
+  CUtensorMap map_q, map_k, map_v, map_kr;
+  // q [B*T rows][n_h * 192], k_c / v_c [B*max_len rows][n_h * 128], the cache's
+  // RoPE columns [B*max_len rows][64] from column d_c: boxes of 64 x 128 rows
+  if (!make_tmap_2d_bf16(&map_q, a.q, (uint64_t)a.n_h * DQ, (uint64_t)a.B * a.T, (uint64_t)a.n_h * DQ * 2, 64, TQ,
+                         128))
+    return cudaErrorInvalidValue;
+  if (!make_tmap_2d_bf16(&map_k, a.k_c, (uint64_t)a.n_h * DH, (uint64_t)a.B * a.max_len, (uint64_t)a.n_h * DH * 2, 64,
+                         TK, 128))
+    return cudaErrorInvalidValue;
+  if (!make_tmap_2d_bf16(&map_v, a.v_c, (uint64_t)a.n_h * DH, (uint64_t)a.B * a.max_len, (uint64_t)a.n_h * DH * 2, 64,
+                         TK, 128))
+    return cudaErrorInvalidValue;
+  const char* rope = static_cast<const char*>(a.cache) + (size_t)a.d_c * 2;
+  if (!make_tmap_2d_bf16(&map_kr, rope, DR, (uint64_t)a.B * a.max_len, (uint64_t)D * 2, 64, TK, 128))
+    return cudaErrorInvalidValue;
+  static bool attr_set = false;
+  if (!attr_set) {
+    cudaError_t e = cudaFuncSetAttribute(mha_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_DYN);
+    if (e != cudaSuccess) return e;
+    attr_set = true;
+  }
+  LaunchCfg lc(dim3((unsigned)((a.T + TQ - 1) / TQ), (unsigned)a.n_h, (unsigned)a.B), dim3(NTHREADS), SMEM_DYN, s);
+  cudaError_t e = cudaLaunchKernelEx(&lc.cfg, mha_tc_kernel, map_q, map_k, map_v, map_kr, a);
+  if (e != cudaSuccess) return e;
+  return cudaGetLastError();
+}
 
 }  // namespace mla

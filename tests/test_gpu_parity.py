@@ -7,7 +7,7 @@ import pytest
 
 import mla_synth as S
 from oracle import mla as O
-from gpu_helpers import (TOL, TOL_E2E, TOL_LSE_E2E, assert_close, dev, dev_i32, host, make_weights_dev, decoder,
+from gpu_helpers import (TOL, TOL_E2E, TOL_LSE_E2E, TOL_LSE_E2E_MANY, assert_close, dev, dev_i32, host, make_weights_dev, decoder,
                          torch_dtype)
 
 pytestmark = pytest.mark.gpu
@@ -463,7 +463,7 @@ def test_premerged_full_size_v2():
 
 
 # --------------------------------------------------------------------- the MHA path (several new tokens)
-MHA_CASES = [("tiny", [5, 0], 3), ("minimind", [40, 7, 0], 6), ("v2", [150, 3], 140)]
+MHA_CASES = [("tiny", [5, 0], 3), ("minimind", [40, 7, 0], 6), ("v2", [150, 3], 140), ("v2", [0, 77], 300)]
 
 
 @pytest.mark.parametrize("name", SMALL)
@@ -559,7 +559,7 @@ def test_mha_path_end_to_end(name, ctx, n_q):
     got_l = lse.cpu().numpy().astype(np.float64)
     for b in range(B):
         assert_close(got_u[b], ref_u[b], shp.dtype, tol=TOL_E2E, what=f"u seq {b}")
-        assert np.abs(got_l[b] - ref_l[b]).max() <= TOL_LSE_E2E[shp.dtype], "lse"
+        assert np.abs(got_l[b] - ref_l[b]).max() <= TOL_LSE_E2E_MANY[shp.dtype], "lse"
 
 
 # --------------------------------------------------------------------- whole step
