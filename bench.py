@@ -309,6 +309,75 @@ def premerged_comparison(M, dec, shp, h_new, pos, device, iters: int = 15):
     return res
 
 
+def prefill_workload(device, peaks, B: int = 2, T: int = 4096, iters: int = 10):
+    """The MHA path on the V2 shape for T new tokens per sequence (no earlier
+    context): K/V materialised for the T cache rows, queries projected, causal
+    multi-head attention, W_O. Times each call (CUDA events, median) and the
+    attention's FLOP rate against the burst bf16 peak (causal: query t attends
+    t + 1 rows; 2 * n_h * (d_h + d_r + d_h) FLOPs per query-row pair)."""
+    import torch
+    import head_latent_attention_24_b300 as M
+    shp = v2_shape()
+    n_h, d_h, d_r, d_c, d = shp.n_h, shp.d_h, shp.d_r, shp.d_c, shp.d
+    g = torch.Generator(device=device)
+    g.manual_seed(shp.seed + 7)
+
+    def w(r, c):
+        return (torch.randn((r, c), generator=g, device=device) / c ** 0.5).to(torch.bfloat16)
+
+    W = {"W_DKV": w(d_c, d), "W_KR": w(d_r, d), "W_DQ": w(shp.d_cq, d), "W_UQ": w(n_h * d_h, shp.d_cq),
+         "W_QR": w(n_h * d_r, shp.d_cq), "W_UK": w(n_h * d_h, d_c), "W_UV": w(n_h * d_h, d_c), "W_O": w(d, n_h * d_h)}
+    h = M.mla_create(d, n_h, d_h, d_c, d_r, shp.d_cq, M.MLA_BF16, T)
+    try:
+        x = torch.randn((B * T, d), generator=g, device=device).to(torch.bfloat16)
+        cache = torch.zeros((B, T, shp.D), dtype=torch.bfloat16, device=device)
+        seq = torch.arange(B, dtype=torch.int32, device=device).repeat_interleave(T)
+        pos = torch.arange(T, dtype=torch.int32, device=device).repeat(B)
+        k_c = torch.empty((B, T, n_h, d_h), dtype=torch.bfloat16, device=device)
+        v_c = torch.empty_like(k_c)
+        q = torch.empty((B, T, n_h, d_h + d_r), dtype=torch.bfloat16, device=device)
+        o = torch.empty((B, T, n_h, d_h), dtype=torch.bfloat16, device=device)
+        lse = torch.empty((B, T, n_h), dtype=torch.float32, device=device)
+        u = torch.empty((B * T, d), dtype=torch.bfloat16, device=device)
+        ws = torch.empty(M.mla_absorb_q_workspace_size(h, B * T), dtype=torch.uint8, device=device)
+        q_pos0 = torch.zeros(B, dtype=torch.int32, device=device)
+        calls = {
+            "append": lambda: M.mla_append_cache(h, x, B * T, W["W_DKV"], W["W_KR"], seq, pos, cache, B, T),
+            "materialise_kv": lambda: M.mla_materialise_kv(h, cache, B * T, W["W_UK"], W["W_UV"], k_c, v_c),
+            "project_q": lambda: M.mla_project_q(h, x, B * T, W["W_DQ"], W["W_UQ"], W["W_QR"], pos, q, ws,
+                                                 ws.numel()),
+            "mha_attn": lambda: M.mla_mha_attn(h, q, B, T, k_c, v_c, cache, T, q_pos0, o, lse),
+            "project_out": lambda: M.mla_project_out(h, o, B * T, W["W_O"], u),
+        }
+        out = {"batch": B, "new_tokens": T, "context": 0}
+        for name, fn in calls.items():
+            for _ in range(2):
+                fn()
+            torch.cuda.synchronize()
+            ts = []
+            for _ in range(iters):
+                e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                e0.record()
+                fn()
+                e1.record()
+                torch.cuda.synchronize()
+                ts.append(e0.elapsed_time(e1) * 1e3)
+            out[name + "_us"] = round(statistics.median(ts), 1)
+        st, bits = M.mla_get_device_status(h)
+        if st != M.MLA_OK:
+            raise RuntimeError(f"prefill: device status {st} bits {bits}")
+        flops = 2.0 * B * n_h * (2 * d_h + d_r) * (T * (T + 1) / 2)
+        t_attn = out["mha_attn_us"] * 1e-6
+        out["mha_attn_tflops"] = round(flops / t_attn / 1e12, 1)
+        out["mha_attn_frac_of_burst_bf16"] = round(flops / t_attn / 1e12 / peaks["bf16_tflops"], 4)
+        total = sum(out[k + "_us"] for k in calls)
+        out["tokens_per_s"] = round(B * T / (total * 1e-6), 1)
+        return out
+    finally:
+        M.mla_destroy(h)
+        torch.cuda.empty_cache()
+
+
 def h_chunks(M, h, B, max_len, device):
     """Split-KV chunk count the attention call uses (CTA pairs of the
     tensor-core kernel): from the SM count."""
@@ -598,6 +667,7 @@ def run_ours(args, rank, world, local_rank):
     if world == 1 and not args.no_workloads:
         out["attention_workloads"] = attention_workloads(device, peaks)
         out["premerged_comparison"] = premerged_comparison(M, dec, shp, h_new, pos, device)
+        out["prefill"] = prefill_workload(device, peaks)
     if world == 1 and not args.no_cpu_baseline:
         import mla_synth as S
 

@@ -136,7 +136,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
       prefetch_tensormap(&map_kr);
       const int qrow = b * a.T + q0;
       mbar_arrive_expect_tx(&ctl.q_full, 3 * CHUNK);
-      for (int c = 0; c < 3; ++c) tma_load_2d(smem + Q_OFF + c * CHUNK, &map_q, &ctl.q_full, head * DQ + c * 64, qrow);
+      tma_load_3d(smem + Q_OFF, &map_q, &ctl.q_full, 0, qrow, head * 3);
       int i = 0;
       bool ok = true;
       for (; i < nk; ++i) {
@@ -146,11 +146,9 @@ __global__ void __launch_bounds__(NTHREADS, 1)
         uint8_t* dst = smem + RING_OFF + st * STAGE;
         const int krow = b * a.max_len + i * TK;
         mbar_arrive_expect_tx(&ctl.full[st], STAGE);
-        tma_load_2d(dst, &map_k, &ctl.full[st], head * DH, krow);
-        tma_load_2d(dst + CHUNK, &map_k, &ctl.full[st], head * DH + 64, krow);
+        tma_load_3d(dst, &map_k, &ctl.full[st], 0, krow, head * 2);
         tma_load_2d(dst + 2 * CHUNK, &map_kr, &ctl.full[st], 0, krow);
-        tma_load_2d(dst + 3 * CHUNK, &map_v, &ctl.full[st], head * DH, krow);
-        tma_load_2d(dst + 4 * CHUNK, &map_v, &ctl.full[st], head * DH + 64, krow);
+        tma_load_3d(dst + 3 * CHUNK, &map_v, &ctl.full[st], 0, krow, head * 2);
       }
       if (!ok) {   // no copy lands after the CTA moves on
         drain_ring(ctl.full, NSTAGE, i);
@@ -234,14 +232,15 @@ __global__ void __launch_bounds__(NTHREADS, 1)
       }
       float alpha = 1.f;
       if (mx > m_ref + RESCALE_THRESHOLD) {   // also the first tile a row sees anything (m_ref = -inf)
-        alpha = exp2f(m_ref - mx);
+        alpha = ex2_approx(m_ref - mx);
         m_ref = mx;
       }
       uint32_t pk[TK / 2];
       float lsum = 0.f;
 #pragma unroll
       for (int c = 0; c < TK; c += 2) {
-        const float p0 = c < nvis ? exp2f(s[c] - m_ref) : 0.f, p1 = c + 1 < nvis ? exp2f(s[c + 1] - m_ref) : 0.f;
+        const float p0 = c < nvis ? ex2_approx(s[c] - m_ref) : 0.f;
+        const float p1 = c + 1 < nvis ? ex2_approx(s[c + 1] - m_ref) : 0.f;
         lsum += p0 + p1;   // the softmax sum from the unrounded weights
         pk[c / 2] = pack_bf16(p0, p1);
       }
@@ -333,17 +332,23 @@ cudaError_t launch_mha_tc(const MhaArgs& a, cudaStream_t s) {
   if (a.n_h > 65535 || a.B > 65535) return cudaErrorInvalidValue;
   const int D = a.d_c + a.d_r;
   CUtensorMap map_q, map_k, map_v, map_kr;
-  // q [B*T rows][n_h * 192], k_c / v_c [B*max_len rows][n_h * 128], the cache's
-  // RoPE columns [B*max_len rows][64] from column d_c: boxes of 64 x 128 rows
-  if (!make_tmap_2d_bf16(&map_q, a.q, (uint64_t)a.n_h * DQ, (uint64_t)a.B * a.T, (uint64_t)a.n_h * DQ * 2, 64, TQ,
-                         128))
-    return cudaErrorInvalidValue;
-  if (!make_tmap_2d_bf16(&map_k, a.k_c, (uint64_t)a.n_h * DH, (uint64_t)a.B * a.max_len, (uint64_t)a.n_h * DH * 2, 64,
-                         TK, 128))
-    return cudaErrorInvalidValue;
-  if (!make_tmap_2d_bf16(&map_v, a.v_c, (uint64_t)a.n_h * DH, (uint64_t)a.B * a.max_len, (uint64_t)a.n_h * DH * 2, 64,
-                         TK, 128))
-    return cudaErrorInvalidValue;
+  // q [B*T rows][n_h * 192] and k_c / v_c [B*max_len rows][n_h * 128] through
+  // 3-D views {64 columns, rows, 64-column chunks} (chunk outermost), so one
+  // box brings a head's 3 (q) or 2 (k_c, v_c) chunks of 128 rows chunk-major:
+  // one TMA operation each, the operation count (not the bytes) being what
+  // limits an SM's copy rate for 16 KB boxes. The cache's RoPE columns
+  // [B*max_len rows][64] from column d_c: one 64 x 128-row box.
+  {
+    const uint64_t dq[3] = {64, (uint64_t)a.B * a.T, (uint64_t)a.n_h * 3};
+    const uint64_t sq[2] = {(uint64_t)a.n_h * DQ * 2, 128};
+    const uint32_t bq[3] = {64, TQ, 3};
+    if (!make_tmap_3d_bf16_sw128(&map_q, a.q, dq, sq, bq)) return cudaErrorInvalidValue;
+    const uint64_t dk[3] = {64, (uint64_t)a.B * a.max_len, (uint64_t)a.n_h * 2};
+    const uint64_t sk[2] = {(uint64_t)a.n_h * DH * 2, 128};
+    const uint32_t bk[3] = {64, TK, 2};
+    if (!make_tmap_3d_bf16_sw128(&map_k, a.k_c, dk, sk, bk)) return cudaErrorInvalidValue;
+    if (!make_tmap_3d_bf16_sw128(&map_v, a.v_c, dk, sk, bk)) return cudaErrorInvalidValue;
+  }
   const char* rope = static_cast<const char*>(a.cache) + (size_t)a.d_c * 2;
   if (!make_tmap_2d_bf16(&map_kr, rope, DR, (uint64_t)a.B * a.max_len, (uint64_t)D * 2, 64, TK, 128))
     return cudaErrorInvalidValue;
