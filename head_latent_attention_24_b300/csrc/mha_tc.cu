@@ -12,15 +12,17 @@
 //   S = Q . K^T      M = 128 queries, N = 128 keys, K = 192   (TMEM, double buffer)
 //   P = 2^(S*scale*log2e - m)  in bf16, written by the softmax threads into TMEM
 //   O += P . V       M = 128 queries, N = 128 (d_h), K = 128 keys, A from TMEM
-// Each softmax thread owns one query row (its TMEM lane): the row maximum is
-// its own, the reference maximum moves lazily (only when a tile's maximum rises
+// Each query row (a TMEM lane) belongs to two softmax threads, one per half of
+// the key tile; they exchange the row's tile maximum, the reference maximum
+// moves lazily (only when a tile's maximum rises
 // more than 8 above it, when the thread rescales its row of O in TMEM), and
 // rows a query may not see (later positions) get P = 0; v_C rows past the last
 // query's position are zeroed in shared memory before PV reads them. The QK of
 // tile j+1 runs on the tensor core while the softmax works on tile j.
 //
-// Warp 0 issues TMA, warp 1 owns TMEM and issues the MMAs from one thread,
-// warps 2-5 run the softmax and the epilogue. Every mbarrier wait is bounded;
+// Warp 0 issues TMA, warp 1 owns TMEM and issues the QK MMAs, warp 2 the PV
+// MMAs, warps 3-10 run the softmax and the epilogue (two warps per query row,
+// each with half of the tile's keys). Every mbarrier wait is bounded;
 // on expiry the CTA records MLA_DEV_TIMEOUT, stops issuing work, waits
 // (bounded) for its own copies in flight and frees its TMEM.
 #include "internal.cuh"
@@ -36,7 +38,7 @@ using namespace tc;
 constexpr int DH = 128, DR = 64, DQ = DH + DR;   // the head shape this kernel serves
 constexpr int TQ = 128;                           // queries per CTA (MMA M)
 constexpr int TK = 128;                           // keys per tile (MMA N of QK, K of PV)
-constexpr int NTHREADS = 192;
+constexpr int NTHREADS = 352;
 constexpr long long WAIT_CYCLES = 4000000000LL;   // ~2 s
 constexpr float kLn2 = 0.693147180559945309f;
 constexpr float RESCALE_THRESHOLD = 8.0f;
@@ -59,6 +61,8 @@ struct Ctl {
   uint32_t tmem_base;
   int abort;
   long long wait_limit;
+  float mx[2][2][TQ];   // per tile parity, key half and query row: the half's tile maximum
+  float ls[2][TQ];      // per key half and query row: the half's softmax sum
 };
 
 __device__ __forceinline__ bool wait_or_abort(uint64_t* bar, uint32_t parity, Ctl& ctl, int32_t* status) {
@@ -76,6 +80,21 @@ __device__ __forceinline__ void drain_ring(uint64_t* full, int ring, int issued)
     const int last = s + ring * ((issued - 1 - s) / ring);
     mbar_wait(&full[s], (uint32_t)((last / ring) & 1), WAIT_CYCLES / 8);
   }
+}
+
+// The two softmax warps of TMEM lane quarter q (named barrier 1 + q, 64 threads).
+__device__ __forceinline__ void pair_sync(int quarter) {
+  asm volatile("bar.sync %0, 64;" ::"r"(1 + quarter) : "memory");
+}
+__device__ __forceinline__ bool pair_all(int quarter, bool v) {
+  uint32_t out;
+  asm volatile(
+      "{\n .reg .pred pi, po;\n setp.ne.u32 pi, %1, 0;\n barrier.cta.red.and.pred po, %2, 64, pi;\n"
+      " selp.u32 %0, 1, 0, po;\n}\n"
+      : "=r"(out)
+      : "r"((uint32_t)v), "r"(1 + quarter)
+      : "memory");
+  return out != 0;
 }
 
 __device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
@@ -96,10 +115,10 @@ __global__ void __launch_bounds__(NTHREADS, 1)
   if (threadIdx.x == 0) {
     mbar_init(&ctl.q_full, 1);
     for (int i = 0; i < NSTAGE; ++i) { mbar_init(&ctl.full[i], 1); mbar_init(&ctl.empty[i], 1); }
-    for (int i = 0; i < 2; ++i) { mbar_init(&ctl.s_full[i], 1); mbar_init(&ctl.s_free[i], 4); }
-    mbar_init(&ctl.p_full, 4);
+    for (int i = 0; i < 2; ++i) { mbar_init(&ctl.s_full[i], 1); mbar_init(&ctl.s_free[i], 8); }
+    mbar_init(&ctl.p_full, 8);
     mbar_init(&ctl.pv_done, 1);
-    mbar_init(&ctl.mma_done, 1);
+    mbar_init(&ctl.mma_done, 2);
     ctl.abort = 0;
     ctl.wait_limit = a.wait_cycles > 0 ? a.wait_cycles : WAIT_CYCLES;
     fence_mbar_init();
@@ -156,20 +175,20 @@ __global__ void __launch_bounds__(NTHREADS, 1)
       }
     }
   } else if (warp == 1) {
-    // ------------------------------------------------------------ MMA issuer
+    // ------------------------------------------------------------ QK issuer
+    // S(j) = Q . K(j)^T into buffer j % 2 once stage j has landed and the
+    // softmax has read the buffer's previous tile. QK and PV have an issuing
+    // thread each, so that a PV never waits behind the next tile's load.
     if (lane == 0) {
       constexpr uint32_t IDESC_QK = idesc_bf16(TQ, TK, false, false);
-      constexpr uint32_t IDESC_PV = idesc_bf16(TQ, DH, false, true);
       const uint64_t q_desc = sdesc_sw128(sbase + Q_OFF, 16, 1024);
       const uint64_t k_desc = sdesc_sw128(sbase + RING_OFF, 16, 1024);
-      const uint64_t v_desc = sdesc_sw128(sbase + RING_OFF + 3 * CHUNK, CHUNK, 1024);
       bool ok = wait_or_abort(&ctl.q_full, 0, ctl, a.status);
-      // S(j) = Q . K(j)^T into buffer j % 2 once stage j has landed and the
-      // softmax has read the buffer's previous tile
-      auto issue_qk = [&](int j) -> bool {
+      for (int j = 0; j < nk && ok; ++j) {
         const int st = j % NSTAGE, sb = j & 1;
-        if (!wait_or_abort(&ctl.full[st], (j / NSTAGE) & 1, ctl, a.status)) return false;
-        if (j >= 2 && !wait_or_abort(&ctl.s_free[sb], ((j >> 1) - 1) & 1, ctl, a.status)) return false;
+        ok = wait_or_abort(&ctl.full[st], (j / NSTAGE) & 1, ctl, a.status) &&
+             (j < 2 || wait_or_abort(&ctl.s_free[sb], ((j >> 1) - 1) & 1, ctl, a.status));
+        if (!ok) break;
         tc_fence_after();
         const uint64_t kd = k_desc + (uint64_t)((st * STAGE) >> 4);
 #pragma unroll
@@ -179,13 +198,21 @@ __global__ void __launch_bounds__(NTHREADS, 1)
             mma_bf16(tbase + S_COL + sb * TK, q_desc + (uint64_t)((c * CHUNK + k * 32) >> 4),
                      kd + (uint64_t)((c * CHUNK + k * 32) >> 4), IDESC_QK, (c > 0 || k > 0) ? 1u : 0u);
         mma_commit(&ctl.s_full[sb]);
-        return true;
-      };
-      if (ok) ok = issue_qk(0);
+      }
+      // nothing of this CTA's reaches the tensor cores after it moves on
+      mma_commit(&ctl.mma_done);
+      mbar_wait(&ctl.mma_done, 0, WAIT_CYCLES / 8);
+    }
+  } else if (warp == 2) {
+    // ------------------------------------------------------------ PV issuer
+    // O += P(j) . V(j) once the softmax has written P(j); the stage is free
+    // when this PV completes (its QK completed before P(j) existed).
+    if (lane == 0) {
+      constexpr uint32_t IDESC_PV = idesc_bf16(TQ, DH, false, true);
+      const uint64_t v_desc = sdesc_sw128(sbase + RING_OFF + 3 * CHUNK, CHUNK, 1024);
+      bool ok = true;
       for (int j = 0; j < nk && ok; ++j) {
-        if (j + 1 < nk) ok = issue_qk(j + 1);
-        // O += P(j) . V(j) once the softmax has written P(j)
-        if (ok) ok = wait_or_abort(&ctl.p_full, j & 1, ctl, a.status);
+        ok = wait_or_abort(&ctl.p_full, j & 1, ctl, a.status);
         if (!ok) break;
         tc_fence_after();
         const int st = j % NSTAGE;
@@ -195,89 +222,95 @@ __global__ void __launch_bounds__(NTHREADS, 1)
           mma_bf16_ta(tbase + O_COL, tbase + P_COL + k * 8, vd + (uint64_t)((k * 2048) >> 4), IDESC_PV,
                       (j > 0 || k > 0) ? 1u : 0u);
         mma_commit(&ctl.pv_done);
-        mma_commit(&ctl.empty[st]);   // the stage's QK and PV are done
+        mma_commit(&ctl.empty[st]);
       }
-      // nothing of this CTA's reaches the tensor cores after it moves on
       mma_commit(&ctl.mma_done);
       mbar_wait(&ctl.mma_done, 0, WAIT_CYCLES / 8);
     }
   } else {
-    // ------------------------------------------------------------ softmax warps 2..5: one query row each
-    const int quarter = warp & 3;
+    // ------------------------------------------------------------ softmax warps 3..10
+    // Two warps per TMEM lane quarter: warps 3..6 and 7..10 share query rows
+    // 32q..32q+31 (one row per lane), each taking 64 of the tile's keys and 64
+    // of O's columns; they meet (named barrier 1+q, 64 threads) to agree on
+    // every wait's outcome and to exchange row maxima and sums.
+    const int quarter = warp & 3, half = (warp - 3) >> 2;
     const int r = quarter * 32 + lane;                 // TMEM lane = query row of the tile
     const uint32_t lane_base = static_cast<uint32_t>(quarter * 32) << 16;
     const int qp = qp0 + r;                            // this row's position (rows past nq: not stored)
     const float sl2 = a.scale_log2;
+    constexpr int HK = TK / 2;                         // keys per half
     float m_ref = -INFINITY, l = 0.f;
     bool ok = true;
     for (int j = 0; j < nk && ok; ++j) {
-      const int sb = j & 1, k0 = j * TK;
-      ok = __all_sync(0xffffffffu, wait_or_abort(&ctl.s_full[sb], (j >> 1) & 1, ctl, a.status));
+      const int sb = j & 1, k0 = j * TK + half * HK;
+      ok = pair_all(quarter, __all_sync(0xffffffffu, wait_or_abort(&ctl.s_full[sb], (j >> 1) & 1, ctl, a.status)));
       if (!ok) break;
       tc_fence_after();
-      float s[TK];
-#pragma unroll
-      for (int c = 0; c < TK; c += 32) tmem_ld32(tbase + lane_base + S_COL + sb * TK + c, s + c);
+      float s[HK];
+      tmem_ld32(tbase + lane_base + S_COL + sb * TK + half * HK, s);
+      tmem_ld32(tbase + lane_base + S_COL + sb * TK + half * HK + 32, s + 32);
       tmem_ld_wait();
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(&ctl.s_free[sb]);
       // causal mask: key k0 + c is visible to this row when k0 + c <= qp
-      const int nvis = max(0, min(TK, qp - k0 + 1));
+      const int nvis = max(0, min(HK, qp - k0 + 1));
       float mx = -INFINITY;
 #pragma unroll
-      for (int c = 0; c < TK; ++c) {
+      for (int c = 0; c < HK; ++c) {
         s[c] = c < nvis ? s[c] * sl2 : -INFINITY;
         mx = fmaxf(mx, s[c]);
       }
+      ctl.mx[j & 1][half][r] = mx;
+      pair_sync(quarter);
+      mx = fmaxf(mx, ctl.mx[j & 1][half ^ 1][r]);   // the row's tile maximum, the same in both halves
       float alpha = 1.f;
       if (mx > m_ref + RESCALE_THRESHOLD) {   // also the first tile a row sees anything (m_ref = -inf)
         alpha = ex2_approx(m_ref - mx);
         m_ref = mx;
       }
-      uint32_t pk[TK / 2];
+      uint32_t pk[HK / 2];
       float lsum = 0.f;
 #pragma unroll
-      for (int c = 0; c < TK; c += 2) {
+      for (int c = 0; c < HK; c += 2) {
         const float p0 = c < nvis ? ex2_approx(s[c] - m_ref) : 0.f;
         const float p1 = c + 1 < nvis ? ex2_approx(s[c + 1] - m_ref) : 0.f;
         lsum += p0 + p1;   // the softmax sum from the unrounded weights
         pk[c / 2] = pack_bf16(p0, p1);
       }
-      l = l * alpha + lsum;
+      l = l * alpha + lsum;   // this half's share of the row sum
       // P(j) replaces P(j-1) in TMEM and O is rescaled: both only after PV(j-1)
       if (j > 0) {
-        ok = __all_sync(0xffffffffu, wait_or_abort(&ctl.pv_done, (j - 1) & 1, ctl, a.status));
+        ok = pair_all(quarter, __all_sync(0xffffffffu, wait_or_abort(&ctl.pv_done, (j - 1) & 1, ctl, a.status)));
         if (!ok) break;
         tc_fence_after();
         if (__any_sync(0xffffffffu, alpha != 1.f)) {
 #pragma unroll 1
-          for (int c = 0; c < DH; c += 32) {
+          for (int c = 0; c < DH / 2; c += 32) {
             float v[32];
-            tmem_ld32(tbase + lane_base + O_COL + c, v);
+            tmem_ld32(tbase + lane_base + O_COL + half * (DH / 2) + c, v);
             tmem_ld_wait();
             uint32_t w[32];
 #pragma unroll
             for (int e = 0; e < 32; ++e) w[e] = __float_as_uint(v[e] * alpha);
-            tmem_st32(tbase + lane_base + O_COL + c, w);
+            tmem_st32(tbase + lane_base + O_COL + half * (DH / 2) + c, w);
           }
         }
       }
-      tmem_st32(tbase + lane_base + P_COL, *reinterpret_cast<const uint32_t(*)[32]>(pk));
-      tmem_st32(tbase + lane_base + P_COL + 32, *reinterpret_cast<const uint32_t(*)[32]>(pk + 32));
+      tmem_st32(tbase + lane_base + P_COL + half * (HK / 2), pk);
       asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
       // the last tile's v_C rows past the last query's position may hold
       // anything (rows no query of this tile may see): zero them in the stage
       // before PV reads it (each warp a share of the rows; its p_full arrival
       // below publishes them)
-      if (j == nk - 1 && qp_last - k0 + 1 < TK) {
+      if (j == nk - 1 && qp_last - j * TK + 1 < TK) {
         const int st = j % NSTAGE;
-        ok = __all_sync(0xffffffffu, wait_or_abort(&ctl.full[st], (j / NSTAGE) & 1, ctl, a.status));
+        ok = pair_all(quarter, __all_sync(0xffffffffu, wait_or_abort(&ctl.full[st], (j / NSTAGE) & 1, ctl, a.status)));
         if (!ok) break;
-        const int first = qp_last - k0 + 1;   // rows first .. TK-1 of both v_C chunks
+        const int first = qp_last - j * TK + 1;   // rows first .. TK-1 of both v_C chunks
         uint8_t* vbase = smem + RING_OFF + st * STAGE + 3 * CHUNK;
-        const int tid = threadIdx.x - 64;
-        for (int w = tid; w < (TK - first) * 16; w += 128) {
+        const int tid = threadIdx.x - 96;
+        for (int w = tid; w < (TK - first) * 16; w += 256) {
           const int row = first + w / 16, part = w % 16;   // 8 x 16 B per row and chunk
           *reinterpret_cast<uint4*>(vbase + (part >> 3) * CHUNK + row * 128 + (part & 7) * 16) =
               make_uint4(0, 0, 0, 0);
@@ -289,14 +322,17 @@ __global__ void __launch_bounds__(NTHREADS, 1)
       if (lane == 0) mbar_arrive(&ctl.p_full);
     }
     // ---------------------------------------------------------------- epilogue
-    if (ok) ok = __all_sync(0xffffffffu, wait_or_abort(&ctl.pv_done, (nk - 1) & 1, ctl, a.status));
+    if (ok) ok = pair_all(quarter, __all_sync(0xffffffffu, wait_or_abort(&ctl.pv_done, (nk - 1) & 1, ctl, a.status)));
     if (ok) {
+      ctl.ls[half][r] = l;
+      pair_sync(quarter);
+      l += ctl.ls[half ^ 1][r];
       tc_fence_after();
       const float inv_l = l > 0.f ? 1.f / l : 0.f;
       const bool store = r < nq;
       __nv_bfloat16* orow = static_cast<__nv_bfloat16*>(a.o) + (((size_t)b * a.T + q0 + r) * a.n_h + head) * DH;
 #pragma unroll 1
-      for (int c = 0; c < DH; c += 32) {
+      for (int c = half * (DH / 2); c < (half + 1) * (DH / 2); c += 32) {
         float v[32];
         tmem_ld32(tbase + lane_base + O_COL + c, v);
         tmem_ld_wait();
@@ -308,7 +344,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
                            pack_bf16(v[e + 4] * inv_l, v[e + 5] * inv_l), pack_bf16(v[e + 6] * inv_l, v[e + 7] * inv_l));
         }
       }
-      if (store) a.lse[((size_t)b * a.T + q0 + r) * a.n_h + head] = (m_ref + log2f(l)) * kLn2;
+      if (store && half == 0) a.lse[((size_t)b * a.T + q0 + r) * a.n_h + head] = (m_ref + log2f(l)) * kLn2;
     }
   }
 
