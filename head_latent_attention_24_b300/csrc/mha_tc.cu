@@ -6,9 +6,10 @@
 // with the RoPE key shared by the heads, §7 scale 1/sqrt(d_h + d_r)).
 //
 // One CTA per (128 queries, head, sequence). The query tile (128 x 192, K-major)
-// stays in shared memory; key tiles of 128 rows stream through a two-stage TMA
-// ring, each stage holding k_C (128 x 128), the shared k_R (128 x 64, read
-// straight from the cache rows) and v_C (128 x 128). Per key tile:
+// stays in shared memory; key tiles of 128 rows stream through two-stage TMA
+// rings, one for k_C (128 x 128) with the shared k_R (128 x 64, read straight
+// from the cache rows), freed after the tile's QK, and one for v_C (128 x 128),
+// freed after its PV. Per key tile:
 //   S = Q . K^T      M = 128 queries, N = 128 keys, K = 192   (TMEM, double buffer)
 //   P = 2^(S*scale*log2e - m)  in bf16, written by the softmax threads into TMEM
 //   O += P . V       M = 128 queries, N = 128 (d_h), K = 128 keys, A from TMEM
@@ -45,10 +46,14 @@ constexpr float RESCALE_THRESHOLD = 8.0f;
 
 constexpr int CHUNK = TK * 128;                   // 16 KB: 128 rows x 64 bf16 (128 B, swizzled)
 constexpr int Q_OFF = 0;                          // 3 chunks: q_C (2), q_R (1)
-constexpr int STAGE = 5 * CHUNK;                  // k_C (2 chunks), k_R (1), v_C (2)
+// Keys and values in rings of their own: a key stage (k_C, 2 chunks, and k_R,
+// 1 chunk) is free once its QK has run, a value stage (v_C, 2 chunks) once its
+// PV has; the next loads of each start that early.
+constexpr int KSTAGE = 3 * CHUNK, VSTAGE = 2 * CHUNK;
 constexpr int NSTAGE = 2;
-constexpr int RING_OFF = Q_OFF + 3 * CHUNK;
-constexpr int SMEM_DYN = RING_OFF + NSTAGE * STAGE + 1024;
+constexpr int KRING_OFF = Q_OFF + 3 * CHUNK;
+constexpr int VRING_OFF = KRING_OFF + NSTAGE * KSTAGE;
+constexpr int SMEM_DYN = VRING_OFF + NSTAGE * VSTAGE + 1024;
 // TMEM columns
 constexpr uint32_t S_COL = 0;                     // 2 x 128 fp32
 constexpr uint32_t O_COL = 256;                   // 128 fp32
@@ -56,7 +61,7 @@ constexpr uint32_t P_COL = 384;                   // 64: 128 bf16 packed two per
 constexpr uint32_t TMEM_COLS = 512;
 
 struct Ctl {
-  uint64_t q_full, full[NSTAGE], empty[NSTAGE];
+  uint64_t q_full, k_full[NSTAGE], k_empty[NSTAGE], v_full[NSTAGE], v_empty[NSTAGE];
   uint64_t s_full[2], s_free[2], p_full, pv_done, mma_done;
   uint32_t tmem_base;
   int abort;
@@ -114,7 +119,10 @@ __global__ void __launch_bounds__(NTHREADS, 1)
 
   if (threadIdx.x == 0) {
     mbar_init(&ctl.q_full, 1);
-    for (int i = 0; i < NSTAGE; ++i) { mbar_init(&ctl.full[i], 1); mbar_init(&ctl.empty[i], 1); }
+    for (int i = 0; i < NSTAGE; ++i) {
+      mbar_init(&ctl.k_full[i], 1); mbar_init(&ctl.k_empty[i], 1);
+      mbar_init(&ctl.v_full[i], 1); mbar_init(&ctl.v_empty[i], 1);
+    }
     for (int i = 0; i < 2; ++i) { mbar_init(&ctl.s_full[i], 1); mbar_init(&ctl.s_free[i], 8); }
     mbar_init(&ctl.p_full, 8);
     mbar_init(&ctl.pv_done, 1);
@@ -147,11 +155,11 @@ __global__ void __launch_bounds__(NTHREADS, 1)
   const uint32_t sbase = smem_u32(smem);
 
   if (warp == 0) {
-    // ------------------------------------------------------------ TMA producer
+    // ------------------------------------------------------------ TMA producers
+    // lane 0: the queries, then the key stages; lane 1: the value stages
     if (lane == 0) {
       prefetch_tensormap(&map_q);
       prefetch_tensormap(&map_k);
-      prefetch_tensormap(&map_v);
       prefetch_tensormap(&map_kr);
       const int qrow = b * a.T + q0;
       mbar_arrive_expect_tx(&ctl.q_full, 3 * CHUNK);
@@ -160,19 +168,30 @@ __global__ void __launch_bounds__(NTHREADS, 1)
       bool ok = true;
       for (; i < nk; ++i) {
         const int st = i % NSTAGE;
-        if (i >= NSTAGE) ok = wait_or_abort(&ctl.empty[st], ((i / NSTAGE) - 1) & 1, ctl, a.status);
+        if (i >= NSTAGE) ok = wait_or_abort(&ctl.k_empty[st], ((i / NSTAGE) - 1) & 1, ctl, a.status);
         if (!ok) break;
-        uint8_t* dst = smem + RING_OFF + st * STAGE;
+        uint8_t* dst = smem + KRING_OFF + st * KSTAGE;
         const int krow = b * a.max_len + i * TK;
-        mbar_arrive_expect_tx(&ctl.full[st], STAGE);
-        tma_load_3d(dst, &map_k, &ctl.full[st], 0, krow, head * 2);
-        tma_load_2d(dst + 2 * CHUNK, &map_kr, &ctl.full[st], 0, krow);
-        tma_load_3d(dst + 3 * CHUNK, &map_v, &ctl.full[st], 0, krow, head * 2);
+        mbar_arrive_expect_tx(&ctl.k_full[st], KSTAGE);
+        tma_load_3d(dst, &map_k, &ctl.k_full[st], 0, krow, head * 2);
+        tma_load_2d(dst + 2 * CHUNK, &map_kr, &ctl.k_full[st], 0, krow);
       }
       if (!ok) {   // no copy lands after the CTA moves on
-        drain_ring(ctl.full, NSTAGE, i);
+        drain_ring(ctl.k_full, NSTAGE, i);
         mbar_wait(&ctl.q_full, 0, WAIT_CYCLES / 8);
       }
+    } else if (lane == 1) {
+      prefetch_tensormap(&map_v);
+      int i = 0;
+      bool ok = true;
+      for (; i < nk; ++i) {
+        const int st = i % NSTAGE;
+        if (i >= NSTAGE) ok = wait_or_abort(&ctl.v_empty[st], ((i / NSTAGE) - 1) & 1, ctl, a.status);
+        if (!ok) break;
+        mbar_arrive_expect_tx(&ctl.v_full[st], VSTAGE);
+        tma_load_3d(smem + VRING_OFF + st * VSTAGE, &map_v, &ctl.v_full[st], 0, b * a.max_len + i * TK, head * 2);
+      }
+      if (!ok) drain_ring(ctl.v_full, NSTAGE, i);
     }
   } else if (warp == 1) {
     // ------------------------------------------------------------ QK issuer
@@ -182,15 +201,15 @@ __global__ void __launch_bounds__(NTHREADS, 1)
     if (lane == 0) {
       constexpr uint32_t IDESC_QK = idesc_bf16(TQ, TK, false, false);
       const uint64_t q_desc = sdesc_sw128(sbase + Q_OFF, 16, 1024);
-      const uint64_t k_desc = sdesc_sw128(sbase + RING_OFF, 16, 1024);
+      const uint64_t k_desc = sdesc_sw128(sbase + KRING_OFF, 16, 1024);
       bool ok = wait_or_abort(&ctl.q_full, 0, ctl, a.status);
       for (int j = 0; j < nk && ok; ++j) {
         const int st = j % NSTAGE, sb = j & 1;
-        ok = wait_or_abort(&ctl.full[st], (j / NSTAGE) & 1, ctl, a.status) &&
+        ok = wait_or_abort(&ctl.k_full[st], (j / NSTAGE) & 1, ctl, a.status) &&
              (j < 2 || wait_or_abort(&ctl.s_free[sb], ((j >> 1) - 1) & 1, ctl, a.status));
         if (!ok) break;
         tc_fence_after();
-        const uint64_t kd = k_desc + (uint64_t)((st * STAGE) >> 4);
+        const uint64_t kd = k_desc + (uint64_t)((st * KSTAGE) >> 4);
 #pragma unroll
         for (int c = 0; c < 3; ++c)
 #pragma unroll
@@ -198,6 +217,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
             mma_bf16(tbase + S_COL + sb * TK, q_desc + (uint64_t)((c * CHUNK + k * 32) >> 4),
                      kd + (uint64_t)((c * CHUNK + k * 32) >> 4), IDESC_QK, (c > 0 || k > 0) ? 1u : 0u);
         mma_commit(&ctl.s_full[sb]);
+        mma_commit(&ctl.k_empty[st]);   // the key stage: its QK is done
       }
       // nothing of this CTA's reaches the tensor cores after it moves on
       mma_commit(&ctl.mma_done);
@@ -205,24 +225,25 @@ __global__ void __launch_bounds__(NTHREADS, 1)
     }
   } else if (warp == 2) {
     // ------------------------------------------------------------ PV issuer
-    // O += P(j) . V(j) once the softmax has written P(j); the stage is free
-    // when this PV completes (its QK completed before P(j) existed).
+    // O += P(j) . V(j) once the softmax has written P(j) and V(j) has landed;
+    // the value stage is free when this PV completes.
     if (lane == 0) {
       constexpr uint32_t IDESC_PV = idesc_bf16(TQ, DH, false, true);
-      const uint64_t v_desc = sdesc_sw128(sbase + RING_OFF + 3 * CHUNK, CHUNK, 1024);
+      const uint64_t v_desc = sdesc_sw128(sbase + VRING_OFF, CHUNK, 1024);
       bool ok = true;
       for (int j = 0; j < nk && ok; ++j) {
-        ok = wait_or_abort(&ctl.p_full, j & 1, ctl, a.status);
+        const int st = j % NSTAGE;
+        ok = wait_or_abort(&ctl.p_full, j & 1, ctl, a.status) &&
+             wait_or_abort(&ctl.v_full[st], (j / NSTAGE) & 1, ctl, a.status);
         if (!ok) break;
         tc_fence_after();
-        const int st = j % NSTAGE;
-        const uint64_t vd = v_desc + (uint64_t)((st * STAGE) >> 4);
+        const uint64_t vd = v_desc + (uint64_t)((st * VSTAGE) >> 4);
 #pragma unroll
         for (int k = 0; k < TK / 16; ++k)
           mma_bf16_ta(tbase + O_COL, tbase + P_COL + k * 8, vd + (uint64_t)((k * 2048) >> 4), IDESC_PV,
                       (j > 0 || k > 0) ? 1u : 0u);
         mma_commit(&ctl.pv_done);
-        mma_commit(&ctl.empty[st]);
+        mma_commit(&ctl.v_empty[st]);
       }
       mma_commit(&ctl.mma_done);
       mbar_wait(&ctl.mma_done, 0, WAIT_CYCLES / 8);
@@ -305,10 +326,10 @@ __global__ void __launch_bounds__(NTHREADS, 1)
       // below publishes them)
       if (j == nk - 1 && qp_last - j * TK + 1 < TK) {
         const int st = j % NSTAGE;
-        ok = pair_all(quarter, __all_sync(0xffffffffu, wait_or_abort(&ctl.full[st], (j / NSTAGE) & 1, ctl, a.status)));
+        ok = pair_all(quarter, __all_sync(0xffffffffu, wait_or_abort(&ctl.v_full[st], (j / NSTAGE) & 1, ctl, a.status)));
         if (!ok) break;
         const int first = qp_last - j * TK + 1;   // rows first .. TK-1 of both v_C chunks
-        uint8_t* vbase = smem + RING_OFF + st * STAGE + 3 * CHUNK;
+        uint8_t* vbase = smem + VRING_OFF + st * VSTAGE;
         const int tid = threadIdx.x - 96;
         for (int w = tid; w < (TK - first) * 16; w += 256) {
           const int row = first + w / 16, part = w % 16;   // 8 x 16 B per row and chunk
