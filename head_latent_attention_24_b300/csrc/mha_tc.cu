@@ -5,12 +5,13 @@
 // visibility with a cache; page "MLA：潜在表示压缩与解耦 RoPE", §6 k = [k_C ; k_R]
 // with the RoPE key shared by the heads, §7 scale 1/sqrt(d_h + d_r)).
 //
-// One CTA per (128 queries, head, sequence). The query tile (128 x 192, K-major)
-// stays in shared memory; key tiles of 128 rows stream through two-stage TMA
-// rings, one for k_C (128 x 128) with the shared k_R (128 x 64, read straight
-// from the cache rows), freed after the tile's QK, and one for v_C (128 x 128),
-// freed after its PV. Per key tile:
-//   S = Q . K^T      M = 128 queries, N = 128 keys, K = 192   (TMEM, double buffer)
+// One CTA per (128 queries, head, sequence). The query tile (128 x 192) is
+// moved into TMEM once and is the A operand of every QK; key tiles of 128 rows
+// stream through two TMA rings, a two-stage one for k_C (128 x 128) with the
+// shared k_R (128 x 64, read straight from the cache rows), freed after the
+// tile's QK, and a three-stage one for v_C (128 x 128), freed after its PV.
+// Per key tile:
+//   S = Q . K^T      M = 128 queries, N = 128 keys, K = 192   (TMEM)
 //   P = 2^(S*scale*log2e - m)  in bf16, written by the softmax threads into TMEM
 //   O += P . V       M = 128 queries, N = 128 (d_h), K = 128 keys, A from TMEM
 // Each query row (a TMEM lane) belongs to two softmax threads, one per half of
@@ -45,24 +46,30 @@ constexpr float kLn2 = 0.693147180559945309f;
 constexpr float RESCALE_THRESHOLD = 8.0f;
 
 constexpr int CHUNK = TK * 128;                   // 16 KB: 128 rows x 64 bf16 (128 B, swizzled)
-constexpr int Q_OFF = 0;                          // 3 chunks: q_C (2), q_R (1)
 // Keys and values in rings of their own: a key stage (k_C, 2 chunks, and k_R,
 // 1 chunk) is free once its QK has run, a value stage (v_C, 2 chunks) once its
-// PV has; the next loads of each start that early.
+// PV has; the next loads of each start that early. The value ring is the
+// deeper one: a value load is issued only when the PV two (three) tiles back
+// has run, and the PV it feeds comes right after the softmax.
 constexpr int KSTAGE = 3 * CHUNK, VSTAGE = 2 * CHUNK;
-constexpr int NSTAGE = 2;
-constexpr int KRING_OFF = Q_OFF + 3 * CHUNK;
-constexpr int VRING_OFF = KRING_OFF + NSTAGE * KSTAGE;
-constexpr int SMEM_DYN = VRING_OFF + NSTAGE * VSTAGE + 1024;
+constexpr int NKS = 2, NVS = 3;
+constexpr int KRING_OFF = 0;
+constexpr int VRING_OFF = KRING_OFF + NKS * KSTAGE;
+constexpr int SMEM_DYN = VRING_OFF + NVS * VSTAGE + 1024;
+// The query tile lands in key stage 1 (3 chunks, the size of a key stage);
+// the softmax warps move it into TMEM, where it is the A operand of QK, and
+// hand the stage back for key tile 1.
+constexpr int Q_STAGE = 1;
 // TMEM columns
-constexpr uint32_t S_COL = 0;                     // 2 x 128 fp32
-constexpr uint32_t O_COL = 256;                   // 128 fp32
-constexpr uint32_t P_COL = 384;                   // 64: 128 bf16 packed two per column
+constexpr uint32_t S_COL = 0;                     // 128 fp32
+constexpr uint32_t O_COL = 128;                   // 128 fp32
+constexpr uint32_t P_COL = 256;                   // 64: 128 bf16 packed two per column
+constexpr uint32_t Q_COL = 320;                   // 96: 192 bf16 packed two per column
 constexpr uint32_t TMEM_COLS = 512;
 
 struct Ctl {
-  uint64_t q_full, k_full[NSTAGE], k_empty[NSTAGE], v_full[NSTAGE], v_empty[NSTAGE];
-  uint64_t s_full[2], s_free[2], p_full, pv_done, mma_done;
+  uint64_t q_full, q_ready, k_full[NKS], k_empty[NKS], v_full[NVS], v_empty[NVS];
+  uint64_t s_full, s_free, p_full, pv_done, mma_done;
   uint32_t tmem_base;
   int abort;
   long long wait_limit;
@@ -119,11 +126,11 @@ __global__ void __launch_bounds__(NTHREADS, 1)
 
   if (threadIdx.x == 0) {
     mbar_init(&ctl.q_full, 1);
-    for (int i = 0; i < NSTAGE; ++i) {
-      mbar_init(&ctl.k_full[i], 1); mbar_init(&ctl.k_empty[i], 1);
-      mbar_init(&ctl.v_full[i], 1); mbar_init(&ctl.v_empty[i], 1);
-    }
-    for (int i = 0; i < 2; ++i) { mbar_init(&ctl.s_full[i], 1); mbar_init(&ctl.s_free[i], 8); }
+    mbar_init(&ctl.q_ready, 8);
+    for (int i = 0; i < NKS; ++i) { mbar_init(&ctl.k_full[i], 1); mbar_init(&ctl.k_empty[i], 1); }
+    for (int i = 0; i < NVS; ++i) { mbar_init(&ctl.v_full[i], 1); mbar_init(&ctl.v_empty[i], 1); }
+    mbar_init(&ctl.s_full, 1);
+    mbar_init(&ctl.s_free, 8);
     mbar_init(&ctl.p_full, 8);
     mbar_init(&ctl.pv_done, 1);
     mbar_init(&ctl.mma_done, 2);
@@ -163,12 +170,13 @@ __global__ void __launch_bounds__(NTHREADS, 1)
       prefetch_tensormap(&map_kr);
       const int qrow = b * a.T + q0;
       mbar_arrive_expect_tx(&ctl.q_full, 3 * CHUNK);
-      tma_load_3d(smem + Q_OFF, &map_q, &ctl.q_full, 0, qrow, head * 3);
+      tma_load_3d(smem + KRING_OFF + Q_STAGE * KSTAGE, &map_q, &ctl.q_full, 0, qrow, head * 3);
       int i = 0;
       bool ok = true;
       for (; i < nk; ++i) {
-        const int st = i % NSTAGE;
-        if (i >= NSTAGE) ok = wait_or_abort(&ctl.k_empty[st], ((i / NSTAGE) - 1) & 1, ctl, a.status);
+        const int st = i % NKS;
+        if (i >= NKS) ok = wait_or_abort(&ctl.k_empty[st], ((i / NKS) - 1) & 1, ctl, a.status);
+        else if (st == Q_STAGE) ok = wait_or_abort(&ctl.q_ready, 0, ctl, a.status);   // the queries have left
         if (!ok) break;
         uint8_t* dst = smem + KRING_OFF + st * KSTAGE;
         const int krow = b * a.max_len + i * TK;
@@ -177,7 +185,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
         tma_load_2d(dst + 2 * CHUNK, &map_kr, &ctl.k_full[st], 0, krow);
       }
       if (!ok) {   // no copy lands after the CTA moves on
-        drain_ring(ctl.k_full, NSTAGE, i);
+        drain_ring(ctl.k_full, NKS, i);
         mbar_wait(&ctl.q_full, 0, WAIT_CYCLES / 8);
       }
     } else if (lane == 1) {
@@ -185,28 +193,27 @@ __global__ void __launch_bounds__(NTHREADS, 1)
       int i = 0;
       bool ok = true;
       for (; i < nk; ++i) {
-        const int st = i % NSTAGE;
-        if (i >= NSTAGE) ok = wait_or_abort(&ctl.v_empty[st], ((i / NSTAGE) - 1) & 1, ctl, a.status);
+        const int st = i % NVS;
+        if (i >= NVS) ok = wait_or_abort(&ctl.v_empty[st], ((i / NVS) - 1) & 1, ctl, a.status);
         if (!ok) break;
         mbar_arrive_expect_tx(&ctl.v_full[st], VSTAGE);
         tma_load_3d(smem + VRING_OFF + st * VSTAGE, &map_v, &ctl.v_full[st], 0, b * a.max_len + i * TK, head * 2);
       }
-      if (!ok) drain_ring(ctl.v_full, NSTAGE, i);
+      if (!ok) drain_ring(ctl.v_full, NVS, i);
     }
   } else if (warp == 1) {
     // ------------------------------------------------------------ QK issuer
-    // S(j) = Q . K(j)^T into buffer j % 2 once stage j has landed and the
-    // softmax has read the buffer's previous tile. QK and PV have an issuing
-    // thread each, so that a PV never waits behind the next tile's load.
+    // S(j) = Q . K(j)^T (Q from TMEM) once key stage j has landed and the
+    // softmax has read S(j-1). QK and PV have an issuing thread each, so that
+    // a PV never waits behind the next tile's load.
     if (lane == 0) {
       constexpr uint32_t IDESC_QK = idesc_bf16(TQ, TK, false, false);
-      const uint64_t q_desc = sdesc_sw128(sbase + Q_OFF, 16, 1024);
       const uint64_t k_desc = sdesc_sw128(sbase + KRING_OFF, 16, 1024);
-      bool ok = wait_or_abort(&ctl.q_full, 0, ctl, a.status);
+      bool ok = wait_or_abort(&ctl.q_ready, 0, ctl, a.status);
       for (int j = 0; j < nk && ok; ++j) {
-        const int st = j % NSTAGE, sb = j & 1;
-        ok = wait_or_abort(&ctl.k_full[st], (j / NSTAGE) & 1, ctl, a.status) &&
-             (j < 2 || wait_or_abort(&ctl.s_free[sb], ((j >> 1) - 1) & 1, ctl, a.status));
+        const int st = j % NKS;
+        ok = wait_or_abort(&ctl.k_full[st], (j / NKS) & 1, ctl, a.status) &&
+             (j < 1 || wait_or_abort(&ctl.s_free, (j - 1) & 1, ctl, a.status));
         if (!ok) break;
         tc_fence_after();
         const uint64_t kd = k_desc + (uint64_t)((st * KSTAGE) >> 4);
@@ -214,9 +221,9 @@ __global__ void __launch_bounds__(NTHREADS, 1)
         for (int c = 0; c < 3; ++c)
 #pragma unroll
           for (int k = 0; k < 4; ++k)
-            mma_bf16(tbase + S_COL + sb * TK, q_desc + (uint64_t)((c * CHUNK + k * 32) >> 4),
-                     kd + (uint64_t)((c * CHUNK + k * 32) >> 4), IDESC_QK, (c > 0 || k > 0) ? 1u : 0u);
-        mma_commit(&ctl.s_full[sb]);
+            mma_bf16_ta(tbase + S_COL, tbase + Q_COL + c * 32 + k * 8, kd + (uint64_t)((c * CHUNK + k * 32) >> 4),
+                        IDESC_QK, (c > 0 || k > 0) ? 1u : 0u);
+        mma_commit(&ctl.s_full);
         mma_commit(&ctl.k_empty[st]);   // the key stage: its QK is done
       }
       // nothing of this CTA's reaches the tensor cores after it moves on
@@ -232,9 +239,9 @@ __global__ void __launch_bounds__(NTHREADS, 1)
       const uint64_t v_desc = sdesc_sw128(sbase + VRING_OFF, CHUNK, 1024);
       bool ok = true;
       for (int j = 0; j < nk && ok; ++j) {
-        const int st = j % NSTAGE;
+        const int st = j % NVS;
         ok = wait_or_abort(&ctl.p_full, j & 1, ctl, a.status) &&
-             wait_or_abort(&ctl.v_full[st], (j / NSTAGE) & 1, ctl, a.status);
+             wait_or_abort(&ctl.v_full[st], (j / NVS) & 1, ctl, a.status);
         if (!ok) break;
         tc_fence_after();
         const uint64_t vd = v_desc + (uint64_t)((st * VSTAGE) >> 4);
@@ -261,19 +268,37 @@ __global__ void __launch_bounds__(NTHREADS, 1)
     const float sl2 = a.scale_log2;
     constexpr int HK = TK / 2;                         // keys per half
     float m_ref = -INFINITY, l = 0.f;
-    bool ok = true;
+    // The query tile from key stage Q_STAGE into TMEM (row r = lane r, 32
+    // columns per 64-column chunk): half 0 moves chunks 0 and 1, half 1 chunk 2.
+    bool ok = pair_all(quarter, __all_sync(0xffffffffu, wait_or_abort(&ctl.q_full, 0, ctl, a.status)));
+    if (ok) {
+      const uint8_t* qs = smem + KRING_OFF + Q_STAGE * KSTAGE + (r >> 3) * 1024 + (r & 7) * 128;
+      for (int c = half * 2; c < (half == 0 ? 2 : 3); ++c) {
+        uint32_t w[32];
+#pragma unroll
+        for (int v = 0; v < 8; ++v) {
+          const uint4 x = *reinterpret_cast<const uint4*>(qs + c * CHUNK + ((v ^ (r & 7)) << 4));
+          w[4 * v] = x.x; w[4 * v + 1] = x.y; w[4 * v + 2] = x.z; w[4 * v + 3] = x.w;
+        }
+        tmem_st32(tbase + lane_base + Q_COL + c * 32, w);
+      }
+      asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&ctl.q_ready);   // also: the stage may take key tile 1
+    }
     for (int j = 0; j < nk && ok; ++j) {
-      const int sb = j & 1, k0 = j * TK + half * HK;
-      ok = pair_all(quarter, __all_sync(0xffffffffu, wait_or_abort(&ctl.s_full[sb], (j >> 1) & 1, ctl, a.status)));
+      const int k0 = j * TK + half * HK;
+      ok = pair_all(quarter, __all_sync(0xffffffffu, wait_or_abort(&ctl.s_full, j & 1, ctl, a.status)));
       if (!ok) break;
       tc_fence_after();
       float s[HK];
-      tmem_ld32(tbase + lane_base + S_COL + sb * TK + half * HK, s);
-      tmem_ld32(tbase + lane_base + S_COL + sb * TK + half * HK + 32, s + 32);
+      tmem_ld32(tbase + lane_base + S_COL + half * HK, s);
+      tmem_ld32(tbase + lane_base + S_COL + half * HK + 32, s + 32);
       tmem_ld_wait();
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive(&ctl.s_free[sb]);
+      if (lane == 0) mbar_arrive(&ctl.s_free);
       // causal mask: key k0 + c is visible to this row when k0 + c <= qp
       const int nvis = max(0, min(HK, qp - k0 + 1));
       float mx = -INFINITY;
@@ -325,8 +350,8 @@ __global__ void __launch_bounds__(NTHREADS, 1)
       // before PV reads it (each warp a share of the rows; its p_full arrival
       // below publishes them)
       if (j == nk - 1 && qp_last - j * TK + 1 < TK) {
-        const int st = j % NSTAGE;
-        ok = pair_all(quarter, __all_sync(0xffffffffu, wait_or_abort(&ctl.v_full[st], (j / NSTAGE) & 1, ctl, a.status)));
+        const int st = j % NVS;
+        ok = pair_all(quarter, __all_sync(0xffffffffu, wait_or_abort(&ctl.v_full[st], (j / NVS) & 1, ctl, a.status)));
         if (!ok) break;
         const int first = qp_last - j * TK + 1;   // rows first .. TK-1 of both v_C chunks
         uint8_t* vbase = smem + VRING_OFF + st * VSTAGE;
