@@ -301,11 +301,21 @@ __global__ void __launch_bounds__(NTHREADS, 1)
       if (lane == 0) mbar_arrive(&ctl.s_free);
       // causal mask: key k0 + c is visible to this row when k0 + c <= qp
       const int nvis = max(0, min(HK, qp - k0 + 1));
+      // Tiles below the diagonal (every key visible to every row of the warp)
+      // take the short path: the maximum of the raw scores, scaled once, and
+      // the scale folded into the exponent's FMA.
+      const bool full = __all_sync(0xffffffffu, nvis == HK);
       float mx = -INFINITY;
+      if (full) {
 #pragma unroll
-      for (int c = 0; c < HK; ++c) {
-        s[c] = c < nvis ? s[c] * sl2 : -INFINITY;
-        mx = fmaxf(mx, s[c]);
+        for (int c = 0; c < HK; ++c) mx = fmaxf(mx, s[c]);
+        mx *= sl2;
+      } else {
+#pragma unroll
+        for (int c = 0; c < HK; ++c) {
+          s[c] = c < nvis ? s[c] * sl2 : -INFINITY;
+          mx = fmaxf(mx, s[c]);
+        }
       }
       ctl.mx[j & 1][half][r] = mx;
       pair_sync(quarter);
@@ -316,15 +326,27 @@ __global__ void __launch_bounds__(NTHREADS, 1)
         m_ref = mx;
       }
       uint32_t pk[HK / 2];
-      float lsum = 0.f;
+      float lsum0 = 0.f, lsum1 = 0.f;   // the softmax sum from the unrounded weights
+      if (full) {
+        const float neg = -m_ref;
 #pragma unroll
-      for (int c = 0; c < HK; c += 2) {
-        const float p0 = c < nvis ? ex2_approx(s[c] - m_ref) : 0.f;
-        const float p1 = c + 1 < nvis ? ex2_approx(s[c + 1] - m_ref) : 0.f;
-        lsum += p0 + p1;   // the softmax sum from the unrounded weights
-        pk[c / 2] = pack_bf16(p0, p1);
+        for (int c = 0; c < HK; c += 2) {
+          const float p0 = ex2_approx(fmaf(s[c], sl2, neg)), p1 = ex2_approx(fmaf(s[c + 1], sl2, neg));
+          lsum0 += p0;
+          lsum1 += p1;
+          pk[c / 2] = pack_bf16(p0, p1);
+        }
+      } else {
+#pragma unroll
+        for (int c = 0; c < HK; c += 2) {
+          const float p0 = c < nvis ? ex2_approx(s[c] - m_ref) : 0.f;
+          const float p1 = c + 1 < nvis ? ex2_approx(s[c + 1] - m_ref) : 0.f;
+          lsum0 += p0;
+          lsum1 += p1;
+          pk[c / 2] = pack_bf16(p0, p1);
+        }
       }
-      l = l * alpha + lsum;   // this half's share of the row sum
+      l = l * alpha + (lsum0 + lsum1);   // this half's share of the row sum
       // P(j) replaces P(j-1) in TMEM and O is rescaled: both only after PV(j-1)
       if (j > 0) {
         ok = pair_all(quarter, __all_sync(0xffffffffu, wait_or_abort(&ctl.pv_done, (j - 1) & 1, ctl, a.status)));
