@@ -1,5 +1,7 @@
 // Host-side creation of TMA tensor maps (cuTensorMapEncodeTiled through the
-// runtime's driver entry point, so the library needs no -lcuda).
+// runtime's driver entry point, so the library needs no -lcuda). Encoded maps
+// are cached by their full parameter set (thread-safe), so calls that repeat
+// the same tensors skip the driver's encoding.
 #pragma once
 #include <cuda.h>
 #include <stdint.h>
