@@ -30,6 +30,9 @@
 // one thread, warps 2-5 drain TMEM, reduce and run the epilogue. Every
 // mbarrier wait is bounded; on expiry the CTA records MLA_DEV_TIMEOUT and
 // skips the rest of its work (still joining the cluster barriers).
+#include <mutex>
+#include <vector>
+
 #include "internal.cuh"
 #include "tc_ptx.cuh"
 #include "tmap.cuh"
@@ -43,6 +46,10 @@ using namespace tc;
 constexpr int BM = 128;            // weight rows per tile (MMA M)
 constexpr int BK = 64;             // reduction columns per chunk (128 B of bf16)
 constexpr int CHUNK_A = BM * BK * 2;   // 16 KB: one chunk of a weight tile
+// Row stride (floats) of the fp32 partial tiles in shared memory: the store
+// loop reads 8 consecutive rows m of two activation rows n per warp, and the
+// 4-float pad puts those two rows on different banks.
+constexpr int CS_LD = BM + 4;
 constexpr int NTHREADS = 192;
 constexpr int MAX_SPLITS = 8;
 constexpr int MAX_MT = 4;
@@ -63,6 +70,10 @@ struct Params {
   const float* rope_cos; const float* rope_sin; int d_r; int max_pos;
   const int32_t* pos;
   const int32_t* tok_seq; const int32_t* tok_pos; int cache_batch; int max_len; int d_c; int row_width;
+  // > 0: the epilogue first copies, for the tile's activation rows, their
+  // positions (and cache sequences) and the RoPE cos/sin rows at those
+  // positions into shared memory at this offset (layout in stage_rope).
+  int rope_off;
   int32_t* status;
 };
 
@@ -82,6 +93,46 @@ __device__ __forceinline__ bool wait_bar(uint64_t* bar, uint32_t parity, Ctl& ct
 
 __device__ __forceinline__ float rope_apply(float v, float partner, bool first_half, float c, float s) {
   return first_half ? (v * c - partner * s) : (v * c + partner * s);
+}
+
+// RoPE on 8 consecutive rows; the partner rows, cos and sin come as pairs of
+// 16-byte loads (each pointer starts an 8-row group, d_r / 2 is a multiple
+// of 8, and every row of the tables and partial tiles is 16-byte aligned).
+__device__ __forceinline__ void rope8(float (&v)[8], const float* pr, bool first, const float* tc, const float* ts) {
+  float q[8], c[8], sn[8];
+  *reinterpret_cast<float4*>(q) = *reinterpret_cast<const float4*>(pr);
+  *reinterpret_cast<float4*>(q + 4) = *reinterpret_cast<const float4*>(pr + 4);
+  *reinterpret_cast<float4*>(c) = *reinterpret_cast<const float4*>(tc);
+  *reinterpret_cast<float4*>(c + 4) = *reinterpret_cast<const float4*>(tc + 4);
+  *reinterpret_cast<float4*>(sn) = *reinterpret_cast<const float4*>(ts);
+  *reinterpret_cast<float4*>(sn + 4) = *reinterpret_cast<const float4*>(ts + 4);
+#pragma unroll
+  for (int e = 0; e < 8; ++e) v[e] = rope_apply(v[e], q[e], first, c[e], sn[e]);
+}
+
+// Shared-memory copy of what the RoPE and cache-row epilogues read per
+// activation row n of the tile: rc[n][j], rs[n][j] (cos, sin at the row's
+// position, j < d_r/2), then pos_s[n] and seq_s[n] as stored (range checks
+// stay with the epilogue). The 128 epilogue threads fill it with independent
+// loads while the MMAs run, so the store loop reads no global memory.
+__device__ __forceinline__ void stage_rope(const Params& p, uint8_t* smem, int n0, int n_valid, bool append, int et) {
+  const int half = p.d_r / 2;
+  float* rc = reinterpret_cast<float*>(smem + p.rope_off);
+  float* rs = rc + p.n_tile * half;
+  int32_t* pos_s = reinterpret_cast<int32_t*>(rs + p.n_tile * half);
+  int32_t* seq_s = pos_s + p.n_tile;
+  const int32_t* pos = append ? p.tok_pos : p.pos;
+  for (int n = et; n < n_valid; n += 128) {
+    pos_s[n] = pos[n0 + n];
+    seq_s[n] = append ? (p.tok_seq ? p.tok_seq[n0 + n] : n0 + n) : 0;
+  }
+  for (int i = et; i < n_valid * half; i += 128) {
+    const int n = i / half, j = i - n * half;
+    int ps = pos[n0 + n];
+    ps = ps < 0 ? 0 : (ps >= p.max_pos ? p.max_pos - 1 : ps);
+    rc[i] = p.rope_cos[(long long)ps * half + j];
+    rs[i] = p.rope_sin[(long long)ps * half + j];
+  }
 }
 
 // CPB: column chunks per stage. TRANS: the weights are stored [K rows][M
@@ -209,8 +260,14 @@ __global__ void __launch_bounds__(NTHREADS, 2)
     // ------------------------------------------------------------ epilogue warps 2..5
     const int quarter = warp & 3;
     const int m = quarter * 32 + lane;           // this thread's TMEM lane = tile row
-    float* cs = reinterpret_cast<float*>(smem);  // [MT][n_tile][BM] partials, reuses the stages
+    float* cs = reinterpret_cast<float*>(smem);  // [MT][n_tile][CS_LD] partials, reuses the stages
     pdl_wait();   // before the epilogue reads indices or writes the output
+    if (p.rope_off) {
+      bool append = false;
+      for (int sg = 0; sg < 3; ++sg) append = append || p.epi[sg] == EPI_APPEND;
+      stage_rope(p, smem, n0, min(p.n_tile, p.N - n0), append, threadIdx.x - 64);
+      asm volatile("bar.sync 1, 128;" ::: "memory");   // the four epilogue warps
+    }
     // warp-uniform: the TMEM loads below are warp-collective
     const bool ok = __all_sync(0xffffffffu, nk > 0 && wait_bar(&ctl.acc_full, 0, ctl, p.status));
     if (ok) tc_fence_after();
@@ -230,7 +287,7 @@ __global__ void __launch_bounds__(NTHREADS, 2)
         }
 #pragma unroll
         for (int i = 0; i < 64; ++i)
-          if (i < nc) cs[(t * p.n_tile + c + i) * BM + m] = v[i];
+          if (i < nc) cs[(t * p.n_tile + c + i) * CS_LD + m] = v[i];
       }
     }
   }
@@ -256,7 +313,7 @@ __global__ void __launch_bounds__(NTHREADS, 2)
 #pragma unroll
         for (int r = 0; r < MAX_SPLITS; ++r)
           if (r < S && n < n_valid) {
-            const uint32_t a = mapa_shared(cs_addr + (uint32_t)((n * BM + m4) * 4), (uint32_t)r);
+            const uint32_t a = mapa_shared(cs_addr + (uint32_t)((n * CS_LD + m4) * 4), (uint32_t)r);
             asm volatile("ld.shared::cluster.v4.f32 {%0,%1,%2,%3}, [%4];"
                          : "=f"(v[q][r].x), "=f"(v[q][r].y), "=f"(v[q][r].z), "=f"(v[q][r].w)
                          : "r"(a));
@@ -272,95 +329,118 @@ __global__ void __launch_bounds__(NTHREADS, 2)
           if (r < S) { acc.x += v[q][r].x; acc.y += v[q][r].y; acc.z += v[q][r].z; acc.w += v[q][r].w; }
         // Peers may still be reading this CTA's partials: the sum goes to a
         // separate region holding this CTA's own rows.
-        *reinterpret_cast<float4*>(cs + p.n_tile * BM + (n / S) * BM + m4) = acc;
+        *reinterpret_cast<float4*>(cs + (p.n_tile + n / S) * CS_LD + m4) = acc;
       }
     }
   }
   cluster_sync();  // all remote reads done: no CTA's shared memory is needed by a peer any more
-  if (warp >= 2) {
-    const int et = threadIdx.x - 64;
+  {
+    // Every warp stores. A thread writes 8 consecutive output columns (one
+    // 16-byte vector) of one activation row per pass: 16 threads span a
+    // 128-row tile, the CTA's threads NTHREADS / 16 rows n at a time. Rows
+    // owned by this CTA: n = split + S j. What depends only on the thread's 8
+    // columns is worked out once per tile, and two rows are loaded before
+    // either is stored so that their shared-memory reads overlap.
     const float* cs = reinterpret_cast<const float*>(smem);
     __nv_bfloat16* out = static_cast<__nv_bfloat16*>(p.out[seg]);
     const int epi = p.epi[seg];
-    const long long ldo = p.ldo[seg], bo = p.bo[seg];
-    // Each thread stores 8 consecutive output columns (one 16-byte vector)
-    // of one activation row per pass: 16 threads span a 128-row tile, the 128
-    // epilogue threads 8 rows n. Rows owned by this CTA: n = split + S j.
-    const int cg = et & 15, jr = et >> 4;
+    const long long ldo = p.ldo[seg];
+    constexpr int JSTEP = NTHREADS / 16;
+    const int cg = threadIdx.x & 15, jr = threadIdx.x >> 4;
     const int n_own = (n_valid - split + S - 1) / S;
+    const int half = p.d_r / 2;
+    const float* rc = reinterpret_cast<const float*>(smem + p.rope_off);   // staged cos rows, then sin rows
+    const int32_t* pos_s = reinterpret_cast<const int32_t*>(rc + p.n_tile * p.d_r);   // then positions, sequences
     for (int t = 0; t < MT; ++t) {
       const int mb = m0 + t * BM + cg * 8;  // first of this thread's 8 rows within the segment
       if (mb >= p.rows[seg]) continue;
       const int mcount = min(8, p.rows[seg] - mb);
-      for (int j = jr; j < n_own; j += 8) {
+      // the 8 columns' place in an output row, and whether and how they rotate
+      long long col = 0;
+      int j0 = 0, sg = 0;
+      bool rope = false;
+      if (epi == EPI_STORE) {
+        col = z * p.bo[seg] + p.col0[seg] + mb;
+      } else if (epi == EPI_SEGS) {
+        // 8 rows inside one segment (seg_len % 8 == 0)
+        const int sl = p.seg_len[seg];
+        col = (long long)(mb / sl) * p.seg_stride[seg] + p.seg_off[seg] + mb % sl;
+      } else if (epi == EPI_ROPE_SEGS) {
+        // 8 rows of one rotated segment, all in one half of it (d_r % 16 == 0)
+        sg = mb / p.d_r;
+        j0 = mb % p.d_r;
+        col = (long long)sg * p.seg_stride[seg] + p.seg_off[seg] + j0;
+        rope = true;
+      } else {  // EPI_APPEND: cache columns, the rotated ones past d_c
+        col = p.col0[seg] + mb;
+        if (col >= p.d_c) { j0 = (int)col - p.d_c; rope = true; }
+      }
+      const bool first = j0 < half;
+      const int jj = first ? j0 : j0 - half;
+      const int pcol = cg * 8 + (first ? half : -half);
+
+      struct Row { float v[8]; __nv_bfloat16* dst; bool ok; };
+      auto load = [&](int j, Row& r) {
         const int n = split + S * j;
-        const float* row = S > 1 ? cs + (p.n_tile + j) * BM : cs + (t * p.n_tile + n) * BM;
+        const float* row = S > 1 ? cs + (p.n_tile + j) * CS_LD : cs + (t * p.n_tile + n) * CS_LD;
         const long long gn = (long long)n0 + n;
-        float v[8];
-        {
-          const float4 a0 = *reinterpret_cast<const float4*>(row + cg * 8);
-          const float4 a1 = *reinterpret_cast<const float4*>(row + cg * 8 + 4);
-          v[0] = a0.x; v[1] = a0.y; v[2] = a0.z; v[3] = a0.w; v[4] = a1.x; v[5] = a1.y; v[6] = a1.z; v[7] = a1.w;
-        }
-        __nv_bfloat16* dst;
-        if (epi == EPI_STORE) {
-          dst = out + z * bo + gn * ldo + p.col0[seg] + mb;
-        } else if (epi == EPI_SEGS) {
-          // 8 rows inside one segment (seg_len % 8 == 0)
-          const int sl = p.seg_len[seg];
-          dst = out + gn * ldo + (mb / sl) * p.seg_stride[seg] + p.seg_off[seg] + mb % sl;
-        } else if (epi == EPI_ROPE_SEGS) {
-          // 8 rows of one rotated segment, all in one half of it (d_r % 16 == 0)
-          const int half = p.d_r / 2;
-          const int sg = mb / p.d_r, j0 = mb % p.d_r;
-          int ps = p.pos[gn];
-          if (ps < 0 || ps >= p.max_pos) {
-            if (j0 == 0 && sg == 0) atomicOr(p.status, MLA_DEV_QPOS_RANGE);
-            ps = ps < 0 ? 0 : p.max_pos - 1;
-          }
-          const bool first = j0 < half;
-          const int jj = first ? j0 : j0 - half;
-          const float* pr = row + cg * 8 + (first ? half : -half);
-#pragma unroll
-          for (int e = 0; e < 8; ++e) {
-            const float c = p.rope_cos[(long long)ps * half + jj + e], sn = p.rope_sin[(long long)ps * half + jj + e];
-            v[e] = rope_apply(v[e], pr[e], first, c, sn);
-          }
-          dst = out + gn * ldo + sg * p.seg_stride[seg] + p.seg_off[seg] + j0;
-        } else {  // EPI_APPEND
-          const int sq = p.tok_seq ? p.tok_seq[gn] : (int)gn, ps = p.tok_pos[gn];
+        *reinterpret_cast<float4*>(r.v) = *reinterpret_cast<const float4*>(row + cg * 8);
+        *reinterpret_cast<float4*>(r.v + 4) = *reinterpret_cast<const float4*>(row + cg * 8 + 4);
+        r.ok = true;
+        int ps = 0;
+        if (epi == EPI_APPEND) {
+          const int sq = p.rope_off ? pos_s[p.n_tile + n] : (p.tok_seq ? p.tok_seq[gn] : (int)gn);
+          ps = p.rope_off ? pos_s[n] : p.tok_pos[gn];
           const bool seq_ok = sq >= 0 && sq < p.cache_batch;
           const bool pos_ok = ps >= 0 && ps < p.max_len && ps < p.max_pos;
-          const int gm = p.col0[seg] + mb;
           if (!seq_ok || !pos_ok) {
-            if (gm == 0) atomicOr(p.status, (seq_ok ? 0 : MLA_DEV_SEQ_RANGE) | (pos_ok ? 0 : MLA_DEV_POS_RANGE));
-            continue;
+            if (col == 0) atomicOr(p.status, (seq_ok ? 0 : MLA_DEV_SEQ_RANGE) | (pos_ok ? 0 : MLA_DEV_POS_RANGE));
+            r.ok = false;
+            return;
           }
-          if (gm >= p.d_c) {
-            const int half = p.d_r / 2;
-            const int j0 = gm - p.d_c;
-            const bool first = j0 < half;
-            const int jj = first ? j0 : j0 - half;
-            const float* pr = row + cg * 8 + (first ? half : -half);
-#pragma unroll
-            for (int e = 0; e < 8; ++e) {
-              const float c = p.rope_cos[(long long)ps * half + jj + e], sn = p.rope_sin[(long long)ps * half + jj + e];
-              v[e] = rope_apply(v[e], pr[e], first, c, sn);
+          r.dst = out + ((long long)sq * p.max_len + ps) * p.row_width + col;
+        } else {
+          r.dst = out + gn * ldo + col;
+          if (rope) {
+            ps = p.rope_off ? pos_s[n] : p.pos[gn];
+            if (ps < 0 || ps >= p.max_pos) {
+              if (j0 == 0 && sg == 0) atomicOr(p.status, MLA_DEV_QPOS_RANGE);
+              ps = ps < 0 ? 0 : p.max_pos - 1;
             }
           }
-          dst = out + ((long long)sq * p.max_len + ps) * p.row_width + gm;
         }
+        if (rope) {
+          const float* tc = p.rope_off ? rc + n * half + jj : p.rope_cos + (long long)ps * half + jj;
+          const float* ts = p.rope_off ? rc + (p.n_tile + n) * half + jj : p.rope_sin + (long long)ps * half + jj;
+          rope8(r.v, row + pcol, first, tc, ts);
+        }
+      };
+      auto store = [&](const Row& r) {
+        if (!r.ok) return;
         if (mcount == 8) {
           uint32_t pk[4];
 #pragma unroll
           for (int e = 0; e < 4; ++e) {
-            __nv_bfloat162 b2 = __floats2bfloat162_rn(v[2 * e], v[2 * e + 1]);
+            __nv_bfloat162 b2 = __floats2bfloat162_rn(r.v[2 * e], r.v[2 * e + 1]);
             pk[e] = *reinterpret_cast<uint32_t*>(&b2);
           }
-          *reinterpret_cast<uint4*>(dst) = make_uint4(pk[0], pk[1], pk[2], pk[3]);
+          *reinterpret_cast<uint4*>(r.dst) = make_uint4(pk[0], pk[1], pk[2], pk[3]);
         } else {
-          for (int e = 0; e < mcount; ++e) dst[e] = __float2bfloat16_rn(v[e]);
+          for (int e = 0; e < mcount; ++e) r.dst[e] = __float2bfloat16_rn(r.v[e]);
         }
+      };
+      int j = jr;
+      for (; j + JSTEP < n_own; j += 2 * JSTEP) {
+        Row a, b;
+        load(j, a);
+        load(j + JSTEP, b);
+        store(a);
+        store(b);
+      }
+      if (j < n_own) {
+        Row a;
+        load(j, a);
+        store(a);
       }
     }
   }
@@ -377,20 +457,105 @@ uint32_t pow2_at_least(uint32_t x) {
   return r;
 }
 
+// The largest dynamic shared memory requested so far of one instantiation.
+template <int CPB, bool TRANS>
+cudaError_t ensure_smem(size_t smem_dyn) {
+  static size_t smem_set = 0;
+  if (smem_dyn <= smem_set) return cudaSuccess;
+  cudaError_t e = cudaFuncSetAttribute(gemm_tc_kernel<CPB, TRANS>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       (int)smem_dyn);
+  if (e == cudaSuccess) smem_set = smem_dyn;
+  return e;
+}
+
 template <int CPB, bool TRANS>
 cudaError_t launch_typed(const CUtensorMap* mw, const CUtensorMap& mx, const Params& p, dim3 grid, size_t smem_dyn,
                          cudaStream_t s) {  // mw: three weight maps
-  static size_t smem_set = 0;  // per instantiation: the largest size requested so far
-  if (smem_dyn > smem_set) {
-    cudaError_t e = cudaFuncSetAttribute(gemm_tc_kernel<CPB, TRANS>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         (int)smem_dyn);
-    if (e != cudaSuccess) return e;
-    smem_set = smem_dyn;
-  }
+  cudaError_t e = ensure_smem<CPB, TRANS>(smem_dyn);
+  if (e != cudaSuccess) return e;
   LaunchCfg lc(grid, dim3(NTHREADS), smem_dyn, s, (unsigned)p.splits);
-  cudaError_t e = cudaLaunchKernelEx(&lc.cfg, gemm_tc_kernel<CPB, TRANS>, mw[0], mw[1], mw[2], mx, p);
+  e = cudaLaunchKernelEx(&lc.cfg, gemm_tc_kernel<CPB, TRANS>, mw[0], mw[1], mw[2], mx, p);
   if (e != cudaSuccess) return e;
   return cudaGetLastError();
+}
+
+template <int CPB, bool TRANS>
+int max_clusters_typed(size_t smem_dyn, int S) {
+  if (ensure_smem<CPB, TRANS>(smem_dyn) != cudaSuccess) return 0;
+  cudaLaunchConfig_t cfg{};
+  cudaLaunchAttribute at{};
+  at.id = cudaLaunchAttributeClusterDimension;
+  at.val.clusterDim.x = (unsigned)S;
+  at.val.clusterDim.y = 1;
+  at.val.clusterDim.z = 1;
+  cfg.gridDim = dim3((unsigned)S);
+  cfg.blockDim = dim3(NTHREADS);
+  cfg.dynamicSmemBytes = smem_dyn;
+  cfg.attrs = &at;
+  cfg.numAttrs = 1;
+  int n = 0;
+  if (cudaOccupancyMaxActiveClusters(&n, gemm_tc_kernel<CPB, TRANS>, &cfg) != cudaSuccess) {
+    (void)cudaGetLastError();
+    return 0;
+  }
+  return n;
+}
+
+// How many clusters of S CTAs the device holds at once (the GPCs bound it:
+// a cluster never spans two). Cached per configuration.
+int max_clusters(int cpb, bool trans, size_t smem_dyn, int S) {
+  struct Entry { int cpb, S; bool trans; size_t smem; int n; };
+  static std::mutex mu;
+  static std::vector<Entry> cache;
+  {
+    std::lock_guard<std::mutex> lock(mu);
+    for (const Entry& e : cache)
+      if (e.cpb == cpb && e.S == S && e.trans == trans && e.smem == smem_dyn) return e.n;
+  }
+  int n;
+  if (trans) n = cpb == 4 ? max_clusters_typed<4, true>(smem_dyn, S) : cpb == 2 ? max_clusters_typed<2, true>(smem_dyn, S)
+                                                                                : max_clusters_typed<1, true>(smem_dyn, S);
+  else n = cpb == 4 ? max_clusters_typed<4, false>(smem_dyn, S) : cpb == 2 ? max_clusters_typed<2, false>(smem_dyn, S)
+                                                                         : max_clusters_typed<1, false>(smem_dyn, S);
+  std::lock_guard<std::mutex> lock(mu);
+  if (cache.size() < 256) cache.push_back(Entry{cpb, S, trans, smem_dyn, n});
+  return n;
+}
+
+// One way to cut a launch into CTAs: CTAs per SM, 128-row tiles per CTA,
+// K splits per tile, and the shared-memory layout that follows.
+struct Choice {
+  int per_sm, mt, S;
+  int cpb, stage_bytes, kstages, nstage;
+  int rope_off;   // where the epilogue's staged RoPE rows start (after the stages)
+  size_t smem_dyn;
+};
+
+// Chunks per stage: as many as keep two stages within the budget (one stage
+// if it is the only one), at most what the reduction has; the fp32 partial
+// tiles [MT][n_tile][128] (plus the reduced own rows when split) reuse the
+// stage buffers and must fit the budget too.
+bool size_choice(Choice& c, int n_tile, int kchunks, int extra) {
+  const int budget = (c.per_sm == 2 ? SMEM_TWO : SMEM_ONE) - extra;
+  auto stage_of = [&](int cpb) { return c.mt * cpb * CHUNK_A + cpb * n_tile * 128; };
+  int cpb = 4;
+  while (cpb > 1 && (cpb > kchunks || 2 * stage_of(cpb) > budget) &&
+         !(cpb <= kchunks && (kchunks + cpb - 1) / cpb == 1 && stage_of(cpb) <= budget))
+    cpb >>= 1;
+  c.cpb = cpb;
+  c.stage_bytes = stage_of(cpb);
+  if (c.stage_bytes > budget) return false;
+  c.kstages = (kchunks + cpb - 1) / cpb;
+  if (c.S > c.kstages) return false;
+  c.nstage = budget / c.stage_bytes;
+  if (c.nstage > 8) c.nstage = 8;
+  if (c.nstage > c.kstages) c.nstage = c.kstages;
+  const size_t cs = (size_t)c.mt * n_tile * CS_LD * 4 + (c.S > 1 ? (size_t)((n_tile + c.S - 1) / c.S) * CS_LD * 4 : 0);
+  if (cs > (size_t)budget) return false;
+  const size_t stages = (size_t)c.nstage * c.stage_bytes;
+  c.rope_off = (int)(((cs > stages ? cs : stages) + 15) / 16 * 16);
+  c.smem_dyn = (size_t)c.rope_off + extra + 1024;
+  return true;
 }
 
 }  // namespace
@@ -452,55 +617,87 @@ cudaError_t launch_gemm_tc(const TcGemm& g, int num_sms, cudaStream_t s) {
   const long long n_tiles = (g.N + p.n_tile - 1) / p.n_tile;
   if (n_tiles > 65535 || g.Z > 65535) return cudaErrorInvalidValue;
   if (num_sms < 1) num_sms = 1;
-  // When the tiles outnumber the SMs, two CTAs share an SM (half the stage
-  // budget each) so that every tile is resident at once; otherwise one CTA
-  // per SM keeps the most bytes in flight per tile.
-  // The epilogue's fp32 partial tile (n_tile x 128) reuses the stage buffers:
-  // two CTAs share an SM only when it fits their half of shared memory.
   const long long tiles_all = (long long)p.mtiles_total * n_tiles * g.Z;
-  const int per_sm = (tiles_all > num_sms && (size_t)p.n_tile * BM * 4 <= (size_t)SMEM_TWO) ? 2 : 1;
-  const int budget = per_sm == 2 ? SMEM_TWO : SMEM_ONE;
-  num_sms *= per_sm;
-
-  // Tiles per CTA: more than one only when the tiles outnumber the SMs and
-  // split-K is therefore off (the tiles' accumulators fit TMEM, and no CTA's
-  // tiles straddle two segments).
-  int mt = 1;
-  const long long tiles1 = (long long)p.mtiles_total * n_tiles * g.Z;
   bool mt_ok = true;
   for (int sg = 0; sg < g.nseg; ++sg) mt_ok = mt_ok && g.epi[sg] != EPI_APPEND;
-  if (tiles1 > num_sms && mt_ok) {
-    for (int c = 2; c <= MAX_MT; c *= 2)
-      if (p.mtiles_total % c == 0 && p.mstart[1] % c == 0 && p.mstart[2] % c == 0 && c * p.n_tile <= 512 &&
-          (size_t)c * p.n_tile * BM * 4 <= (size_t)budget) {
-        mt = c;
-        if (tiles1 / c <= num_sms) break;
-      }
+  auto mt_fits = [&](int c) {
+    return mt_ok && p.mtiles_total % c == 0 && p.mstart[1] % c == 0 && p.mstart[2] % c == 0 && c * p.n_tile <= 512;
+  };
+  Choice best{};
+  bool have = false;
+  // With one activation tile (decode) a RoPE or cache-row epilogue stages
+  // its per-row positions and cos/sin rows in shared memory (stage_rope).
+  bool roped = false;
+  for (int sg = 0; sg < g.nseg; ++sg) roped = roped || g.epi[sg] == EPI_ROPE_SEGS || g.epi[sg] == EPI_APPEND;
+  const int rope_extra = roped ? p.n_tile * (g.d_r * 4 + 8) : 0;
+  if (n_tiles == 1) {
+    // Decode-sized N (one activation tile): the launch is one wave, and its
+    // time is the larger of the weights' HBM time and the busiest SM's copy
+    // time (an SM lands about 85 GB/s of TMA boxes). Among the ways to cut it
+    // (CTAs per SM, tiles per CTA sharing their activations, K splits over a
+    // cluster that the GPCs can hold at once) take the fastest estimate; a
+    // split costs its cluster sum, and near-ties go to more CTAs.
+    const double hbm_s = ((double)p.mtiles_total * BM * g.K + (double)g.N * g.K) * 2.0 * g.Z / 6.3e12;
+    double best_t = 0;
+    long long best_ctas = 0;
+    for (int per_sm = 1; per_sm <= 2; ++per_sm)
+      for (int mt = 1; mt <= MAX_MT; mt *= 2)
+        for (int S = 1; S <= MAX_SPLITS; ++S) {
+          if (mt > 1 && (S > 1 || !mt_fits(mt))) continue;
+          Choice c{per_sm, mt, S};
+          if (!size_choice(c, p.n_tile, kchunks, rope_extra)) continue;
+          const long long groups = tiles_all / mt, ctas = groups * S;
+          if (ctas > (long long)per_sm * num_sms) continue;
+          if (S > 1 && groups > max_clusters(c.cpb, g.w_transposed != 0, c.smem_dyn, S)) continue;
+          const double cta_bytes = (double)((c.kstages + S - 1) / S) * c.stage_bytes;
+          const double busiest = (double)((ctas + num_sms - 1) / num_sms) * cta_bytes;
+          const double t = (hbm_s > busiest / 85e9 ? hbm_s : busiest / 85e9) + (S > 1 ? 1e-6 : 0.0);
+          if (!have || t < best_t * 0.99 || (t <= best_t * 1.01 && ctas > best_ctas)) {
+            best = c;
+            best_t = t;
+            best_ctas = ctas;
+            have = true;
+          }
+        }
   }
+  if (!have) {
+    // Many activation tiles (several tokens per sequence): when the tiles
+    // outnumber the SMs two CTAs share an SM (half the stage budget each,
+    // when the fp32 partial tile fits it) so that every tile is resident at
+    // once, and a CTA takes several tiles sharing their activations; else
+    // one CTA per SM keeps the most bytes in flight per tile and the
+    // reduction is split over a cluster.
+    Choice c{};
+    c.per_sm = (tiles_all > num_sms && (size_t)p.n_tile * CS_LD * 4 <= (size_t)SMEM_TWO) ? 2 : 1;
+    const int slots = num_sms * c.per_sm;
+    const int budget = c.per_sm == 2 ? SMEM_TWO : SMEM_ONE;
+    c.mt = 1;
+    if (tiles_all > slots)
+      for (int m = 2; m <= MAX_MT; m *= 2)
+        if (mt_fits(m) && (size_t)m * p.n_tile * CS_LD * 4 <= (size_t)budget) {
+          c.mt = m;
+          if (tiles_all / m <= slots) break;
+        }
+    const long long tiles = tiles_all / c.mt;
+    long long S = tiles >= slots ? 1 : slots / tiles;
+    if (S > MAX_SPLITS) S = MAX_SPLITS;
+    if (c.mt > 1 || S < 1) S = 1;
+    c.S = (int)S;
+    while (!size_choice(c, p.n_tile, kchunks, 0)) {
+      if (c.S > 1) { --c.S; continue; }
+      return cudaErrorInvalidValue;
+    }
+    best = c;
+  }
+  const int mt = best.mt, cpb = best.cpb;
   p.mt = mt;
-  // Chunks per stage: as many as keep two stages within the budget (one
-  // stage if it is the only one), at most what the reduction has.
-  auto stage_of = [&](int cpb) { return mt * cpb * CHUNK_A + cpb * p.n_tile * 128; };
-  int cpb = 4;
-  while (cpb > 1 && (cpb > kchunks || 2 * stage_of(cpb) > budget) &&
-         !(cpb <= kchunks && (kchunks + cpb - 1) / cpb == 1 && stage_of(cpb) <= budget))
-    cpb >>= 1;
-  p.stage_bytes = stage_of(cpb);
-  if (p.stage_bytes > budget) return cudaErrorInvalidValue;
-  p.kstages = (kchunks + cpb - 1) / cpb;
-  p.nstage = budget / p.stage_bytes;
-  if (p.nstage > 8) p.nstage = 8;
-  if (p.nstage > p.kstages) p.nstage = p.kstages;
-  const long long tiles = tiles1 / mt;
-  long long S = tiles >= num_sms ? 1 : num_sms / tiles;
-  if (S > MAX_SPLITS) S = MAX_SPLITS;
-  if (S > p.kstages) S = p.kstages;
-  if (mt > 1 || S < 1) S = 1;
-  p.splits = (int)S;
-  // Partial tiles [MT][n_tile][128] fp32, plus the reduced own rows when split.
-  const size_t cs_bytes = (size_t)mt * p.n_tile * BM * 4 + (S > 1 ? (size_t)((p.n_tile + S - 1) / S) * BM * 4 : 0);
-  const size_t stages = (size_t)p.nstage * p.stage_bytes;
-  const size_t smem_dyn = (cs_bytes > stages ? cs_bytes : stages) + 1024;
+  p.splits = best.S;
+  p.stage_bytes = best.stage_bytes;
+  p.kstages = best.kstages;
+  p.nstage = best.nstage;
+  const size_t smem_dyn = best.smem_dyn;
+  const long long S = best.S;
+  p.rope_off = have && roped ? best.rope_off : 0;
   p.tmem_cols = pow2_at_least((uint32_t)(mt * p.n_tile));
   p.idesc = idesc_bf16(BM, p.n_tile, g.w_transposed != 0, false);
   p.rope_cos = g.rope_cos; p.rope_sin = g.rope_sin; p.d_r = g.d_r; p.max_pos = g.max_pos;

@@ -660,7 +660,11 @@ def test_captured_step_matches_eager():
 def test_step_call_matches_four_calls(name):
     """mla_decode_step (S1 and c_Q in one launch where the tensor-core kernel
     takes both; MiniMind's W_UK^T falls back) writes the same cache rows and u
-    as the four entry points called in turn."""
+    as the four entry points called in turn. The fused launch may cut K into
+    other split-K pieces than the separate S1 and c_Q launches (one choice for
+    all its tiles), so its fp32 sums can associate differently: a stored
+    element then agrees to one bf16 rounding step, u to the end-to-end
+    tolerance."""
     shp = S.workload(name)
     B, L = 6, 400
     W = S.draw_weights(shp)
@@ -675,8 +679,11 @@ def test_step_call_matches_four_calls(name):
     cache_b = cache0.clone()
     u_b = dec.step(h, pos, cache_b, seqlens).clone()
     torch.cuda.synchronize()
-    assert torch.equal(cache_b, cache_a)
-    assert torch.equal(u_b, u_a)
+    a, b = host(cache_a), host(cache_b)
+    step = 2.0 ** -7 if shp.dtype == "bf16" else 2.0 ** -23
+    assert (np.abs(a - b) <= step * np.maximum(np.abs(a), np.abs(b))).all()
+    assert (a != b).mean() < 0.02
+    assert_close(host(u_b), host(u_a), shp.dtype, tol=TOL_E2E, what="u, fused step vs four calls")
     st, bits = M.mla_get_device_status(dec.handle)
     assert st == M.MLA_OK and bits == 0
     dec.close()
