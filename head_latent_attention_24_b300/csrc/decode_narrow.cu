@@ -95,7 +95,11 @@ struct Shape {
   static constexpr int Q_OFF = NSLOT * SLOT;           // two query buffers (piece parity)
   static constexpr int P_OFF = Q_OFF + 2 * Q_STRIDE;   // NPP P buffers (tile g in g % NPP)
   static constexpr int END = P_OFF + NPP * P_BYTES;
-  static constexpr int SMEM_DYN = END + 1024;
+  // the split plan when the kernel computes it (B + PLAN_EXTRA entries): what the ring leaves, at most 4 KB
+  static constexpr int PLAN_OFF = END;
+  static constexpr int PLAN_ROOM = (SMEM_LIMIT - CTL_RESERVE - 1024 - END) / 16 * 16;
+  static constexpr int PLAN_BYTES = PLAN_ROOM < 4096 ? PLAN_ROOM : 4096;
+  static constexpr int SMEM_DYN = END + PLAN_BYTES + 1024;
   // TMEM: NSB S^T buffers (16 columns each), then NOB O_t^T buffers (16 per latent block)
   static constexpr uint32_t S_COL = 0;
   static constexpr uint32_t O_COL = NSB * NPAD;
@@ -106,6 +110,7 @@ struct Shape {
   static_assert(NSLOT >= 3, "ring");
   static_assert(SLOT % 1024 == 0, "slot alignment");
   static_assert(SMEM_DYN + CTL_RESERVE <= SMEM_LIMIT, "shared memory");
+  static_assert(PLAN_BYTES >= 256, "plan room");
 };
 
 struct Ctl {   // static shared memory: at most CTL_RESERVE bytes
@@ -121,7 +126,7 @@ struct Ctl {   // static shared memory: at most CTL_RESERVE bytes
   float wmax[2][4][NPAD];     // per tile parity, TMEM lane quarter and head: the tile's maximum
   float wsum[4][NPAD];        // per TMEM lane quarter and head: the piece's softmax sum
 };
-static_assert(sizeof(Ctl) <= CTL_RESERVE, "control block");
+static_assert(sizeof(Ctl) + 512 <= CTL_RESERVE, "control block and the plan's scratch");
 
 // Every wait gives up after ctl.wait_limit cycles, or as soon as another role
 // of this CTA has given up; the first to expire records MLA_DEV_TIMEOUT.
@@ -236,6 +241,16 @@ __global__ void __launch_bounds__(96 + 128 * NGRP, 1)
   pdl_trigger();
   pdl_wait();      // the plan, the queries and the cache come from earlier kernels
   const uint32_t sbase = smem_u32(smem);
+  // The split plan: every CTA works it out from the lengths (CTA 0 also
+  // stores it for the merge kernel), or it comes from the plan launch.
+  const int32_t* plan = a.plan;
+  if (a.inline_plan) {
+    int32_t* ps = reinterpret_cast<int32_t*>(smem + L::PLAN_OFF);
+    plan_rows(a.seqlens, B, a.max_len, a.grid_chunks, 64, a.allow_whole, 2 * TR, ps, a.status, blockIdx.x == 0);
+    if (blockIdx.x == 0)
+      for (int i = threadIdx.x; i < B + PLAN_EXTRA; i += 96 + 128 * NGRP) a.plan[i] = ps[i];
+    plan = ps;
+  }
 
   if (warp == 0) {
     // ------------------------------------------------------------ TMA producer
@@ -245,7 +260,7 @@ __global__ void __launch_bounds__(96 + 128 * NGRP, 1)
       prefetch_tensormap(&map_qlat);
       prefetch_tensormap(&map_qrope);
       Pieces it;
-      it.init(a.plan, B, chunk);
+      it.init(plan, B, chunk);
       int seq, t0, t1;
       bool whole;
       int i = 0, piece = 0, qissued = 0;
@@ -291,7 +306,7 @@ __global__ void __launch_bounds__(96 + 128 * NGRP, 1)
       const uint64_t q_k = sdesc(sbase + L::Q_OFF, 16, 1024, 2);
       const uint64_t q_r = sdesc(sbase + L::Q_OFF, 16, L::ROPE_SBO, L::ROPE_LAYOUT);
       Pieces it;
-      it.init(a.plan, B, chunk);
+      it.init(plan, B, chunk);
       int seq, t0, t1;
       bool whole;
       int piece = 0, g = 0;
@@ -340,7 +355,7 @@ __global__ void __launch_bounds__(96 + 128 * NGRP, 1)
       const uint64_t ring_v = sdesc(sbase + L::RING_OFF, L::LAT_CHUNK, 1024, 2);
       const uint64_t p_k = sdesc(sbase + L::P_OFF, 16, 1024, 2);
       Pieces it;
-      it.init(a.plan, B, chunk);
+      it.init(plan, B, chunk);
       int seq, t0, t1;
       bool whole;
       int g = 0;
@@ -385,7 +400,7 @@ __global__ void __launch_bounds__(96 + 128 * NGRP, 1)
     const uint32_t lane_base = static_cast<uint32_t>(quarter * 32) << 16;
     const float sl2 = a.scale_log2;
     Pieces it;
-    it.init(a.plan, B, chunk);
+    it.init(plan, B, chunk);
     int seq, t0, t1;
     bool whole;
     int g = 0;
@@ -573,7 +588,7 @@ __global__ void __launch_bounds__(96 + 128 * NGRP, 1)
 }
 
 template <int DC, int DR, int NGRP>
-cudaError_t launch_typed(const DecodeArgs& a, cudaStream_t s) {
+cudaError_t launch_typed(const DecodeArgs& a, cudaStream_t s, bool* inlined) {
   using L = Shape<DC, DR>;
   const int D = DC + DR;
   CUtensorMap map_lat, map_rope, map_qlat, map_qrope;
@@ -603,9 +618,17 @@ cudaError_t launch_typed(const DecodeArgs& a, cudaStream_t s) {
     if (e != cudaSuccess) return e;
     attr_set = true;
   }
+  DecodeArgs k = a;
+  k.inline_plan = (a.B + PLAN_EXTRA) * 4 <= L::PLAN_BYTES;
+  *inlined = k.inline_plan != 0;
+  if (!k.inline_plan) {
+    cudaError_t e = launch_decode_plan(a.seqlens, a.B, a.max_len, a.grid_chunks, 64, a.allow_whole, 2 * TR, a.plan,
+                                       a.status, s);
+    if (e != cudaSuccess) return e;
+  }
   LaunchCfg lc(dim3((unsigned)a.grid_chunks), dim3(96 + 128 * NGRP), L::SMEM_DYN, s);
   cudaError_t e = cudaLaunchKernelEx(&lc.cfg, decode_narrow_kernel<DC, DR, NGRP>, map_lat, map_rope, map_qlat,
-                                     map_qrope, a);
+                                     map_qrope, k);
   if (e != cudaSuccess) return e;
   return cudaGetLastError();
 }
@@ -621,20 +644,19 @@ int decode_narrow_chunks(const mla_handle_s* h) { return h->num_sms < 1 ? 1 : h-
 
 cudaError_t launch_decode_narrow(const mla_handle_s* h, const DecodeArgs& a, cudaStream_t s, int* launches) {
   if (!decode_narrow_supported(h)) return cudaErrorInvalidValue;
-  cudaError_t e = launch_decode_plan(a.seqlens, a.B, a.max_len, a.grid_chunks, 64, a.allow_whole, 2 * TR, a.plan,
-                                     a.status, s);
-  if (e != cudaSuccess) return e;
   // one softmax group of four warps per four heads
   const int n_h = h->cfg.n_h;
+  bool inl = false;
+  cudaError_t e;
   if (h->cfg.d_r == 32)
-    e = n_h <= 4 ? launch_typed<128, 32, 1>(a, s) : n_h <= 8 ? launch_typed<128, 32, 2>(a, s)
-                                                             : launch_typed<128, 32, 4>(a, s);
+    e = n_h <= 4 ? launch_typed<128, 32, 1>(a, s, &inl) : n_h <= 8 ? launch_typed<128, 32, 2>(a, s, &inl)
+                                                                   : launch_typed<128, 32, 4>(a, s, &inl);
   else
-    e = n_h <= 4 ? launch_typed<128, 64, 1>(a, s) : n_h <= 8 ? launch_typed<128, 64, 2>(a, s)
-                                                             : launch_typed<128, 64, 4>(a, s);
+    e = n_h <= 4 ? launch_typed<128, 64, 1>(a, s, &inl) : n_h <= 8 ? launch_typed<128, 64, 2>(a, s, &inl)
+                                                                   : launch_typed<128, 64, 4>(a, s, &inl);
   if (e != cudaSuccess) return e;
   e = launch_decode_combine(a, MLA_BF16, s);
-  if (launches) *launches = 3;
+  if (launches) *launches = inl ? 2 : 3;
   return e;
 }
 

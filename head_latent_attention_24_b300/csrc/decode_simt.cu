@@ -51,75 +51,17 @@ __device__ __forceinline__ float warp_sum(float v) {
   for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
   return v;
 }
-__device__ __forceinline__ int warp_iscan(int v, int lane) {
-#pragma unroll
-  for (int o = 1; o < 32; o <<= 1) {
-    const int n = __shfl_up_sync(0xffffffffu, v, o);
-    if (lane >= o) v += n;
-  }
-  return v;
-}
 
-// plan[0..B] = cumulative clamped lengths, plan[B+1] = chunk length,
-// plan[B+2] = total rows, plan[B+3] = 1 when each chunk c < B takes sequence c
-// whole instead (see launch_decode_plan).
+// The split plan as its own launch (plan_rows, one CTA), for batches too
+// large for the attention kernels to compute it themselves.
 __global__ void __launch_bounds__(1024) decode_plan_kernel(const int32_t* __restrict__ seqlens, int B,
                                                            int max_len, int chunks, int granule,
                                                            int allow_whole, int split_cost_rows,
                                                            int32_t* __restrict__ plan,
                                                            int32_t* __restrict__ status) {
-  __shared__ int warp_tot[32];
-  __shared__ int warp_max[32];
-  __shared__ int carry, longest;
   pdl_trigger();
   pdl_wait();
-  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  if (tid == 0) { carry = 0; longest = 0; plan[0] = 0; }
-  __syncthreads();
-  for (int base = 0; base < B; base += 1024) {
-    const int b = base + tid;
-    int v = 0;
-    if (b < B) {
-      v = seqlens[b];
-      if (v < 0 || v > max_len) {
-        atomicOr(status, MLA_DEV_SEQLEN_RANGE);
-        v = v < 0 ? 0 : max_len;
-      }
-    }
-    int x = warp_iscan(v, lane);
-    int m = v;
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) m = max(m, __shfl_xor_sync(0xffffffffu, m, o));
-    if (lane == 31) warp_tot[warp] = x;
-    if (lane == 0) warp_max[warp] = m;
-    __syncthreads();
-    if (warp == 0) {
-      const int t = warp_iscan(warp_tot[lane], lane);
-      warp_tot[lane] = t;
-      int mm = warp_max[lane];
-#pragma unroll
-      for (int o = 16; o > 0; o >>= 1) mm = max(mm, __shfl_xor_sync(0xffffffffu, mm, o));
-      if (lane == 0) longest = max(longest, mm);
-    }
-    __syncthreads();
-    if (warp > 0) x += warp_tot[warp - 1];
-    if (b < B) plan[b + 1] = carry + x;
-    __syncthreads();
-    if (tid == 0) carry += warp_tot[31];
-    __syncthreads();
-  }
-  if (tid == 0) {
-    const int total = carry;
-    long long cl = ((long long)total + chunks - 1) / chunks;
-    cl = (cl + granule - 1) / granule * granule;
-    if (cl < granule) cl = granule;
-    plan[B + 1] = (int)cl;
-    plan[B + 2] = total;
-    // Whole sequences per chunk when every sequence has a chunk of its own and
-    // the longest one costs no more than an equal split plus the price of
-    // splitting (partial writes and their merge).
-    plan[B + 3] = (allow_whole && B <= chunks && (long long)longest <= cl + split_cost_rows) ? 1 : 0;
-  }
+  plan_rows(seqlens, B, max_len, chunks, granule, allow_whole, split_cost_rows, plan, status, true);
 }
 
 // First sequence whose row range contains global row r (skipping empty sequences).
@@ -294,8 +236,10 @@ __global__ void __launch_bounds__(256) decode_combine_kernel(const DecodeArgs a)
   const int b = blockIdx.x, warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int h = blockIdx.y * 8 + warp;
   const int B = a.B, d_c = a.d_c;
-  if (h >= a.n_h) return;
   const int32_t* cum = a.plan;
+  // whole sequences and none empty: the attention kernel wrote everything
+  if (cum[B + 3] && !cum[B + 4]) return;
+  if (h >= a.n_h) return;
   const int chunk_len = cum[B + 1];
   const int s0 = cum[b], s1 = cum[b + 1];
   T* o_out = static_cast<T*>(a.o_lat) + ((long long)b * a.n_h + h) * d_c;

@@ -146,18 +146,92 @@ struct DecodeArgs {
   int B, max_len, n_h, d_c, d_r;
   float scale_log2;            // scale * log2(e)
   // workspace carve-up
-  int32_t* plan;               // [B+1] cumulative lengths, then [chunk_len, total, whole]
+  int32_t* plan;               // [B+1] cumulative lengths, then [chunk_len, total, whole, any empty]
   float* part_o;               // [slots, n_h, d_c]
   float* part_lse;             // [slots, n_h]  (natural log)
   int grid_chunks;             // number of token chunks (CTAs along x)
   int allow_whole;             // the plan may give each chunk one whole sequence
+  int inline_plan;             // 1: every CTA of the few-head kernel computes the plan itself
+                               // (plan_rows into shared memory; CTA 0 also writes `plan`)
   long long wait_cycles;       // bound of every mbarrier wait (0 = the kernel's default, ~2 s)
   int fault;                   // 1: the tensor-core kernel withholds one internal arrival (test hook)
   int32_t* status;
 };
 
 // Workspace layout for decode: plan | partial O | partial LSE.
-constexpr int PLAN_EXTRA = 4;  // the plan holds B + PLAN_EXTRA int32 entries
+constexpr int PLAN_EXTRA = 5;  // the plan holds B + PLAN_EXTRA int32 entries
+
+// The split plan, computed by every thread of one CTA together (blockDim.x a
+// multiple of 32, at most 1024): plan[0..B] = cumulative lengths (clamped to
+// [0, max_len]), plan[B+1] = chunk length, plan[B+2] = total rows, plan[B+3]
+// = 1 when chunk c < B takes the whole of sequence c, plan[B+4] = 1 when some
+// sequence is empty. `plan` may be shared or global memory; a length out of
+// range is flagged in `status` when flag_errors. Ends with a barrier.
+__device__ __forceinline__ void plan_rows(const int32_t* __restrict__ seqlens, int B, int max_len, int chunks,
+                                          int granule, int allow_whole, int split_cost_rows, int32_t* plan,
+                                          int32_t* status, bool flag_errors) {
+  __shared__ int warp_tot[32], warp_max[32];
+  __shared__ int carry, longest, empty;
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5, nw = blockDim.x >> 5;
+  if (tid == 0) { carry = 0; longest = 0; empty = 0; plan[0] = 0; }
+  __syncthreads();
+  for (int base = 0; base < B; base += blockDim.x) {
+    const int b = base + tid;
+    int v = 0;
+    if (b < B) {
+      v = seqlens[b];
+      if (v < 0 || v > max_len) {
+        if (flag_errors) atomicOr(status, MLA_DEV_SEQLEN_RANGE);
+        v = v < 0 ? 0 : max_len;
+      }
+      if (v == 0) empty = 1;
+    }
+    int x = v, m = v;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int n = __shfl_up_sync(0xffffffffu, x, o);
+      if (lane >= o) x += n;
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) m = max(m, __shfl_xor_sync(0xffffffffu, m, o));
+    if (lane == 31) warp_tot[warp] = x;
+    if (lane == 0) warp_max[warp] = m;
+    __syncthreads();
+    if (warp == 0) {
+      int t = lane < nw ? warp_tot[lane] : 0, mm = lane < nw ? warp_max[lane] : 0;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const int n = __shfl_up_sync(0xffffffffu, t, o);
+        if (lane >= o) t += n;
+      }
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) mm = max(mm, __shfl_xor_sync(0xffffffffu, mm, o));
+      if (lane < nw) warp_tot[lane] = t;
+      if (lane == 0) longest = max(longest, mm);
+    }
+    __syncthreads();
+    if (warp > 0) x += warp_tot[warp - 1];
+    if (b < B) plan[b + 1] = carry + x;
+    __syncthreads();
+    if (tid == 0) carry += warp_tot[nw - 1];
+    __syncthreads();
+  }
+  if (tid == 0) {
+    const int total = carry;
+    long long cl = ((long long)total + chunks - 1) / chunks;
+    cl = (cl + granule - 1) / granule * granule;
+    if (cl < granule) cl = granule;
+    plan[B + 1] = (int)cl;
+    plan[B + 2] = total;
+    // Whole sequences per chunk when every sequence has a chunk of its own and
+    // the longest one costs no more than an equal split plus the price of
+    // splitting (partial writes and their merge).
+    const bool whole = allow_whole && B <= chunks && (long long)longest <= cl + split_cost_rows;
+    plan[B + 3] = whole ? 1 : 0;
+    plan[B + 4] = empty ? 1 : 0;
+  }
+  __syncthreads();
+}
 size_t decode_ws_bytes(int B, int n_h, int d_c, int chunks);
 void decode_ws_carve(void* ws, int B, int n_h, int d_c, int chunks,
                      int32_t** plan, float** part_o, float** part_lse);
