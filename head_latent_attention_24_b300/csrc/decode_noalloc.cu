@@ -24,24 +24,23 @@ constexpr int kHeadsPerCta = 16;                          // the CUDA-core kerne
 __device__ __align__(256) unsigned char g_noalloc_scratch[kNoAllocScratchBytes];
 
 std::mutex g_setup_mu;
-void* g_scratch_addr[kMaxDevices];
 int g_num_sms[kMaxDevices];
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
-// Device address of the scratch array and the SM count, set up once per device.
+// Device address of the scratch array (looked up on every call: a device
+// reset reloads the module and moves it) and the SM count (cached per device).
 mla_status_t device_scratch(int dev, void** addr, int* sms) {
+  void* p = nullptr;
+  if (cudaGetSymbolAddress(&p, g_noalloc_scratch) != cudaSuccess || !p) return MLA_ERR_CUDA;
   std::lock_guard<std::mutex> lock(g_setup_mu);
-  if (!g_scratch_addr[dev]) {
-    void* p = nullptr;
-    if (cudaGetSymbolAddress(&p, g_noalloc_scratch) != cudaSuccess || !p) return MLA_ERR_CUDA;
+  if (g_num_sms[dev] <= 0) {
     int n = 0;
     if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0)
       return MLA_ERR_CUDA;
     g_num_sms[dev] = n;
-    g_scratch_addr[dev] = p;
   }
-  *addr = g_scratch_addr[dev];
+  *addr = p;
   *sms = g_num_sms[dev];
   return MLA_OK;
 }
