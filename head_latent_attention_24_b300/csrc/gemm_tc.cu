@@ -636,7 +636,9 @@ cudaError_t launch_gemm_tc(const TcGemm& g, int num_sms, cudaStream_t s) {
     // time (an SM lands about 85 GB/s of TMA boxes). Among the ways to cut it
     // (CTAs per SM, tiles per CTA sharing their activations, K splits over a
     // cluster that the GPCs can hold at once) take the fastest estimate; a
-    // split costs its cluster sum, and near-ties go to more CTAs.
+    // split costs its cluster sum. The estimate leaves out the epilogue, which
+    // is latency-bound and shorter with fewer tiles per CTA and more CTAs per
+    // SM, so estimates within 15 % count as a tie and go to more CTAs.
     const double hbm_s = ((double)p.mtiles_total * BM * g.K + (double)g.N * g.K) * 2.0 * g.Z / 6.3e12;
     double best_t = 0;
     long long best_ctas = 0;
@@ -652,7 +654,8 @@ cudaError_t launch_gemm_tc(const TcGemm& g, int num_sms, cudaStream_t s) {
           const double cta_bytes = (double)((c.kstages + S - 1) / S) * c.stage_bytes;
           const double busiest = (double)((ctas + num_sms - 1) / num_sms) * cta_bytes;
           const double t = (hbm_s > busiest / 85e9 ? hbm_s : busiest / 85e9) + (S > 1 ? 1e-6 : 0.0);
-          if (!have || t < best_t * 0.99 || (t <= best_t * 1.01 && ctas > best_ctas)) {
+          const bool better = ctas > best_ctas ? t <= best_t * 1.15 : t * 1.15 < best_t;
+          if (!have || better) {
             best = c;
             best_t = t;
             best_ctas = ctas;
