@@ -5,11 +5,15 @@
 // visibility with a cache; page "MLA：潜在表示压缩与解耦 RoPE", §6 k = [k_C ; k_R]
 // with the RoPE key shared by the heads, §7 scale 1/sqrt(d_h + d_r)).
 //
-// One CTA per (128 queries, head, sequence). The query tile (128 x 192) is
-// moved into TMEM once and is the A operand of every QK; key tiles of 128 rows
-// stream through two TMA rings, a two-stage one for k_C (128 x 128) with the
-// shared k_R (128 x 64, read straight from the cache rows), freed after the
-// tile's QK, and a three-stage one for v_C (128 x 128), freed after its PV.
+// One CTA per SM runs work items of 128 queries of one head of one sequence,
+// longest key ranges first. An item's query tile (128 x 192) is moved into
+// TMEM and is the A operand of every QK; key tiles of 128 rows stream through
+// two TMA rings, a two-stage one for k_C (128 x 128) with the shared k_R
+// (128 x 64, read straight from the cache rows), freed after the tile's QK,
+// and a three-stage one for v_C (128 x 128), freed after its PV. The next
+// item's query tile comes through the key ring behind the current item's
+// keys and goes into TMEM as soon as the current item's last scores are read,
+// so its first QK runs during the current item's last PV and epilogue.
 // Per key tile:
 //   S = Q . K^T      M = 128 queries, N = 128 keys, K = 192   (TMEM)
 //   P = 2^(S*scale*log2e - m)  in bf16, written by the softmax threads into TMEM
@@ -23,10 +27,12 @@
 // tile j+1 runs on the tensor core while the softmax works on tile j.
 //
 // Warp 0 issues TMA, warp 1 owns TMEM and issues the QK MMAs, warp 2 the PV
-// MMAs, warps 3-10 run the softmax and the epilogue (two warps per query row,
+// MMAs, warps 3-10 move the queries and run the softmax and the epilogue (two warps per query row,
 // each with half of the tile's keys). Every mbarrier wait is bounded;
 // on expiry the CTA records MLA_DEV_TIMEOUT, stops issuing work, waits
 // (bounded) for its own copies in flight and frees its TMEM.
+#include <atomic>
+
 #include "internal.cuh"
 #include "tc_ptx.cuh"
 #include "tmap.cuh"
@@ -56,10 +62,6 @@ constexpr int NKS = 2, NVS = 3;
 constexpr int KRING_OFF = 0;
 constexpr int VRING_OFF = KRING_OFF + NKS * KSTAGE;
 constexpr int SMEM_DYN = VRING_OFF + NVS * VSTAGE + 1024;
-// The query tile lands in key stage 1 (3 chunks, the size of a key stage);
-// the softmax warps move it into TMEM, where it is the A operand of QK, and
-// hand the stage back for key tile 1.
-constexpr int Q_STAGE = 1;
 // TMEM columns
 constexpr uint32_t S_COL = 0;                     // 128 fp32
 constexpr uint32_t O_COL = 128;                   // 128 fp32
@@ -67,8 +69,19 @@ constexpr uint32_t P_COL = 256;                   // 64: 128 bf16 packed two per
 constexpr uint32_t Q_COL = 320;                   // 96: 192 bf16 packed two per column
 constexpr uint32_t TMEM_COLS = 512;
 
+// Work items are handed out at run time: the key-ring producer takes the next
+// item index from a per-launch device counter and passes it to the other
+// roles through a small ring in shared memory (NIR entries; the readers are
+// the value producer, both MMA issuers and the eight softmax warps).
+constexpr int NIR = 4, IR_READERS = 11;
+constexpr int NCTR = 64;   // launches in flight that may use the counters at once
+__device__ unsigned int g_item_next[NCTR];
+__device__ unsigned int g_cta_done[NCTR];
+
 struct Ctl {
-  uint64_t q_full, q_ready, k_full[NKS], k_empty[NKS], v_full[NVS], v_empty[NVS];
+  uint64_t q_ready, k_full[NKS], k_empty[NKS], v_full[NVS], v_empty[NVS];
+  uint64_t ir_full[NIR], ir_empty[NIR];
+  int ir_item[NIR];
   uint64_t s_full, s_free, p_full, pv_done, mma_done;
   uint32_t tmem_base;
   int abort;
@@ -114,26 +127,55 @@ __device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
   return *reinterpret_cast<uint32_t*>(&v);
 }
 
+// One work item: 128 queries of one head of one sequence. Items are numbered
+// sequence- and head-major and, inside a head, longest key range first (the
+// last query tile first): the CTAs working at one time share a few heads'
+// keys and values in L2, and the short items come last.
+struct Item {
+  int q0, head, b;   // first query of the tile, head, sequence
+  int qp0, nq, nk;   // position of the first query, queries in the tile, key tiles
+  int qp_last;
+};
+
+__device__ __forceinline__ Item item_of(const MhaArgs& a, int k, bool flag) {
+  const int nqt = (a.T + TQ - 1) / TQ;
+  Item it;
+  const int bh = k / nqt, qt = nqt - 1 - k % nqt;
+  it.b = bh / a.n_h;
+  it.head = bh % a.n_h;
+  it.q0 = qt * TQ;
+  int pos0 = a.q_pos0[it.b];
+  if (pos0 < 0 || pos0 > a.max_len - a.T) {
+    if (flag) atomicOr(a.status, MLA_DEV_QPOS_RANGE);
+    pos0 = pos0 < 0 ? 0 : a.max_len - a.T;
+  }
+  it.nq = min(TQ, a.T - it.q0);
+  it.qp0 = pos0 + it.q0;
+  it.qp_last = it.qp0 + it.nq - 1;
+  it.nk = it.qp_last / TK + 1;
+  return it;
+}
+
 __global__ void __launch_bounds__(NTHREADS, 1)
     mha_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ CUtensorMap map_k,
                   const __grid_constant__ CUtensorMap map_v, const __grid_constant__ CUtensorMap map_kr,
-                  const MhaArgs a) {
+                  const MhaArgs a, const int ctr) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   __shared__ Ctl ctl;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int q0 = blockIdx.x * TQ, head = blockIdx.y, b = blockIdx.z;
+  const int items = ((a.T + TQ - 1) / TQ) * a.n_h * a.B;
 
   if (threadIdx.x == 0) {
-    mbar_init(&ctl.q_full, 1);
-    mbar_init(&ctl.q_ready, 8);
     for (int i = 0; i < NKS; ++i) { mbar_init(&ctl.k_full[i], 1); mbar_init(&ctl.k_empty[i], 1); }
     for (int i = 0; i < NVS; ++i) { mbar_init(&ctl.v_full[i], 1); mbar_init(&ctl.v_empty[i], 1); }
+    mbar_init(&ctl.q_ready, 8);
     mbar_init(&ctl.s_full, 1);
     mbar_init(&ctl.s_free, 8);
     mbar_init(&ctl.p_full, 8);
     mbar_init(&ctl.pv_done, 1);
     mbar_init(&ctl.mma_done, 2);
+    for (int i = 0; i < NIR; ++i) { mbar_init(&ctl.ir_full[i], 1); mbar_init(&ctl.ir_empty[i], IR_READERS); }
     ctl.abort = 0;
     ctl.wait_limit = a.wait_cycles > 0 ? a.wait_cycles : WAIT_CYCLES;
     fence_mbar_init();
@@ -148,83 +190,106 @@ __global__ void __launch_bounds__(NTHREADS, 1)
   const uint32_t tbase = ctl.tmem_base;
   pdl_trigger();
   pdl_wait();   // q, k_c and v_c come from earlier kernels
-
-  // The queries of this tile sit at positions qp0 .. qp0 + nq - 1 and see keys
-  // 0 .. qp_last; key tiles 0 .. nk - 1 cover them.
-  int pos0 = a.q_pos0[b];
-  if (pos0 < 0 || pos0 > a.max_len - a.T) {
-    if (threadIdx.x == 0 && blockIdx.x == 0 && head == 0) atomicOr(a.status, MLA_DEV_QPOS_RANGE);
-    pos0 = pos0 < 0 ? 0 : a.max_len - a.T;
-  }
-  const int nq = min(TQ, a.T - q0);
-  const int qp0 = pos0 + q0, qp_last = qp0 + nq - 1;
-  const int nk = qp_last / TK + 1;
   const uint32_t sbase = smem_u32(smem);
+  // The e-th item of this CTA (-1: no more), from the item ring; each reading
+  // thread (one per reading warp) frees its entry once it has the index.
+  auto next_item = [&](int e, int& k) -> bool {
+    const int sl = e % NIR;
+    if (!wait_or_abort(&ctl.ir_full[sl], (e / NIR) & 1, ctl, a.status)) return false;
+    k = *reinterpret_cast<volatile int*>(&ctl.ir_item[sl]);
+    mbar_arrive(&ctl.ir_empty[sl]);
+    return true;
+  };
 
+  // The key ring carries, per item, the query tile (3 chunks, the size of a
+  // key stage) and then the item's key tiles; load n of the CTA goes to stage
+  // n % NKS. The value ring and the score / P / PV handshakes count the CTA's
+  // key tiles over all its items.
   if (warp == 0) {
     // ------------------------------------------------------------ TMA producers
-    // lane 0: the queries, then the key stages; lane 1: the value stages
+    // lane 0: the queries and the key stages; lane 1: the value stages
     if (lane == 0) {
       prefetch_tensormap(&map_q);
       prefetch_tensormap(&map_k);
       prefetch_tensormap(&map_kr);
-      const int qrow = b * a.T + q0;
-      mbar_arrive_expect_tx(&ctl.q_full, 3 * CHUNK);
-      tma_load_3d(smem + KRING_OFF + Q_STAGE * KSTAGE, &map_q, &ctl.q_full, 0, qrow, head * 3);
-      int i = 0;
+      int n = 0;
       bool ok = true;
-      for (; i < nk; ++i) {
-        const int st = i % NKS;
-        if (i >= NKS) ok = wait_or_abort(&ctl.k_empty[st], ((i / NKS) - 1) & 1, ctl, a.status);
-        else if (st == Q_STAGE) ok = wait_or_abort(&ctl.q_ready, 0, ctl, a.status);   // the queries have left
+      for (int e = 0; ok; ++e) {
+        const int sl = e % NIR;
+        if (e >= NIR) ok = wait_or_abort(&ctl.ir_empty[sl], ((e / NIR) - 1) & 1, ctl, a.status);
         if (!ok) break;
-        uint8_t* dst = smem + KRING_OFF + st * KSTAGE;
-        const int krow = b * a.max_len + i * TK;
-        mbar_arrive_expect_tx(&ctl.k_full[st], KSTAGE);
-        tma_load_3d(dst, &map_k, &ctl.k_full[st], 0, krow, head * 2);
-        tma_load_2d(dst + 2 * CHUNK, &map_kr, &ctl.k_full[st], 0, krow);
+        const unsigned int got = atomicAdd(&g_item_next[ctr], 1u);
+        const int k = got < (unsigned int)items ? (int)got : -1;
+        ctl.ir_item[sl] = k;
+        mbar_arrive(&ctl.ir_full[sl]);
+        if (k < 0) break;
+        const Item it = item_of(a, k, false);
+        for (int j = -1; j < it.nk; ++j, ++n) {   // j = -1: the query tile
+          const int st = n % NKS;
+          if (n >= NKS) ok = wait_or_abort(&ctl.k_empty[st], ((n / NKS) - 1) & 1, ctl, a.status);
+          if (!ok) break;
+          uint8_t* dst = smem + KRING_OFF + st * KSTAGE;
+          mbar_arrive_expect_tx(&ctl.k_full[st], KSTAGE);
+          if (j < 0) {
+            tma_load_3d(dst, &map_q, &ctl.k_full[st], 0, it.b * a.T + it.q0, it.head * 3);
+          } else {
+            const int krow = it.b * a.max_len + j * TK;
+            tma_load_3d(dst, &map_k, &ctl.k_full[st], 0, krow, it.head * 2);
+            tma_load_2d(dst + 2 * CHUNK, &map_kr, &ctl.k_full[st], 0, krow);
+          }
+        }
       }
-      if (!ok) {   // no copy lands after the CTA moves on
-        drain_ring(ctl.k_full, NKS, i);
-        mbar_wait(&ctl.q_full, 0, WAIT_CYCLES / 8);
-      }
+      if (!ok) drain_ring(ctl.k_full, NKS, n);   // no copy lands after the CTA moves on
     } else if (lane == 1) {
       prefetch_tensormap(&map_v);
-      int i = 0;
+      int n = 0, k = 0;
       bool ok = true;
-      for (; i < nk; ++i) {
-        const int st = i % NVS;
-        if (i >= NVS) ok = wait_or_abort(&ctl.v_empty[st], ((i / NVS) - 1) & 1, ctl, a.status);
-        if (!ok) break;
-        mbar_arrive_expect_tx(&ctl.v_full[st], VSTAGE);
-        tma_load_3d(smem + VRING_OFF + st * VSTAGE, &map_v, &ctl.v_full[st], 0, b * a.max_len + i * TK, head * 2);
+      for (int e = 0; ok && (ok = next_item(e, k)) && k >= 0; ++e) {
+        const Item it = item_of(a, k, false);
+        for (int j = 0; j < it.nk; ++j, ++n) {
+          const int st = n % NVS;
+          if (n >= NVS) ok = wait_or_abort(&ctl.v_empty[st], ((n / NVS) - 1) & 1, ctl, a.status);
+          if (!ok) break;
+          mbar_arrive_expect_tx(&ctl.v_full[st], VSTAGE);
+          tma_load_3d(smem + VRING_OFF + st * VSTAGE, &map_v, &ctl.v_full[st], 0, it.b * a.max_len + j * TK,
+                      it.head * 2);
+        }
       }
-      if (!ok) drain_ring(ctl.v_full, NVS, i);
+      if (!ok) drain_ring(ctl.v_full, NVS, n);
     }
   } else if (warp == 1) {
     // ------------------------------------------------------------ QK issuer
-    // S(j) = Q . K(j)^T (Q from TMEM) once key stage j has landed and the
-    // softmax has read S(j-1). QK and PV have an issuing thread each, so that
-    // a PV never waits behind the next tile's load.
+    // S(g) = Q . K(g)^T (Q from TMEM) once key stage g has landed and the
+    // softmax has read S(g-1); for an item's first tile, once its queries are
+    // in TMEM (which also frees their stage). QK and PV have an issuing thread
+    // each, so that a PV never waits behind the next tile's load.
     if (lane == 0) {
       constexpr uint32_t IDESC_QK = idesc_bf16(TQ, TK, false, false);
       const uint64_t k_desc = sdesc_sw128(sbase + KRING_OFF, 16, 1024);
-      bool ok = wait_or_abort(&ctl.q_ready, 0, ctl, a.status);
-      for (int j = 0; j < nk && ok; ++j) {
-        const int st = j % NKS;
-        ok = wait_or_abort(&ctl.k_full[st], (j / NKS) & 1, ctl, a.status) &&
-             (j < 1 || wait_or_abort(&ctl.s_free, (j - 1) & 1, ctl, a.status));
+      int n = 0, g = 0, k = 0;
+      bool ok = true;
+      for (int i = 0; ok && (ok = next_item(i, k)) && k >= 0; ++i) {
+        const Item it = item_of(a, k, false);
+        ok = wait_or_abort(&ctl.q_ready, i & 1, ctl, a.status);
         if (!ok) break;
-        tc_fence_after();
-        const uint64_t kd = k_desc + (uint64_t)((st * KSTAGE) >> 4);
+        mbar_arrive(&ctl.k_empty[n % NKS]);   // the query stage: copied into TMEM
+        ++n;
+        for (int j = 0; j < it.nk; ++j, ++n, ++g) {
+          const int st = n % NKS;
+          ok = wait_or_abort(&ctl.k_full[st], (n / NKS) & 1, ctl, a.status) &&
+               (g < 1 || wait_or_abort(&ctl.s_free, (g - 1) & 1, ctl, a.status));
+          if (!ok) break;
+          tc_fence_after();
+          const uint64_t kd = k_desc + (uint64_t)((st * KSTAGE) >> 4);
 #pragma unroll
-        for (int c = 0; c < 3; ++c)
+          for (int c = 0; c < 3; ++c)
 #pragma unroll
-          for (int k = 0; k < 4; ++k)
-            mma_bf16_ta(tbase + S_COL, tbase + Q_COL + c * 32 + k * 8, kd + (uint64_t)((c * CHUNK + k * 32) >> 4),
-                        IDESC_QK, (c > 0 || k > 0) ? 1u : 0u);
-        mma_commit(&ctl.s_full);
-        mma_commit(&ctl.k_empty[st]);   // the key stage: its QK is done
+            for (int kk = 0; kk < 4; ++kk)
+              mma_bf16_ta(tbase + S_COL, tbase + Q_COL + c * 32 + kk * 8, kd + (uint64_t)((c * CHUNK + kk * 32) >> 4),
+                          IDESC_QK, (c > 0 || kk > 0) ? 1u : 0u);
+          mma_commit(&ctl.s_full);
+          mma_commit(&ctl.k_empty[st]);   // the key stage: its QK is done
+        }
       }
       // nothing of this CTA's reaches the tensor cores after it moves on
       mma_commit(&ctl.mma_done);
@@ -232,25 +297,30 @@ __global__ void __launch_bounds__(NTHREADS, 1)
     }
   } else if (warp == 2) {
     // ------------------------------------------------------------ PV issuer
-    // O += P(j) . V(j) once the softmax has written P(j) and V(j) has landed;
-    // the value stage is free when this PV completes.
+    // O += P(g) . V(g) once the softmax has written P(g) and V(g) has landed;
+    // an item's first PV starts O afresh. The value stage is free when this
+    // PV completes.
     if (lane == 0) {
       constexpr uint32_t IDESC_PV = idesc_bf16(TQ, DH, false, true);
       const uint64_t v_desc = sdesc_sw128(sbase + VRING_OFF, CHUNK, 1024);
+      int g = 0, k = 0;
       bool ok = true;
-      for (int j = 0; j < nk && ok; ++j) {
-        const int st = j % NVS;
-        ok = wait_or_abort(&ctl.p_full, j & 1, ctl, a.status) &&
-             wait_or_abort(&ctl.v_full[st], (j / NVS) & 1, ctl, a.status);
-        if (!ok) break;
-        tc_fence_after();
-        const uint64_t vd = v_desc + (uint64_t)((st * VSTAGE) >> 4);
+      for (int e = 0; ok && (ok = next_item(e, k)) && k >= 0; ++e) {
+        const Item it = item_of(a, k, false);
+        for (int j = 0; j < it.nk; ++j, ++g) {
+          const int st = g % NVS;
+          ok = wait_or_abort(&ctl.p_full, g & 1, ctl, a.status) &&
+               wait_or_abort(&ctl.v_full[st], (g / NVS) & 1, ctl, a.status);
+          if (!ok) break;
+          tc_fence_after();
+          const uint64_t vd = v_desc + (uint64_t)((st * VSTAGE) >> 4);
 #pragma unroll
-        for (int k = 0; k < TK / 16; ++k)
-          mma_bf16_ta(tbase + O_COL, tbase + P_COL + k * 8, vd + (uint64_t)((k * 2048) >> 4), IDESC_PV,
-                      (j > 0 || k > 0) ? 1u : 0u);
-        mma_commit(&ctl.pv_done);
-        mma_commit(&ctl.v_empty[st]);
+          for (int kk = 0; kk < TK / 16; ++kk)
+            mma_bf16_ta(tbase + O_COL, tbase + P_COL + kk * 8, vd + (uint64_t)((kk * 2048) >> 4), IDESC_PV,
+                        (j > 0 || kk > 0) ? 1u : 0u);
+          mma_commit(&ctl.pv_done);
+          mma_commit(&ctl.v_empty[st]);
+        }
       }
       mma_commit(&ctl.mma_done);
       mbar_wait(&ctl.mma_done, 0, WAIT_CYCLES / 8);
@@ -264,15 +334,17 @@ __global__ void __launch_bounds__(NTHREADS, 1)
     const int quarter = warp & 3, half = (warp - 3) >> 2;
     const int r = quarter * 32 + lane;                 // TMEM lane = query row of the tile
     const uint32_t lane_base = static_cast<uint32_t>(quarter * 32) << 16;
-    const int qp = qp0 + r;                            // this row's position (rows past nq: not stored)
     const float sl2 = a.scale_log2;
     constexpr int HK = TK / 2;                         // keys per half
-    float m_ref = -INFINITY, l = 0.f;
-    // The query tile from key stage Q_STAGE into TMEM (row r = lane r, 32
-    // columns per 64-column chunk): half 0 moves chunks 0 and 1, half 1 chunk 2.
-    bool ok = pair_all(quarter, __all_sync(0xffffffffu, wait_or_abort(&ctl.q_full, 0, ctl, a.status)));
-    if (ok) {
-      const uint8_t* qs = smem + KRING_OFF + Q_STAGE * KSTAGE + (r >> 3) * 1024 + (r & 7) * 128;
+    // An item's query tile from its key-ring stage into TMEM (row r = lane r,
+    // 32 columns per 64-column chunk): half 0 moves chunks 0 and 1, half 1
+    // chunk 2. The previous item's last QK, the last reader of the queries in
+    // TMEM, has completed: its scores have been waited for.
+    auto move_queries = [&](int n) -> bool {
+      const int st = n % NKS;
+      if (!pair_all(quarter, __all_sync(0xffffffffu, wait_or_abort(&ctl.k_full[st], (n / NKS) & 1, ctl, a.status))))
+        return false;
+      const uint8_t* qs = smem + KRING_OFF + st * KSTAGE + (r >> 3) * 1024 + (r & 7) * 128;
       for (int c = half * 2; c < (half == 0 ? 2 : 3); ++c) {
         uint32_t w[32];
 #pragma unroll
@@ -285,120 +357,147 @@ __global__ void __launch_bounds__(NTHREADS, 1)
       asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive(&ctl.q_ready);   // also: the stage may take key tile 1
-    }
-    for (int j = 0; j < nk && ok; ++j) {
-      const int k0 = j * TK + half * HK;
-      ok = pair_all(quarter, __all_sync(0xffffffffu, wait_or_abort(&ctl.s_full, j & 1, ctl, a.status)));
-      if (!ok) break;
-      tc_fence_after();
-      float s[HK];
-      tmem_ld32(tbase + lane_base + S_COL + half * HK, s);
-      tmem_ld32(tbase + lane_base + S_COL + half * HK + 32, s + 32);
-      tmem_ld_wait();
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&ctl.s_free);
-      // causal mask: key k0 + c is visible to this row when k0 + c <= qp
-      const int nvis = max(0, min(HK, qp - k0 + 1));
-      // Tiles below the diagonal (every key visible to every row of the warp)
-      // take the short path: the maximum of the raw scores, scaled once, and
-      // the scale folded into the exponent's FMA.
-      const bool full = __all_sync(0xffffffffu, nvis == HK);
-      float mx = -INFINITY;
-      if (full) {
-#pragma unroll
-        for (int c = 0; c < HK; ++c) mx = fmaxf(mx, s[c]);
-        mx *= sl2;
-      } else {
-#pragma unroll
-        for (int c = 0; c < HK; ++c) {
-          s[c] = c < nvis ? s[c] * sl2 : -INFINITY;
-          mx = fmaxf(mx, s[c]);
-        }
-      }
-      ctl.mx[j & 1][half][r] = mx;
-      pair_sync(quarter);
-      mx = fmaxf(mx, ctl.mx[j & 1][half ^ 1][r]);   // the row's tile maximum, the same in both halves
-      float alpha = 1.f;
-      if (mx > m_ref + RESCALE_THRESHOLD) {   // also the first tile a row sees anything (m_ref = -inf)
-        alpha = ex2_approx(m_ref - mx);
-        m_ref = mx;
-      }
-      uint32_t pk[HK / 2];
-      float lsum0 = 0.f, lsum1 = 0.f;   // the softmax sum from the unrounded weights
-      if (full) {
-        const float neg = -m_ref;
-#pragma unroll
-        for (int c = 0; c < HK; c += 2) {
-          const float p0 = ex2_approx(fmaf(s[c], sl2, neg)), p1 = ex2_approx(fmaf(s[c + 1], sl2, neg));
-          lsum0 += p0;
-          lsum1 += p1;
-          pk[c / 2] = pack_bf16(p0, p1);
-        }
-      } else {
-#pragma unroll
-        for (int c = 0; c < HK; c += 2) {
-          const float p0 = c < nvis ? ex2_approx(s[c] - m_ref) : 0.f;
-          const float p1 = c + 1 < nvis ? ex2_approx(s[c + 1] - m_ref) : 0.f;
-          lsum0 += p0;
-          lsum1 += p1;
-          pk[c / 2] = pack_bf16(p0, p1);
-        }
-      }
-      l = l * alpha + (lsum0 + lsum1);   // this half's share of the row sum
-      // P(j) replaces P(j-1) in TMEM and O is rescaled: both only after PV(j-1)
-      if (j > 0) {
-        ok = pair_all(quarter, __all_sync(0xffffffffu, wait_or_abort(&ctl.pv_done, (j - 1) & 1, ctl, a.status)));
+      if (lane == 0) mbar_arrive(&ctl.q_ready);
+      return true;
+    };
+    // the CTA's items, read by lane 0 of each softmax warp
+    auto item_at = [&](int e, int& k) -> bool {
+      int kk = 0;
+      bool got = true;
+      if (lane == 0) got = next_item(e, kk);
+      got = pair_all(quarter, __all_sync(0xffffffffu, __shfl_sync(0xffffffffu, got ? 1 : 0, 0) != 0));
+      k = __shfl_sync(0xffffffffu, kk, 0);
+      return got;
+    };
+    int n = 0, g = 0;   // key-ring loads and key tiles of this CTA so far
+    int k = 0, k_next = 0;
+    bool ok = item_at(0, k) && (k < 0 || move_queries(0));
+    Item nxt = item_of(a, k < 0 ? 0 : k, threadIdx.x == 96 && k >= 0);
+    for (int e = 0; ok && k >= 0; ++e, k = k_next) {
+      const Item it = nxt;
+      const int qp = it.qp0 + r;                       // this row's position (rows past nq: not stored)
+      float m_ref = -INFINITY, l = 0.f;
+      ++n;                                             // past the query tile
+      for (int j = 0; j < it.nk && ok; ++j, ++n, ++g) {
+        const int k0 = j * TK + half * HK;
+        ok = pair_all(quarter, __all_sync(0xffffffffu, wait_or_abort(&ctl.s_full, g & 1, ctl, a.status)));
         if (!ok) break;
         tc_fence_after();
-        if (__any_sync(0xffffffffu, alpha != 1.f)) {
-#pragma unroll 1
-          for (int c = 0; c < DH / 2; c += 32) {
-            float v[32];
-            tmem_ld32(tbase + lane_base + O_COL + half * (DH / 2) + c, v);
-            tmem_ld_wait();
-            uint32_t w[32];
+        float s[HK];
+        tmem_ld32(tbase + lane_base + S_COL + half * HK, s);
+        tmem_ld32(tbase + lane_base + S_COL + half * HK + 32, s + 32);
+        tmem_ld_wait();
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&ctl.s_free);
+        // causal mask: key k0 + c is visible to this row when k0 + c <= qp
+        const int nvis = max(0, min(HK, qp - k0 + 1));
+        // Tiles below the diagonal (every key visible to every row of the warp)
+        // take the short path: the maximum of the raw scores, scaled once, and
+        // the scale folded into the exponent's FMA.
+        const bool full = __all_sync(0xffffffffu, nvis == HK);
+        float mx = -INFINITY;
+        if (full) {
 #pragma unroll
-            for (int e = 0; e < 32; ++e) w[e] = __float_as_uint(v[e] * alpha);
-            tmem_st32(tbase + lane_base + O_COL + half * (DH / 2) + c, w);
+          for (int c = 0; c < HK; ++c) mx = fmaxf(mx, s[c]);
+          mx *= sl2;
+        } else {
+#pragma unroll
+          for (int c = 0; c < HK; ++c) {
+            s[c] = c < nvis ? s[c] * sl2 : -INFINITY;
+            mx = fmaxf(mx, s[c]);
           }
         }
-      }
-      tmem_st32(tbase + lane_base + P_COL + half * (HK / 2), pk);
-      asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
-      // the last tile's v_C rows past the last query's position may hold
-      // anything (rows no query of this tile may see): zero them in the stage
-      // before PV reads it (each warp a share of the rows; its p_full arrival
-      // below publishes them)
-      if (j == nk - 1 && qp_last - j * TK + 1 < TK) {
-        const int st = j % NVS;
-        ok = pair_all(quarter, __all_sync(0xffffffffu, wait_or_abort(&ctl.v_full[st], (j / NVS) & 1, ctl, a.status)));
-        if (!ok) break;
-        const int first = qp_last - j * TK + 1;   // rows first .. TK-1 of both v_C chunks
-        uint8_t* vbase = smem + VRING_OFF + st * VSTAGE;
-        const int tid = threadIdx.x - 96;
-        for (int w = tid; w < (TK - first) * 16; w += 256) {
-          const int row = first + w / 16, part = w % 16;   // 8 x 16 B per row and chunk
-          *reinterpret_cast<uint4*>(vbase + (part >> 3) * CHUNK + row * 128 + (part & 7) * 16) =
-              make_uint4(0, 0, 0, 0);
+        ctl.mx[g & 1][half][r] = mx;
+        pair_sync(quarter);
+        mx = fmaxf(mx, ctl.mx[g & 1][half ^ 1][r]);   // the row's tile maximum, the same in both halves
+        float alpha = 1.f;
+        if (mx > m_ref + RESCALE_THRESHOLD) {   // also the first tile a row sees anything (m_ref = -inf)
+          alpha = ex2_approx(m_ref - mx);
+          m_ref = mx;
         }
-        fence_proxy_async_smem();
+        uint32_t pk[HK / 2];
+        float lsum0 = 0.f, lsum1 = 0.f;   // the softmax sum from the unrounded weights
+        if (full) {
+          const float neg = -m_ref;
+#pragma unroll
+          for (int c = 0; c < HK; c += 2) {
+            const float p0 = ex2_approx(fmaf(s[c], sl2, neg)), p1 = ex2_approx(fmaf(s[c + 1], sl2, neg));
+            lsum0 += p0;
+            lsum1 += p1;
+            pk[c / 2] = pack_bf16(p0, p1);
+          }
+        } else {
+#pragma unroll
+          for (int c = 0; c < HK; c += 2) {
+            const float p0 = c < nvis ? ex2_approx(s[c] - m_ref) : 0.f;
+            const float p1 = c + 1 < nvis ? ex2_approx(s[c + 1] - m_ref) : 0.f;
+            lsum0 += p0;
+            lsum1 += p1;
+            pk[c / 2] = pack_bf16(p0, p1);
+          }
+        }
+        l = l * alpha + (lsum0 + lsum1);   // this half's share of the row sum
+        // P(g) replaces P(g-1) in TMEM and O is rescaled: both only after
+        // PV(g-1) (for an item's first tile, the previous item's epilogue
+        // already waited for its last PV)
+        if (j > 0) {
+          ok = pair_all(quarter, __all_sync(0xffffffffu, wait_or_abort(&ctl.pv_done, (g - 1) & 1, ctl, a.status)));
+          if (!ok) break;
+          tc_fence_after();
+          if (__any_sync(0xffffffffu, alpha != 1.f)) {
+#pragma unroll 1
+            for (int c = 0; c < DH / 2; c += 32) {
+              float v[32];
+              tmem_ld32(tbase + lane_base + O_COL + half * (DH / 2) + c, v);
+              tmem_ld_wait();
+              uint32_t w[32];
+#pragma unroll
+              for (int e = 0; e < 32; ++e) w[e] = __float_as_uint(v[e] * alpha);
+              tmem_st32(tbase + lane_base + O_COL + half * (DH / 2) + c, w);
+            }
+          }
+        }
+        tmem_st32(tbase + lane_base + P_COL + half * (HK / 2), pk);
+        asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
+        // the last tile's v_C rows past the last query's position may hold
+        // anything (rows no query of this tile may see): zero them in the stage
+        // before PV reads it (each warp a share of the rows; its p_full arrival
+        // below publishes them)
+        if (j == it.nk - 1 && it.qp_last - j * TK + 1 < TK) {
+          const int st = g % NVS;
+          ok = pair_all(quarter, __all_sync(0xffffffffu, wait_or_abort(&ctl.v_full[st], (g / NVS) & 1, ctl, a.status)));
+          if (!ok) break;
+          const int first = it.qp_last - j * TK + 1;   // rows first .. TK-1 of both v_C chunks
+          uint8_t* vbase = smem + VRING_OFF + st * VSTAGE;
+          const int tid = threadIdx.x - 96;
+          for (int w = tid; w < (TK - first) * 16; w += 256) {
+            const int row = first + w / 16, part = w % 16;   // 8 x 16 B per row and chunk
+            *reinterpret_cast<uint4*>(vbase + (part >> 3) * CHUNK + row * 128 + (part & 7) * 16) =
+                make_uint4(0, 0, 0, 0);
+          }
+          fence_proxy_async_smem();
+        }
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&ctl.p_full);
       }
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&ctl.p_full);
-    }
-    // ---------------------------------------------------------------- epilogue
-    if (ok) ok = pair_all(quarter, __all_sync(0xffffffffu, wait_or_abort(&ctl.pv_done, (nk - 1) & 1, ctl, a.status)));
-    if (ok) {
+      if (!ok) break;
+      // The next item's queries go into TMEM now, so that its first QK runs
+      // while this item's last PV and epilogue do.
+      ok = item_at(e + 1, k_next) && (k_next < 0 || move_queries(n));
+      if (ok && k_next >= 0) nxt = item_of(a, k_next, threadIdx.x == 96);   // its position is read during the epilogue
+      // ---------------------------------------------------------------- epilogue
+      if (ok) ok = pair_all(quarter, __all_sync(0xffffffffu, wait_or_abort(&ctl.pv_done, (g - 1) & 1, ctl, a.status)));
+      if (!ok) break;
       ctl.ls[half][r] = l;
       pair_sync(quarter);
       l += ctl.ls[half ^ 1][r];
       tc_fence_after();
       const float inv_l = l > 0.f ? 1.f / l : 0.f;
-      const bool store = r < nq;
-      __nv_bfloat16* orow = static_cast<__nv_bfloat16*>(a.o) + (((size_t)b * a.T + q0 + r) * a.n_h + head) * DH;
+      const bool store = r < it.nq;
+      __nv_bfloat16* orow =
+          static_cast<__nv_bfloat16*>(a.o) + (((size_t)it.b * a.T + it.q0 + r) * a.n_h + it.head) * DH;
 #pragma unroll 1
       for (int c = half * (DH / 2); c < (half + 1) * (DH / 2); c += 32) {
         float v[32];
@@ -412,7 +511,12 @@ __global__ void __launch_bounds__(NTHREADS, 1)
                            pack_bf16(v[e + 4] * inv_l, v[e + 5] * inv_l), pack_bf16(v[e + 6] * inv_l, v[e + 7] * inv_l));
         }
       }
-      if (store && half == 0) a.lse[((size_t)b * a.T + q0 + r) * a.n_h + head] = (m_ref + log2f(l)) * kLn2;
+      if (store && half == 0) a.lse[((size_t)it.b * a.T + it.q0 + r) * a.n_h + it.head] = (m_ref + log2f(l)) * kLn2;
+      // the O reads are done before this item's successor writes P (program
+      // order) and its first PV starts O afresh; the sums' exchange slots are
+      // rewritten only after the next pair_sync
+      tc_fence_before();
+      pair_sync(quarter);
     }
   }
 
@@ -422,6 +526,16 @@ __global__ void __launch_bounds__(NTHREADS, 1)
   __syncthreads();
   tc_fence_after();
   if (warp == 1) tmem_dealloc(tbase, TMEM_COLS);
+  // The last CTA to leave resets the launch's counters (every CTA has taken
+  // its last index by now) for the next launch that uses them.
+  if (threadIdx.x == 0) {
+    __threadfence();
+    if (atomicAdd(&g_cta_done[ctr], 1u) == gridDim.x - 1) {
+      atomicExch(&g_item_next[ctr], 0u);
+      atomicExch(&g_cta_done[ctr], 0u);
+      __threadfence();
+    }
+  }
 }
 
 }  // namespace
@@ -462,8 +576,21 @@ cudaError_t launch_mha_tc(const MhaArgs& a, cudaStream_t s) {
     if (e != cudaSuccess) return e;
     attr_set = true;
   }
-  LaunchCfg lc(dim3((unsigned)((a.T + TQ - 1) / TQ), (unsigned)a.n_h, (unsigned)a.B), dim3(NTHREADS), SMEM_DYN, s);
-  cudaError_t e = cudaLaunchKernelEx(&lc.cfg, mha_tc_kernel, map_q, map_k, map_v, map_kr, a);
+  // one CTA per SM (or per item, when there are fewer items)
+  static int sms = 0;
+  if (sms <= 0) {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || sms <= 0)
+      return cudaErrorInvalidValue;
+  }
+  const long long items = (long long)((a.T + TQ - 1) / TQ) * a.n_h * a.B;
+  if (items > 0x7fffffffLL) return cudaErrorInvalidValue;
+  LaunchCfg lc(dim3((unsigned)(items < sms ? items : sms)), dim3(NTHREADS), SMEM_DYN, s);
+  // each launch in a stream's flight uses counters of its own (slots rotate)
+  static std::atomic<unsigned int> next_ctr{0};
+  const int ctr = (int)(next_ctr.fetch_add(1u) % NCTR);
+  cudaError_t e = cudaLaunchKernelEx(&lc.cfg, mha_tc_kernel, map_q, map_k, map_v, map_kr, a, ctr);
   if (e != cudaSuccess) return e;
   return cudaGetLastError();
 }

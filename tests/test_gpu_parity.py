@@ -190,6 +190,30 @@ def test_decode_attn_any_chunk_count(name, chunks):
     dec.close()
 
 
+@pytest.mark.parametrize("B", [507, 508, 900])
+def test_decode_attn_many_short_sequences(B):
+    """Batches around and past the size whose split plan the few-head kernel
+    works out in its own shared memory (up to 507 sequences; larger batches
+    take the separate plan launch): short ragged sequences, some empty, against
+    the oracle."""
+    shp = S.workload("minimind")
+    max_len = 40
+    seqlens = np.random.default_rng(B).integers(0, max_len + 1, size=B)
+    seqlens[:3] = [0, 1, max_len]
+    q = S.draw_absorbed_queries(shp, B)
+    rows = [S.draw_latent_rows(shp, int(seqlens[b]), sub=b) for b in range(B)]
+    ref_o, ref_l = oracle_decode(shp, q, rows, seqlens)
+    got_o, got_l, st, bits, dec = run_decode(shp, q, rows, seqlens, max_len)
+    assert M.mla_get_decode_path(dec.handle) == M.MLA_DECODE_TCGEN05
+    assert M.mla_last_launch_count(dec.handle) == (2 if B <= 507 else 3)
+    assert st == M.MLA_OK and bits == 0
+    nz = seqlens > 0
+    assert_close(got_o[nz], ref_o[nz], shp.dtype, what="o_lat")
+    assert np.all(got_o[~nz] == 0) and np.all(np.isneginf(got_l[~nz]))
+    assert np.abs(got_l[nz] - ref_l[nz]).max() <= 2e-4 * max(1, np.abs(ref_l[nz]).max())
+    dec.close()
+
+
 @pytest.mark.parametrize("name", SMALL)
 @pytest.mark.parametrize("pattern", list(SEQLEN_PATTERNS))
 def test_decode_attn_matches_oracle(name, pattern):
