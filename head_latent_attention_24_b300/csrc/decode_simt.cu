@@ -224,22 +224,14 @@ __global__ void __launch_bounds__(NT) decode_simt_kernel(const DecodeArgs a) {
   }
 }
 
-// One CTA per (sequence, head): merges the partial results of a split sequence
-// and writes o_lat = 0, lse = -inf for an empty one.
-// One warp per (sequence, head): every lane reads the pieces' LSEs and its
-// columns of their fp32 partials with 16-byte loads (a warp reads 512
-// contiguous bytes per load), writing o_lat = sum_j e^{lse_j - lse} o_j.
+// Merges the partial results of split sequences and writes o_lat = 0,
+// lse = -inf for empty ones. One warp per (sequence, head): every lane reads
+// the pieces' LSEs and its columns of their fp32 partials with 16-byte loads
+// (a warp reads 512 contiguous bytes per load), writing
+// o_lat = sum_j e^{lse_j - lse} o_j.
 template <typename T>
-__global__ void __launch_bounds__(256) decode_combine_kernel(const DecodeArgs a) {
-  pdl_trigger();
-  pdl_wait();
-  const int b = blockIdx.x, warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int h = blockIdx.y * 8 + warp;
+__device__ __forceinline__ void combine_one(const DecodeArgs& a, const int32_t* cum, int b, int h, int lane) {
   const int B = a.B, d_c = a.d_c;
-  const int32_t* cum = a.plan;
-  // whole sequences and none empty: the attention kernel wrote everything
-  if (cum[B + 3] && !cum[B + 4]) return;
-  if (h >= a.n_h) return;
   const int chunk_len = cum[B + 1];
   const int s0 = cum[b], s1 = cum[b + 1];
   T* o_out = static_cast<T*>(a.o_lat) + ((long long)b * a.n_h + h) * d_c;
@@ -317,6 +309,25 @@ __global__ void __launch_bounds__(256) decode_combine_kernel(const DecodeArgs a)
   if (lane == 0) a.lse[(long long)b * a.n_h + h] = mx + logf(sum);
 }
 
+// The CTAs walk the (sequence, 8 heads) groups. When the plan may give every
+// sequence a chunk of its own (B <= chunks: usually whole sequences, nothing
+// to merge) the grid is at most one CTA per SM, so that the launch is over as
+// soon as its CTAs have read the plan; otherwise a CTA per group, so that the
+// merges run side by side.
+template <typename T>
+__global__ void __launch_bounds__(256) decode_combine_kernel(const DecodeArgs a) {
+  pdl_trigger();
+  pdl_wait();
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int32_t* cum = a.plan;
+  if (cum[a.B + 3] && !cum[a.B + 4]) return;
+  const int hg = (a.n_h + 7) / 8;
+  for (long long g = blockIdx.x; g < (long long)a.B * hg; g += gridDim.x) {
+    const int b = (int)(g / hg), h = (int)(g % hg) * 8 + warp;
+    if (h < a.n_h) combine_one<T>(a, cum, b, h, lane);
+  }
+}
+
 }  // namespace
 
 int decode_simt_chunks(const mla_handle_s* h) {
@@ -357,7 +368,17 @@ cudaError_t launch_decode_simt(const DecodeArgs& a, int dtype, cudaStream_t s, i
 }
 
 cudaError_t launch_decode_combine(const DecodeArgs& a, int dtype, cudaStream_t s) {
-  LaunchCfg lc(dim3(a.B, (a.n_h + 7) / 8), dim3(256), 0, s);
+  static int sms = 0;
+  if (sms <= 0) {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || sms <= 0)
+      return cudaErrorInvalidValue;
+  }
+  const long long groups = (long long)a.B * ((a.n_h + 7) / 8);
+  const long long grid = (a.allow_whole && a.B <= a.grid_chunks && groups > sms) ? sms : groups;
+  if (grid > 0x7fffffffLL) return cudaErrorInvalidValue;
+  LaunchCfg lc(dim3((unsigned)grid), dim3(256), 0, s);
   cudaError_t e = dtype == MLA_BF16 ? cudaLaunchKernelEx(&lc.cfg, decode_combine_kernel<__nv_bfloat16>, a)
                                     : cudaLaunchKernelEx(&lc.cfg, decode_combine_kernel<float>, a);
   if (e != cudaSuccess) return e;
