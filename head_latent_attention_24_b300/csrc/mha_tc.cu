@@ -6,11 +6,11 @@
 // with the RoPE key shared by the heads, §7 scale 1/sqrt(d_h + d_r)).
 //
 // One CTA per SM runs work items of 128 queries of one head of one sequence,
-// longest key ranges first. An item's query tile (128 x 192) is moved into
-// TMEM and is the A operand of every QK; key tiles of 128 rows stream through
-// two TMA rings, a two-stage one for k_C (128 x 128) with the shared k_R
-// (128 x 64, read straight from the cache rows), freed after the tile's QK,
-// and a three-stage one for v_C (128 x 128), freed after its PV. The next
+// taken at run time (Item, item_of below). An item's query tile (128 x 192)
+// is moved into TMEM and is the A operand of every QK; key tiles of 128 rows
+// stream through two TMA rings, a two-stage one for k_C (128 x 128) with the
+// shared k_R (128 x 64, read straight from the cache rows), freed after the
+// tile's QK, and a three-stage one for v_C (128 x 128), freed after its PV. The next
 // item's query tile comes through the key ring behind the current item's
 // keys and goes into TMEM as soon as the current item's last scores are read,
 // so its first QK runs during the current item's last PV and epilogue.
@@ -20,17 +20,17 @@
 //   O += P . V       M = 128 queries, N = 128 (d_h), K = 128 keys, A from TMEM
 // Each query row (a TMEM lane) belongs to two softmax threads, one per half of
 // the key tile; they exchange the row's tile maximum, the reference maximum
-// moves lazily (only when a tile's maximum rises
-// more than 8 above it, when the thread rescales its row of O in TMEM), and
+// moves lazily (only when a tile's maximum rises more than 8 above it, when
+// the thread rescales its row of O in TMEM), and
 // rows a query may not see (later positions) get P = 0; v_C rows past the last
 // query's position are zeroed in shared memory before PV reads them. The QK of
 // tile j+1 runs on the tensor core while the softmax works on tile j.
 //
 // Warp 0 issues TMA, warp 1 owns TMEM and issues the QK MMAs, warp 2 the PV
-// MMAs, warps 3-10 move the queries and run the softmax and the epilogue (two warps per query row,
-// each with half of the tile's keys). Every mbarrier wait is bounded;
-// on expiry the CTA records MLA_DEV_TIMEOUT, stops issuing work, waits
-// (bounded) for its own copies in flight and frees its TMEM.
+// MMAs, warps 3-10 move the queries and run the softmax and the epilogue (two
+// warps per query row, each with half of the tile's keys). Every mbarrier
+// wait is bounded; on expiry the CTA records MLA_DEV_TIMEOUT, stops issuing
+// work, waits (bounded) for its own copies in flight and frees its TMEM.
 #include <atomic>
 
 #include "internal.cuh"
