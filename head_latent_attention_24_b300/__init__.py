@@ -398,15 +398,21 @@ class MLADecoder:
         """Record one decode step as a CUDA graph: the step reads its inputs
         from the decoder's buffers h_in [B, d], pos_in [B] and seqlens_in [B]
         (copy each step's values into them) and works on `cache`; replay()
-        then runs the whole step with one launch from the host. The graph
-        keeps this cache's and these buffers' addresses and the kernels'
-        launch parameters, so it is valid while they stay allocated. Run at
-        least one eager step first (it sets the kernels' launch attributes)."""
+        then runs the whole step with one launch from the host. pos_in and
+        seqlens_in are rows 0 and 1 of ps_in [2, B4] (B4 = B rounded up to 4,
+        so that both rows start 16-byte aligned): one copy of a [2, B4] host
+        tensor fills both. The graph keeps this cache's and these buffers'
+        addresses and the kernels' launch parameters, so it is valid while
+        they stay allocated. Run at least one eager step first (it sets the
+        kernels' launch attributes)."""
         import torch
         dev = self.u.device
+        b4 = (self.batch + 3) // 4 * 4
         self.h_in = torch.zeros((self.batch, self.shape.d), dtype=self.torch_dtype, device=dev)
-        self.pos_in = torch.zeros(self.batch, dtype=torch.int32, device=dev)
-        self.seqlens_in = torch.ones(self.batch, dtype=torch.int32, device=dev)
+        self.ps_in = torch.zeros((2, b4), dtype=torch.int32, device=dev)
+        self.ps_in[1].fill_(1)
+        self.pos_in = self.ps_in[0, :self.batch]
+        self.seqlens_in = self.ps_in[1, :self.batch]
         torch.cuda.synchronize(dev)
         graph = torch.cuda.CUDAGraph()
         with torch.cuda.graph(graph):
