@@ -258,7 +258,12 @@ MLA_API mla_status_t mla_out_proj_premerged(mla_handle_t handle, const void* o_l
        q [batch, n_q, n_h, d_h + d_r], k_c / v_c [batch, max_len, n_h, d_h],
        cache [batch, max_len, d_c + d_r] (k_R read from its last d_r columns),
        o [batch, n_q, n_h, d_h] out (normalised), lse [batch, n_q, n_h] fp32 out
-       (natural log). d_h <= 128, else MLA_ERR_UNSUPPORTED.
+       (natural log). d_h <= 128, else MLA_ERR_UNSUPPORTED. The tensor-core
+       kernel (V2 head shape) hands out its work items through a device
+       counter of the library's, one of 64 that successive launches take in
+       turn and leave reset: at most 64 of its launches may be in flight at
+       once (across streams), and a captured graph holding one must not be
+       replayed on two streams at the same time.
    mla_project_out: u [n_tokens, d] = W_O o for o [n_tokens, n_h * d_h].
    All asynchronous on `stream`; the caller owns every buffer. */
 MLA_API mla_status_t mla_project_q(mla_handle_t handle, const void* x, int32_t n_tokens, const void* W_DQ,
