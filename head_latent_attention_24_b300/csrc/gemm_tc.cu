@@ -612,7 +612,11 @@ cudaError_t launch_gemm_tc(const TcGemm& g, int num_sms, cudaStream_t s) {
   }
   p.mtiles_total = p.mstart[3];
   p.N = g.N; p.K = g.K; p.Z = g.Z;
-  p.n_tile = g.N >= 256 ? 256 : ((g.N + 15) / 16) * 16;
+  // Activation tiles of up to 256 rows for decode-sized batches (one tile);
+  // with more tokens, tiles of 128 rows, whose fp32 partial tile leaves room
+  // for two CTAs per SM (one's epilogue runs beside the other's stream):
+  // measured 4-12 % faster on the MHA path's projections (8192 tokens).
+  p.n_tile = g.N > 256 ? 128 : (g.N >= 256 ? 256 : ((g.N + 15) / 16) * 16);
   const int kchunks = g.K / BK;
   const long long n_tiles = (g.N + p.n_tile - 1) / p.n_tile;
   if (n_tiles > 65535 || g.Z > 65535) return cudaErrorInvalidValue;
